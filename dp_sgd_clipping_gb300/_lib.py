@@ -1,0 +1,89 @@
+"""ctypes loader of libdpclip.so and the raw C-ABI (names as in include/dpclip.h).
+
+Loading needs no GPU; the library refuses to fall back to anything else: if
+the shared object is missing the import of this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+ERR_TIMEOUT = -5
+
+F32 = 0
+BF16 = 1
+
+EXACT_AUTO, EXACT_GHOST, EXACT_DIRECT = 0, 1, 2
+OP_NORMS_EXACT, OP_NORMS_HUTCH, OP_NORMS_HUTCHPP, OP_CLIPPED_NOISY_GRAD = 0, 1, 2, 3
+HUTCH_MAX_K = 32
+HUTCHPP_MAX_K = 48
+
+_c = ctypes
+_vp, _i, _u64, _u32, _i64, _f = _c.c_void_p, _c.c_int, _c.c_uint64, _c.c_uint32, _c.c_int64, _c.c_float
+_sz = _c.c_size_t
+
+# symbol -> (restype, argtypes)
+SIGNATURES = {
+    "dpclip_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, _i, _c.POINTER(_sz)]),
+    "dpclip_norms_exact": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "dpclip_norms_hutch": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp, _sz, _vp]),
+    "dpclip_norms_hutchpp": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp, _sz, _vp]),
+    "dpclip_clipped_noisy_grad": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _f, _u64, _u64,
+                                       _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dpclip_clip_scales": (_i, [_vp, _i, _f, _vp, _vp, _vp]),
+    "dpclip_philox_normal": (_i, [_vp, _i64, _i, _u64, _u32, _u64, _vp]),
+    "dpclip_workspace_status": (_i, [_vp, _vp]),
+    "dpclip_selftest_wait_timeout": (_i, [_vp, _sz, _i, _vp]),
+    "dpclip_status_string": (_c.c_char_p, [_i]),
+    "dpclip_version": (_c.c_char_p, []),
+}
+
+
+class DpclipError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def _load():
+    path = lib_path()
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libdpclip.so is not built ({path}); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.dpclip_status_string(status).decode()
+
+
+def check(fn: str, status: int) -> None:
+    if status != OK:
+        raise DpclipError(fn, status, status_string(status))
+
+
+def workspace_size(op: int, B: int, T: int, d: int, p: int, dtype: int, param: int) -> int:
+    n = _sz(0)
+    check("dpclip_workspace_size", lib.dpclip_workspace_size(op, B, T, d, p, dtype, param,
+                                                             ctypes.byref(n)))
+    return n.value

@@ -1,0 +1,127 @@
+"""Torch-facing wrappers of the C-ABI.
+
+Argument marshalling only: tensors are checked for device, dtype and
+contiguity, a workspace is taken from the PyTorch caching allocator (or the
+caller's), and the C entry point is called on the current CUDA stream.  Every
+step of the computation runs in libdpclip's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+__all__ = ["norms_exact", "norms_hutch", "norms_hutchpp", "clipped_noisy_grad", "clip_scales",
+           "philox_normal", "workspace_bytes", "workspace_status", "selftest_wait_timeout"]
+
+_DT = {torch.float32: L.F32, torch.bfloat16: L.BF16}
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_pair(A: torch.Tensor, G: torch.Tensor):
+    if not (A.is_cuda and G.is_cuda):
+        raise ValueError("A and G must be CUDA tensors")
+    if A.dtype != G.dtype or A.dtype not in _DT:
+        raise ValueError("A and G must both be float32 or both bfloat16")
+    if A.dim() != 3 or G.dim() != 3 or A.shape[:2] != G.shape[:2]:
+        raise ValueError("A must be [B, T, d] and G [B, T, p]")
+    if not (A.is_contiguous() and G.is_contiguous()):
+        raise ValueError("A and G must be contiguous")
+    B, T, d = A.shape
+    return B, T, d, G.shape[2], _DT[A.dtype]
+
+
+def workspace_bytes(op: int, B: int, T: int, d: int, p: int, dtype: int, param: int) -> int:
+    return L.workspace_size(op, B, T, d, p, dtype, param)
+
+
+def _workspace(nbytes: int, device, ws):
+    if ws is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if ws.numel() * ws.element_size() < nbytes:
+        raise ValueError(f"workspace too small: {ws.numel() * ws.element_size()} < {nbytes}")
+    return ws
+
+
+def norms_exact(A, G, method: int = L.EXACT_AUTO, out=None, ws=None, stream=None):
+    B, T, d, p, dt = _check_pair(A, G)
+    nb = workspace_bytes(L.OP_NORMS_EXACT, B, T, d, p, dt, method)
+    ws = _workspace(nb, A.device, ws)
+    out = torch.empty(B, dtype=torch.float32, device=A.device) if out is None else out
+    L.check("dpclip_norms_exact", L.lib.dpclip_norms_exact(
+        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, method, out.data_ptr(), ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return out
+
+
+def norms_hutch(A, G, k: int, seed: int, offset: int = 0, out=None, ws=None, stream=None):
+    B, T, d, p, dt = _check_pair(A, G)
+    nb = workspace_bytes(L.OP_NORMS_HUTCH, B, T, d, p, dt, k)
+    ws = _workspace(nb, A.device, ws)
+    out = torch.empty(B, dtype=torch.float32, device=A.device) if out is None else out
+    L.check("dpclip_norms_hutch", L.lib.dpclip_norms_hutch(
+        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, k, seed, offset, out.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    return out
+
+
+def norms_hutchpp(A, G, k: int, seed: int, offset: int = 0, out=None, ws=None, stream=None):
+    B, T, d, p, dt = _check_pair(A, G)
+    nb = workspace_bytes(L.OP_NORMS_HUTCHPP, B, T, d, p, dt, k)
+    ws = _workspace(nb, A.device, ws)
+    out = torch.empty(B, dtype=torch.float32, device=A.device) if out is None else out
+    L.check("dpclip_norms_hutchpp", L.lib.dpclip_norms_hutchpp(
+        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, k, seed, offset, out.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    return out
+
+
+def clipped_noisy_grad(A, G, sqnorms, C: float, sigma: float, seed: int, offset: int = 0,
+                       grad=None, scales=None, clipped=None, ws=None, stream=None,
+                       want_scales: bool = True):
+    """Returns (grad [d, p] fp32, scales [B] fp32, clipped [B] uint8)."""
+    B, T, d, p, dt = _check_pair(A, G)
+    if sqnorms.dtype != torch.float32 or sqnorms.numel() != B or not sqnorms.is_cuda:
+        raise ValueError("sqnorms must be a CUDA float32 tensor of B entries")
+    nb = workspace_bytes(L.OP_CLIPPED_NOISY_GRAD, B, T, d, p, dt, 0)
+    ws = _workspace(nb, A.device, ws)
+    grad = torch.empty(d, p, dtype=torch.float32, device=A.device) if grad is None else grad
+    if want_scales:
+        scales = torch.empty(B, dtype=torch.float32, device=A.device) if scales is None else scales
+        clipped = torch.empty(B, dtype=torch.uint8, device=A.device) if clipped is None else clipped
+    L.check("dpclip_clipped_noisy_grad", L.lib.dpclip_clipped_noisy_grad(
+        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, sqnorms.data_ptr(), float(C), float(sigma),
+        seed, offset, grad.data_ptr(), scales.data_ptr() if scales is not None else None,
+        clipped.data_ptr() if clipped is not None else None, ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return grad, scales, clipped
+
+
+def clip_scales(sqnorms, C: float, stream=None):
+    B = sqnorms.numel()
+    scales = torch.empty(B, dtype=torch.float32, device=sqnorms.device)
+    clipped = torch.empty(B, dtype=torch.uint8, device=sqnorms.device)
+    L.check("dpclip_clip_scales", L.lib.dpclip_clip_scales(
+        sqnorms.data_ptr(), B, float(C), scales.data_ptr(), clipped.data_ptr(), _stream(stream)))
+    return scales, clipped
+
+
+def philox_normal(n: int, seed: int, stream_id: int, offset: int = 0, dtype=torch.float32,
+                  device="cuda", stream=None):
+    out = torch.empty(n, dtype=dtype, device=device)
+    L.check("dpclip_philox_normal", L.lib.dpclip_philox_normal(
+        out.data_ptr(), n, _DT[dtype], seed, stream_id, offset, _stream(stream)))
+    return out
+
+
+def workspace_status(ws, stream=None) -> int:
+    return L.lib.dpclip_workspace_status(ws.data_ptr(), _stream(stream))
+
+
+def selftest_wait_timeout(ws, timeout_us: int, stream=None) -> None:
+    L.check("dpclip_selftest_wait_timeout", L.lib.dpclip_selftest_wait_timeout(
+        ws.data_ptr(), ws.numel() * ws.element_size(), timeout_us, _stream(stream)))

@@ -1,0 +1,140 @@
+// Small kernels of the clipping path: Philox probe fill, clip scales,
+// deterministic reduction of per-tile norm partials, gradient noise for the
+// fp32 path and the bounded-wait self-test.
+#include "common.cuh"
+
+namespace dpclip {
+namespace {
+
+// out (rows x cols, row-major) = normals of one Philox stream for the first
+// rows_valid rows (element e = j * cols + c uses Philox block e / 4, lane
+// e % 4), zeros below.  One thread per Philox block of four elements.
+template <bool kBf16>
+__global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
+                                   uint64_t seed, uint32_t stream_id, uint64_t offset) {
+  const int64_t nvalid = rows_valid * cols, ntotal = rows * cols;
+  const int64_t nblk = (ntotal + 3) / 4;
+  for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+    if (4 * b < nvalid) philox_normal4(seed, stream_id, offset, (uint32_t)b, z);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const int64_t e = 4 * b + l;
+      if (e >= ntotal) break;
+      const float v = e < nvalid ? z[l] : 0.f;
+      if (kBf16)
+        static_cast<__nv_bfloat16*>(out)[e] = __float2bfloat16_rn(v);
+      else
+        static_cast<float*>(out)[e] = v;
+    }
+  }
+}
+
+__global__ void clip_scales_kernel(const float* sq, int B, float C, float* scales, uint8_t* clipped) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B; i += gridDim.x * blockDim.x) {
+    const float q = sq[i];
+    if (scales) scales[i] = q > 0.f ? fminf(1.f, C / sqrtf(q)) : 1.f;
+    if (clipped) clipped[i] = (uint8_t)(sqrtf(fmaxf(q, 0.f)) > C);
+  }
+}
+
+// sq[i] = scale * sum over units u and slots w of part[(u*su + i*si)*nw + w];
+// one block per sample, fixed summation tree.
+__global__ void finalize_norms_kernel(const float* part, int nunits, long long su, long long si,
+                                      int nw, float scale, float* sq) {
+  __shared__ float red[32];
+  const int i = blockIdx.x;
+  const long long n = (long long)nunits * nw;
+  float acc = 0.f;
+  for (long long e = threadIdx.x; e < n; e += blockDim.x) {
+    const long long u = e / nw, w = e % nw;
+    acc += part[(u * su + (long long)i * si) * nw + w];
+  }
+  acc = warp_sum(acc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+    sq[i] = scale * s;
+  }
+}
+
+__global__ void noise_add_kernel(float* grad, long long n, float scale, uint64_t seed,
+                                 uint64_t offset) {
+  const long long nblk = (n + 3) / 4;
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblk;
+       b += (long long)gridDim.x * blockDim.x) {
+    float z[4];
+    philox_normal4(seed, 3u, offset, (uint32_t)b, z);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const long long e = 4 * b + l;
+      if (e < n) grad[e] = fmaf(scale, z[l], grad[e]);
+    }
+  }
+}
+
+// Waits on a barrier that nothing completes; the bounded wait gives up after
+// limit_ns, records DPCLIP_ERR_TIMEOUT and the kernel returns normally.
+__global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtx wc{&abort_flag, err, limit_ns};
+    mbar_wait(&bar, 0, wc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid, bool bf16,
+                               uint64_t seed, uint32_t stream_id, uint64_t offset, cudaStream_t s) {
+  const int64_t nblk = (rows * cols + 3) / 4;
+  const int threads = 256;
+  const int grid = (int)std::min<int64_t>((nblk + threads - 1) / threads, 152 * 16);
+  if (grid <= 0) return cudaSuccess;
+  if (bf16)
+    philox_fill_kernel<true><<<grid, threads, 0, s>>>(out, rows, cols, rows_valid, seed, stream_id, offset);
+  else
+    philox_fill_kernel<false><<<grid, threads, 0, s>>>(out, rows, cols, rows_valid, seed, stream_id, offset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
+                               cudaStream_t s) {
+  const int threads = 256;
+  const int grid = std::min((B + threads - 1) / threads, 1024);
+  clip_scales_kernel<<<grid, threads, 0, s>>>(sq, B, C, scales, clipped);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long long su, long long si,
+                                  int nw, float scale, float* sq, cudaStream_t s) {
+  finalize_norms_kernel<<<B, 256, 0, s>>>(part, nunits, su, si, nw, scale, sq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_noise_add(float* grad, long long n, float scale, uint64_t seed, uint64_t offset,
+                             cudaStream_t s) {
+  const long long nblk = (n + 3) / 4;
+  const int threads = 256;
+  const int grid = (int)std::min<long long>((nblk + threads - 1) / threads, 152 * 16);
+  if (grid <= 0) return cudaSuccess;
+  noise_add_kernel<<<grid, threads, 0, s>>>(grad, n, scale, seed, offset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace dpclip

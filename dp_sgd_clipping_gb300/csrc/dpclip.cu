@@ -1,0 +1,785 @@
+// C-ABI of libdpclip: argument checks, workspace layout, TMA tensor maps and
+// the launch sequence of each entry point on the caller's stream.
+//
+// Entry points and the passages they implement (randomized-clipping summary
+// = "Technical summary: efficient DP-SGD for LLMs with randomized clipping",
+// gist.science; glossary = "DP-SGD" entry of jisaku.com):
+//   dpclip_norms_exact         trace identity, "Core mechanism"; ghost and
+//                              direct forms of "Problem definition"
+//   dpclip_norms_hutch         "Core mechanism", item 1
+//   dpclip_norms_hutchpp       "Core mechanism", item 2
+//   dpclip_clipped_noisy_grad  glossary "DP-SGD algorithm" steps 3-4;
+//                              "Algorithmic flow" steps 4-5
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace dpclip {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kTargetCtas = 304;      // two resident CTAs on each of 152 SMs
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Carves named regions out of the workspace; offsets are 256-byte aligned.
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = align_up(off, kAlign);
+    off = o + bytes;
+    return o;
+  }
+  size_t total() const { return align_up(off, kAlign); }
+};
+
+// K-split factor of a skinny GEMM: enough CTAs to keep ~two per SM resident,
+// at least 4 K-blocks per split, no empty split.
+void choose_splits(int ntiles, int kblocks, int& splits, int& per) {
+  int s = std::max(1, kTargetCtas / std::max(1, ntiles));
+  s = std::min(s, std::max(1, kblocks / 4));
+  per = cdiv(kblocks, s);
+  splits = cdiv(kblocks, per);
+}
+
+// ------------------------------------------------------------------ TMA maps
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeFn) nullptr;
+    return reinterpret_cast<EncodeFn>(p);
+  }();
+  return fn;
+}
+
+// bf16 tensor [n2][n1][n0] (n0 innermost), box {b0, b1, 1}, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap* map, const void* base, long long n0, long long n1, long long n2, int b0,
+              int b1) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)n0, (cuuint64_t)n1, (cuuint64_t)n2};
+  const cuuint64_t strides[2] = {(cuuint64_t)n0 * 2, (cuuint64_t)n0 * n1 * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ checks
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shapes(const void* A, const void* G, int B, int T, int d, int p, int dtype) {
+  if (!A || !G) return DPCLIP_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
+  if ((long long)d * p > (1ll << 34)) return DPCLIP_ERR_UNSUPPORTED;   // Philox block index
+  if ((long long)B * T > (1ll << 30)) return DPCLIP_ERR_UNSUPPORTED;
+  if (dtype == DPCLIP_BF16) {
+    if (d % 8 || p % 8) return DPCLIP_ERR_UNSUPPORTED;   // 16-byte TMA row strides
+    if (!aligned(A, 16) || !aligned(G, 16)) return DPCLIP_ERR_UNSUPPORTED;
+  } else {
+    if (!aligned(A, 4) || !aligned(G, 4)) return DPCLIP_ERR_UNSUPPORTED;
+  }
+  return DPCLIP_OK;
+}
+
+int check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return DPCLIP_ERR_WORKSPACE;
+  if (!aligned(ws, kAlign)) return DPCLIP_ERR_WORKSPACE;
+  if (ws_bytes < need) return DPCLIP_ERR_WORKSPACE;
+  return DPCLIP_OK;
+}
+
+int resolve_exact(int method, int T, int d, int p) {
+  if (method == DPCLIP_EXACT_AUTO) {
+    const double ghost = (double)T * T * (d + p);   // upper triangle of two T x T Grams
+    const double direct = 2.0 * T * d * p;
+    return direct < ghost ? DPCLIP_EXACT_DIRECT : DPCLIP_EXACT_GHOST;
+  }
+  return method;
+}
+
+// ------------------------------------------------------------------ plans
+// Every workspace starts with a control block: word 0 = device error code,
+// then the integer tickets of the split reductions.  It is cleared at the
+// start of each call.
+struct Plan {
+  size_t total = 0;
+  size_t ctrl = 0, ctrl_bytes = 0;
+  size_t off[16] = {};
+  // skinny-GEMM geometry
+  int mtiles = 0, Tp = 0, tblocks = 0;
+};
+
+enum {
+  kP = 0, kYhi, kYlo, kPart, kPart2, kQpart,                 // hutch
+  kS = 0, kGp, kY1hi, kY1lo, kZ1hi, kZ1lo, kUhi, kUlo,       // hutch++ ...
+  kV, kQWhi, kQWlo, kY3hi, kY3lo, kQ1, kHPart, kHQpart,
+};
+
+int np_for(int n) { return n <= 16 ? 16 : 32; }
+
+Plan plan_hutch_bf16(int B, int T, int d, int p, int k) {
+  Plan pl;
+  const int NP = np_for(k);
+  pl.mtiles = cdiv(T, kTokTileM);
+  pl.Tp = pl.mtiles * kTokTileM;
+  pl.tblocks = cdiv(T, kBlockK);
+  int s1, per1, s2, per2;
+  choose_splits(B * pl.mtiles, cdiv(p, kBlockK), s1, per1);
+  const int ftiles = cdiv(d, kFeatTileM);
+  choose_splits(B * ftiles, pl.tblocks, s2, per2);
+  Carve c;
+  const size_t ncnt = std::max<size_t>((size_t)B * pl.mtiles, (size_t)B * ftiles + B);
+  pl.ctrl_bytes = align_up(4 * (1 + ncnt), kAlign);
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  pl.off[kP] = c.take((size_t)NP * p * 2);
+  pl.off[kYhi] = c.take((size_t)B * NP * pl.Tp * 2);
+  pl.off[kYlo] = c.take((size_t)B * NP * pl.Tp * 2);
+  pl.off[kPart] = c.take(s1 > 1 ? (size_t)s1 * B * NP * pl.Tp * 4 : 0);
+  pl.off[kPart2] = c.take(s2 > 1 ? (size_t)s2 * B * NP * ftiles * kFeatTileM * 4 : 0);
+  pl.off[kQpart] = c.take((size_t)B * ftiles * 4);
+  pl.total = c.total();
+  return pl;
+}
+
+Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
+  Plan pl;
+  const int r = k / 3, m = k - 2 * r;
+  (void)m;
+  pl.mtiles = cdiv(T, kTokTileM);
+  pl.Tp = pl.mtiles * kTokTileM;
+  pl.tblocks = cdiv(T, kBlockK);
+  const int fd = cdiv(d, kFeatTileM), fp = cdiv(p, kFeatTileM);
+  size_t part = 0;
+  for (int F : {p, d}) {   // tok_gemm over features F (NP up to 32)
+    int s, per;
+    choose_splits(B * pl.mtiles, cdiv(F, kBlockK), s, per);
+    if (s > 1) part = std::max(part, (size_t)s * B * 32 * pl.Tp * 4);
+  }
+  for (int ft : {fd, fp}) {  // feat_gemm over tokens
+    int s, per;
+    choose_splits(B * ft, pl.tblocks, s, per);
+    if (s > 1) part = std::max(part, (size_t)s * B * 32 * ft * kFeatTileM * 4);
+  }
+  Carve c;
+  const size_t ncnt =
+      std::max<size_t>((size_t)B * pl.mtiles, (size_t)B * std::max(fd, fp) + B);
+  pl.ctrl_bytes = align_up(4 * (1 + ncnt), kAlign);
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  pl.off[kS] = c.take((size_t)16 * p * 2);
+  pl.off[kGp] = c.take((size_t)32 * p * 2);
+  pl.off[kY1hi] = c.take((size_t)B * 16 * pl.Tp * 2);
+  pl.off[kY1lo] = c.take((size_t)B * 16 * pl.Tp * 2);
+  pl.off[kZ1hi] = c.take((size_t)B * 16 * d * 2);
+  pl.off[kZ1lo] = c.take((size_t)B * 16 * d * 2);
+  pl.off[kUhi] = c.take((size_t)B * 16 * pl.Tp * 2);
+  pl.off[kUlo] = c.take((size_t)B * 16 * pl.Tp * 2);
+  pl.off[kV] = c.take((size_t)B * 16 * p * 4);
+  pl.off[kQWhi] = c.take((size_t)B * 32 * p * 2);
+  pl.off[kQWlo] = c.take((size_t)B * 32 * p * 2);
+  pl.off[kY3hi] = c.take((size_t)B * 32 * pl.Tp * 2);
+  pl.off[kY3lo] = c.take((size_t)B * 32 * pl.Tp * 2);
+  pl.off[kQ1] = c.take((size_t)B * r * p * 8);
+  pl.off[kHPart] = c.take(part);
+  pl.off[kHQpart] = c.take((size_t)B * std::max(fd, fp) * 4);
+  pl.total = c.total();
+  return pl;
+}
+
+int dp_ntiles(int d, int p) { return cdiv(d, kDpTileM) * cdiv(p, kDpTileN); }
+int ghost_npairs(int T) {
+  const int n = cdiv(T, kGhostTile);
+  return n * (n + 1) / 2;
+}
+
+Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
+  Plan pl;
+  Carve c;
+  pl.ctrl_bytes = kAlign;
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  const size_t units = method == DPCLIP_EXACT_DIRECT ? (size_t)dp_ntiles(d, p) * B
+                                                     : (size_t)ghost_npairs(T) * B;
+  pl.off[0] = c.take(units * kEpiWarps * 4);
+  pl.total = c.total();
+  return pl;
+}
+
+// fp32 plans
+enum { kFP = 0, kFY, kFPart, kFS, kFGp, kFY1, kFZ1, kFU, kFV, kFQW, kFQ1, kFY3, kFW };
+
+Plan plan_hutch_f32(int B, int T, int d, int p, int k) {
+  Plan pl;
+  Carve c;
+  pl.ctrl_bytes = kAlign;
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  pl.off[kFP] = c.take((size_t)k * p * 4);
+  pl.off[kFY] = c.take((size_t)B * T * k * 4);
+  pl.off[kFPart] = c.take((size_t)B * simt_nblocks(d, k) * 4);
+  pl.total = c.total();
+  return pl;
+}
+
+Plan plan_hutchpp_f32(int B, int T, int d, int p, int k) {
+  Plan pl;
+  const int r = k / 3, m = k - 2 * r;
+  Carve c;
+  pl.ctrl_bytes = kAlign;
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  pl.off[kFS] = c.take((size_t)r * p * 4);
+  pl.off[kFGp] = c.take((size_t)m * p * 4);
+  pl.off[kFY1] = c.take((size_t)B * T * r * 4);
+  pl.off[kFZ1] = c.take((size_t)B * d * r * 4);
+  pl.off[kFU] = c.take((size_t)B * T * r * 4);
+  pl.off[kFV] = c.take((size_t)B * 16 * p * 4);
+  pl.off[kFQW] = c.take((size_t)B * 32 * p * 4);
+  pl.off[kFQ1] = c.take((size_t)B * r * p * 8);
+  pl.off[kFY3] = c.take((size_t)B * T * (r + m) * 4);
+  pl.off[kFPart] = c.take((size_t)B * simt_nblocks(d, r + m) * 4);
+  pl.total = c.total();
+  return pl;
+}
+
+Plan plan_exact_f32(int B, int T, int d, int p, int method) {
+  Plan pl;
+  Carve c;
+  pl.ctrl_bytes = kAlign;
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  if (method == DPCLIP_EXACT_DIRECT) {
+    pl.off[kFPart] = c.take((size_t)B * simt_nblocks(d, p) * 4);
+  } else {
+    pl.off[kFW] = c.take((size_t)B * T * T * 4);
+    pl.off[kFPart] = c.take((size_t)B * simt_nblocks(T, T) * 4);
+  }
+  pl.total = c.total();
+  return pl;
+}
+
+Plan plan_grad() {
+  Plan pl;
+  Carve c;
+  pl.ctrl_bytes = kAlign;
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  pl.total = c.total();
+  return pl;
+}
+
+int hutch_k_ok(int k) { return k >= 1 && k <= DPCLIP_HUTCH_MAX_K; }
+int hutchpp_k_ok(int k) { return k >= 3 && k <= DPCLIP_HUTCHPP_MAX_K && (k - k / 3) <= kMaxNP; }
+
+int plan_for(int op, int B, int T, int d, int p, int dtype, int param, Plan& pl) {
+  switch (op) {
+    case DPCLIP_OP_NORMS_EXACT: {
+      if (param < DPCLIP_EXACT_AUTO || param > DPCLIP_EXACT_DIRECT) return DPCLIP_ERR_INVALID_ARG;
+      const int m = resolve_exact(param, T, d, p);
+      pl = dtype == DPCLIP_BF16 ? plan_exact_bf16(B, T, d, p, m) : plan_exact_f32(B, T, d, p, m);
+      return DPCLIP_OK;
+    }
+    case DPCLIP_OP_NORMS_HUTCH:
+      if (!hutch_k_ok(param)) return DPCLIP_ERR_UNSUPPORTED;
+      pl = dtype == DPCLIP_BF16 ? plan_hutch_bf16(B, T, d, p, param) : plan_hutch_f32(B, T, d, p, param);
+      return DPCLIP_OK;
+    case DPCLIP_OP_NORMS_HUTCHPP:
+      if (!hutchpp_k_ok(param)) return DPCLIP_ERR_UNSUPPORTED;
+      pl = dtype == DPCLIP_BF16 ? plan_hutchpp_bf16(B, T, d, p, param)
+                                : plan_hutchpp_f32(B, T, d, p, param);
+      return DPCLIP_OK;
+    case DPCLIP_OP_CLIPPED_NOISY_GRAD:
+      pl = plan_grad();
+      return DPCLIP_OK;
+    default:
+      return DPCLIP_ERR_INVALID_ARG;
+  }
+}
+
+#define DPCLIP_CUDA(call)                        \
+  do {                                           \
+    if ((call) != cudaSuccess) {                 \
+      (void)cudaGetLastError();                  \
+      return DPCLIP_ERR_CUDA;                    \
+    }                                            \
+  } while (0)
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ------------------------------------------------------------------ skinny launches
+int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo, int NP,
+            bool per_sample, const Plan& pl, void* ws, size_t part_off, void* out_hi, void* out_lo,
+            cudaStream_t s) {
+  TokGemmParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  const int Bw = per_sample ? B : 1;
+  if (!make_map(&tp.map_x, X, F, T, B, kBlockK, kTokTileM)) return DPCLIP_ERR_UNSUPPORTED;
+  if (!make_map(&tp.map_whi, Whi, F, NP, Bw, kBlockK, NP)) return DPCLIP_ERR_UNSUPPORTED;
+  if (Wlo) {
+    if (!make_map(&tp.map_wlo, Wlo, F, NP, Bw, kBlockK, NP)) return DPCLIP_ERR_UNSUPPORTED;
+  } else {
+    tp.map_wlo = tp.map_whi;
+  }
+  tp.B = B;
+  tp.T = T;
+  tp.F = F;
+  tp.NP = NP;
+  tp.w_per_sample = per_sample ? 1 : 0;
+  tp.has_lo = Wlo ? 1 : 0;
+  tp.mtiles = pl.mtiles;
+  tp.kblocks = cdiv(F, kBlockK);
+  choose_splits(B * pl.mtiles, tp.kblocks, tp.splits, tp.kb_per_split);
+  tp.Tp = pl.Tp;
+  tp.out_hi = static_cast<__nv_bfloat16*>(out_hi);
+  tp.out_lo = static_cast<__nv_bfloat16*>(out_lo);
+  tp.part = at<float>(ws, part_off);
+  tp.counters = at<uint32_t>(ws, pl.ctrl + 4);
+  tp.err = at<uint32_t>(ws, pl.ctrl);
+  DPCLIP_CUDA(launch_tok_gemm(tp, s));
+  return DPCLIP_OK;
+}
+
+int run_feat(const void* X, int B, int T, int F, const void* Yhi, const void* Ylo, int NP, int mode,
+             const float* w, const Plan& pl, void* ws, size_t part_off, size_t qpart_off,
+             float* out_f32, void* out_hi, void* out_lo, float* sq, cudaStream_t s) {
+  FeatGemmParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  if (!make_map(&fp.map_x, X, F, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
+  if (!make_map(&fp.map_yhi, Yhi, pl.Tp, NP, B, kBlockK, NP)) return DPCLIP_ERR_UNSUPPORTED;
+  if (!make_map(&fp.map_ylo, Ylo, pl.Tp, NP, B, kBlockK, NP)) return DPCLIP_ERR_UNSUPPORTED;
+  fp.B = B;
+  fp.T = T;
+  fp.F = F;
+  fp.NP = NP;
+  fp.Tp = pl.Tp;
+  fp.ftiles = cdiv(F, kFeatTileM);
+  fp.Fp = fp.ftiles * kFeatTileM;
+  fp.tblocks = pl.tblocks;
+  choose_splits(B * fp.ftiles, fp.tblocks, fp.splits, fp.tb_per_split);
+  for (int j = 0; j < kMaxNP; ++j) fp.w[j] = w ? w[j] : 0.f;
+  fp.out_f32 = out_f32;
+  fp.out_hi = static_cast<__nv_bfloat16*>(out_hi);
+  fp.out_lo = static_cast<__nv_bfloat16*>(out_lo);
+  fp.sq = sq;
+  fp.part = at<float>(ws, part_off);
+  fp.qpart = at<float>(ws, qpart_off);
+  fp.counters = at<uint32_t>(ws, pl.ctrl + 4);
+  fp.err = at<uint32_t>(ws, pl.ctrl);
+  DPCLIP_CUDA(launch_feat_gemm(fp, mode, s));
+  return DPCLIP_OK;
+}
+
+SimtParams simt_base() {
+  SimtParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  for (int j = 0; j < 64; ++j) sp.w[j] = 1.f;
+  return sp;
+}
+
+#define DPCLIP_TRY(expr)           \
+  do {                             \
+    const int st_ = (expr);        \
+    if (st_ != DPCLIP_OK) return st_; \
+  } while (0)
+
+}  // namespace
+}  // namespace dpclip
+
+using namespace dpclip;
+
+extern "C" {
+
+const char* dpclip_version(void) { return "dpclip 0.1 (sm_103a)"; }
+
+const char* dpclip_status_string(int status) {
+  switch (status) {
+    case DPCLIP_OK: return "ok";
+    case DPCLIP_ERR_INVALID_ARG: return "invalid argument";
+    case DPCLIP_ERR_UNSUPPORTED: return "unsupported shape, alignment or parameter";
+    case DPCLIP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DPCLIP_ERR_CUDA: return "CUDA error";
+    case DPCLIP_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int dpclip_workspace_size(int op, int B, int T, int d, int p, int dtype, int param, size_t* bytes) {
+  if (!bytes) return DPCLIP_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
+  Plan pl;
+  DPCLIP_TRY(plan_for(op, B, T, d, p, dtype, param, pl));
+  *bytes = pl.total;
+  return DPCLIP_OK;
+}
+
+int dpclip_philox_normal(void* out, int64_t n, int dtype, uint64_t seed, uint32_t stream_id,
+                         uint64_t offset, dpclip_stream_t stream) {
+  if (!out || n < 0) return DPCLIP_ERR_INVALID_ARG;
+  if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
+  if (!aligned(out, 4)) return DPCLIP_ERR_UNSUPPORTED;
+  if (n > (int64_t)4 * 0xFFFFFFFFll) return DPCLIP_ERR_UNSUPPORTED;
+  if (n == 0) return DPCLIP_OK;
+  DPCLIP_CUDA(launch_philox_fill(out, 1, n, 1, dtype == DPCLIP_BF16, seed, stream_id, offset,
+                                 (cudaStream_t)stream));
+  return DPCLIP_OK;
+}
+
+int dpclip_clip_scales(const float* sqnorms, int B, float C, float* scales, uint8_t* clipped,
+                       dpclip_stream_t stream) {
+  if (!sqnorms || B <= 0) return DPCLIP_ERR_INVALID_ARG;
+  if (!(C > 0.f) || !std::isfinite(C)) return DPCLIP_ERR_INVALID_ARG;
+  if (!scales && !clipped) return DPCLIP_OK;
+  DPCLIP_CUDA(launch_clip_scales(sqnorms, B, C, scales, clipped, (cudaStream_t)stream));
+  return DPCLIP_OK;
+}
+
+int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                       int method, float* sqnorms, void* ws, size_t ws_bytes,
+                       dpclip_stream_t stream) {
+  DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
+  if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
+  Plan pl;
+  DPCLIP_TRY(plan_for(DPCLIP_OP_NORMS_EXACT, B, T, d, p, dtype, method, pl));
+  DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
+  const int m = resolve_exact(method, T, d, p);
+  cudaStream_t s = (cudaStream_t)stream;
+  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  if (dtype == DPCLIP_BF16) {
+    if (m == DPCLIP_EXACT_DIRECT) {
+      GemmDpParams gp;
+      std::memset(&gp, 0, sizeof(gp));
+      if (!make_map(&gp.map_a, A, d, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
+      if (!make_map(&gp.map_g, G, p, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
+      gp.B = B;
+      gp.T = T;
+      gp.d = d;
+      gp.p = p;
+      gp.mtiles = cdiv(d, kDpTileM);
+      gp.ntiles = cdiv(p, kDpTileN);
+      gp.tblocks = cdiv(T, kBlockK);
+      gp.part = at<float>(ws, pl.off[0]);
+      gp.err = at<uint32_t>(ws, pl.ctrl);
+      const int ntiles = gp.mtiles * gp.ntiles;
+      DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min(ntiles, num_sms()), s));
+      DPCLIP_CUDA(launch_finalize_norms(gp.part, B, ntiles, B, 1, kEpiWarps, 1.f, sqnorms, s));
+    } else {
+      GhostParams gh;
+      std::memset(&gh, 0, sizeof(gh));
+      if (!make_map(&gh.map_a, A, d, T, B, kBlockK, kGhostTile)) return DPCLIP_ERR_UNSUPPORTED;
+      if (!make_map(&gh.map_g, G, p, T, B, kBlockK, kGhostTile)) return DPCLIP_ERR_UNSUPPORTED;
+      gh.B = B;
+      gh.T = T;
+      gh.d = d;
+      gh.p = p;
+      gh.ntt = cdiv(T, kGhostTile);
+      gh.npairs = ghost_npairs(T);
+      gh.dblocks = cdiv(d, kBlockK);
+      gh.pblocks = cdiv(p, kBlockK);
+      gh.part = at<float>(ws, pl.off[0]);
+      gh.err = at<uint32_t>(ws, pl.ctrl);
+      DPCLIP_CUDA(launch_ghost(gh, std::min(B * gh.npairs, num_sms()), s));
+      DPCLIP_CUDA(launch_finalize_norms(gh.part, B, gh.npairs, 1, gh.npairs, kEpiWarps, 1.f,
+                                        sqnorms, s));
+    }
+    return DPCLIP_OK;
+  }
+  // fp32
+  const float* Af = static_cast<const float*>(A);
+  const float* Gf = static_cast<const float*>(G);
+  SimtParams sp = simt_base();
+  int nb = 0;
+  if (m == DPCLIP_EXACT_DIRECT) {
+    sp.X = Af; sp.xb = (long long)T * d; sp.xm = 1; sp.xk = d;     // A_i^T : (f, t)
+    sp.Y = Gf; sp.yb = (long long)T * p; sp.yk = p; sp.yn = 1;     // G_i   : (t, c)
+    sp.batch = B; sp.M = d; sp.N = p; sp.K = T;
+    sp.part = at<float>(ws, pl.off[kFPart]);
+    DPCLIP_CUDA(launch_simt(sp, kSimtSqNorm, s, &nb));
+  } else {
+    float* W = at<float>(ws, pl.off[kFW]);
+    sp.X = Af; sp.xb = (long long)T * d; sp.xm = d; sp.xk = 1;     // A_i   : (t, f)
+    sp.Y = Af; sp.yb = (long long)T * d; sp.yk = 1; sp.yn = d;     // A_i^T : (f, t2)
+    sp.batch = B; sp.M = T; sp.N = T; sp.K = d;
+    sp.out = W; sp.ob = (long long)T * T; sp.om = T; sp.on = 1;
+    DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+    sp.X = Gf; sp.xb = (long long)T * p; sp.xm = p; sp.xk = 1;
+    sp.Y = Gf; sp.yb = (long long)T * p; sp.yk = 1; sp.yn = p;
+    sp.K = p;
+    sp.part = at<float>(ws, pl.off[kFPart]);
+    DPCLIP_CUDA(launch_simt(sp, kSimtDotWith, s, &nb));
+  }
+  DPCLIP_CUDA(launch_finalize_norms(sp.part, B, nb, 1, nb, 1, 1.f, sqnorms, s));
+  return DPCLIP_OK;
+}
+
+int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p, int dtype, int k,
+                       uint64_t seed, uint64_t offset, float* sqnorms, void* ws, size_t ws_bytes,
+                       dpclip_stream_t stream) {
+  DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
+  if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
+  Plan pl;
+  DPCLIP_TRY(plan_for(DPCLIP_OP_NORMS_HUTCH, B, T, d, p, dtype, k, pl));
+  DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
+  cudaStream_t s = (cudaStream_t)stream;
+  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  if (dtype == DPCLIP_BF16) {
+    const int NP = np_for(k);
+    void* P = at<void>(ws, pl.off[kP]);
+    DPCLIP_CUDA(launch_philox_fill(P, NP, p, k, true, seed, 0u, offset, s));
+    void* Yhi = at<void>(ws, pl.off[kYhi]);
+    void* Ylo = at<void>(ws, pl.off[kYlo]);
+    DPCLIP_TRY(run_tok(G, B, T, p, P, nullptr, NP, false, pl, ws, pl.off[kPart], Yhi, Ylo, s));
+    float w[kMaxNP];
+    for (int j = 0; j < kMaxNP; ++j) w[j] = j < k ? 1.f / (float)k : 0.f;
+    DPCLIP_TRY(run_feat(A, B, T, d, Yhi, Ylo, NP, kFeatSqNorm, w, pl, ws, pl.off[kPart2],
+                        pl.off[kQpart], nullptr, nullptr, nullptr, sqnorms, s));
+    return DPCLIP_OK;
+  }
+  const float* Af = static_cast<const float*>(A);
+  const float* Gf = static_cast<const float*>(G);
+  float* P = at<float>(ws, pl.off[kFP]);
+  float* Y = at<float>(ws, pl.off[kFY]);
+  DPCLIP_CUDA(launch_philox_fill(P, k, p, k, false, seed, 0u, offset, s));
+  SimtParams sp = simt_base();
+  int nb = 0;
+  sp.X = Gf; sp.xb = (long long)T * p; sp.xm = p; sp.xk = 1;        // G_i : (t, c)
+  sp.Y = P; sp.yb = 0; sp.yk = 1; sp.yn = p;                         // P   : (c, j)
+  sp.batch = B; sp.M = T; sp.N = k; sp.K = p;
+  sp.out = Y; sp.ob = (long long)T * k; sp.om = k; sp.on = 1;
+  DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+  sp = simt_base();
+  sp.X = Af; sp.xb = (long long)T * d; sp.xm = 1; sp.xk = d;         // A_i^T : (f, t)
+  sp.Y = Y; sp.yb = (long long)T * k; sp.yk = k; sp.yn = 1;          // Y_i   : (t, j)
+  sp.batch = B; sp.M = d; sp.N = k; sp.K = T;
+  sp.part = at<float>(ws, pl.off[kFPart]);
+  DPCLIP_CUDA(launch_simt(sp, kSimtSqNorm, s, &nb));
+  DPCLIP_CUDA(launch_finalize_norms(sp.part, B, nb, 1, nb, 1, 1.f / (float)k, sqnorms, s));
+  return DPCLIP_OK;
+}
+
+int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int p, int dtype, int k,
+                         uint64_t seed, uint64_t offset, float* sqnorms, void* ws, size_t ws_bytes,
+                         dpclip_stream_t stream) {
+  DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
+  if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
+  Plan pl;
+  DPCLIP_TRY(plan_for(DPCLIP_OP_NORMS_HUTCHPP, B, T, d, p, dtype, k, pl));
+  DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
+  const int r = k / 3, m = k - 2 * r;
+  cudaStream_t s = (cudaStream_t)stream;
+  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  float w[kMaxNP];
+  for (int j = 0; j < kMaxNP; ++j) w[j] = j < r ? 1.f : (j < r + m ? 1.f / (float)m : 0.f);
+  if (dtype == DPCLIP_BF16) {
+    void* S = at<void>(ws, pl.off[kS]);
+    void* Gp = at<void>(ws, pl.off[kGp]);
+    DPCLIP_CUDA(launch_philox_fill(S, 16, p, r, true, seed, 1u, offset, s));
+    DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, true, seed, 2u, offset, s));
+    void *Y1h = at<void>(ws, pl.off[kY1hi]), *Y1l = at<void>(ws, pl.off[kY1lo]);
+    void *Z1h = at<void>(ws, pl.off[kZ1hi]), *Z1l = at<void>(ws, pl.off[kZ1lo]);
+    void *Uh = at<void>(ws, pl.off[kUhi]), *Ul = at<void>(ws, pl.off[kUlo]);
+    float* V = at<float>(ws, pl.off[kV]);
+    void *QWh = at<void>(ws, pl.off[kQWhi]), *QWl = at<void>(ws, pl.off[kQWlo]);
+    void *Y3h = at<void>(ws, pl.off[kY3hi]), *Y3l = at<void>(ws, pl.off[kY3lo]);
+    const size_t part = pl.off[kHPart], qpart = pl.off[kHQpart];
+    // sweep 1: Y1 = G S, Z1 = A^T Y1
+    DPCLIP_TRY(run_tok(G, B, T, p, S, nullptr, 16, false, pl, ws, part, Y1h, Y1l, s));
+    DPCLIP_TRY(run_feat(A, B, T, d, Y1h, Y1l, 16, kFeatOutHiLo, nullptr, pl, ws, part, qpart,
+                        nullptr, Z1h, Z1l, nullptr, s));
+    // sweep 2: U = A Z1, V = G^T U  (= O S)
+    DPCLIP_TRY(run_tok(A, B, T, d, Z1h, Z1l, 16, true, pl, ws, part, Uh, Ul, s));
+    DPCLIP_TRY(run_feat(G, B, T, p, Uh, Ul, 16, kFeatOutF32, nullptr, pl, ws, part, qpart, V,
+                        nullptr, nullptr, nullptr, s));
+    // Q, W
+    HppQrParams hq;
+    std::memset(&hq, 0, sizeof(hq));
+    hq.V = V;
+    hq.ldv = 16;
+    hq.Gp = Gp;
+    hq.gp_bf16 = 1;
+    hq.B = B;
+    hq.p = p;
+    hq.r = r;
+    hq.m = m;
+    hq.Q1 = at<double>(ws, pl.off[kQ1]);
+    hq.out_hi = static_cast<__nv_bfloat16*>(QWh);
+    hq.out_lo = static_cast<__nv_bfloat16*>(QWl);
+    hq.err = at<uint32_t>(ws, pl.ctrl);
+    DPCLIP_CUDA(launch_hpp_qr(hq, s));
+    // sweep 3: Y3 = G [Q | W], head + tail / m from A^T Y3
+    DPCLIP_TRY(run_tok(G, B, T, p, QWh, QWl, 32, true, pl, ws, part, Y3h, Y3l, s));
+    DPCLIP_TRY(run_feat(A, B, T, d, Y3h, Y3l, 32, kFeatSqNorm, w, pl, ws, part, qpart, nullptr,
+                        nullptr, nullptr, sqnorms, s));
+    return DPCLIP_OK;
+  }
+  const float* Af = static_cast<const float*>(A);
+  const float* Gf = static_cast<const float*>(G);
+  float* S = at<float>(ws, pl.off[kFS]);
+  float* Gp = at<float>(ws, pl.off[kFGp]);
+  float* Y1 = at<float>(ws, pl.off[kFY1]);
+  float* Z1 = at<float>(ws, pl.off[kFZ1]);
+  float* U = at<float>(ws, pl.off[kFU]);
+  float* V = at<float>(ws, pl.off[kFV]);
+  float* QW = at<float>(ws, pl.off[kFQW]);
+  float* Y3 = at<float>(ws, pl.off[kFY3]);
+  DPCLIP_CUDA(launch_philox_fill(S, r, p, r, false, seed, 1u, offset, s));
+  DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, false, seed, 2u, offset, s));
+  int nb = 0;
+  SimtParams sp = simt_base();
+  // Y1 = G S
+  sp.X = Gf; sp.xb = (long long)T * p; sp.xm = p; sp.xk = 1;
+  sp.Y = S; sp.yb = 0; sp.yk = 1; sp.yn = p;
+  sp.batch = B; sp.M = T; sp.N = r; sp.K = p;
+  sp.out = Y1; sp.ob = (long long)T * r; sp.om = r; sp.on = 1;
+  DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+  // Z1 = A^T Y1  (d x r)
+  sp = simt_base();
+  sp.X = Af; sp.xb = (long long)T * d; sp.xm = 1; sp.xk = d;
+  sp.Y = Y1; sp.yb = (long long)T * r; sp.yk = r; sp.yn = 1;
+  sp.batch = B; sp.M = d; sp.N = r; sp.K = T;
+  sp.out = Z1; sp.ob = (long long)d * r; sp.om = r; sp.on = 1;
+  DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+  // U = A Z1  (T x r)
+  sp = simt_base();
+  sp.X = Af; sp.xb = (long long)T * d; sp.xm = d; sp.xk = 1;
+  sp.Y = Z1; sp.yb = (long long)d * r; sp.yk = r; sp.yn = 1;
+  sp.batch = B; sp.M = T; sp.N = r; sp.K = d;
+  sp.out = U; sp.ob = (long long)T * r; sp.om = r; sp.on = 1;
+  DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+  // V = G^T U  (p x r), stored [B][16][p]
+  sp = simt_base();
+  sp.X = Gf; sp.xb = (long long)T * p; sp.xm = 1; sp.xk = p;
+  sp.Y = U; sp.yb = (long long)T * r; sp.yk = r; sp.yn = 1;
+  sp.batch = B; sp.M = p; sp.N = r; sp.K = T;
+  sp.out = V; sp.ob = (long long)16 * p; sp.om = 1; sp.on = p;
+  DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+  HppQrParams hq;
+  std::memset(&hq, 0, sizeof(hq));
+  hq.V = V;
+  hq.ldv = 16;
+  hq.Gp = Gp;
+  hq.gp_bf16 = 0;
+  hq.B = B;
+  hq.p = p;
+  hq.r = r;
+  hq.m = m;
+  hq.Q1 = at<double>(ws, pl.off[kFQ1]);
+  hq.out_f32 = QW;
+  hq.err = at<uint32_t>(ws, pl.ctrl);
+  DPCLIP_CUDA(launch_hpp_qr(hq, s));
+  // Y3 = G [Q | W]  (T x (r+m))
+  sp = simt_base();
+  sp.X = Gf; sp.xb = (long long)T * p; sp.xm = p; sp.xk = 1;
+  sp.Y = QW; sp.yb = (long long)32 * p; sp.yk = 1; sp.yn = p;
+  sp.batch = B; sp.M = T; sp.N = r + m; sp.K = p;
+  sp.out = Y3; sp.ob = (long long)T * (r + m); sp.om = r + m; sp.on = 1;
+  DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+  // head + tail / m
+  sp = simt_base();
+  for (int j = 0; j < 64; ++j) sp.w[j] = j < r ? 1.f : (j < r + m ? 1.f / (float)m : 0.f);
+  sp.X = Af; sp.xb = (long long)T * d; sp.xm = 1; sp.xk = d;
+  sp.Y = Y3; sp.yb = (long long)T * (r + m); sp.yk = r + m; sp.yn = 1;
+  sp.batch = B; sp.M = d; sp.N = r + m; sp.K = T;
+  sp.part = at<float>(ws, pl.off[kFPart]);
+  DPCLIP_CUDA(launch_simt(sp, kSimtSqNorm, s, &nb));
+  DPCLIP_CUDA(launch_finalize_norms(sp.part, B, nb, 1, nb, 1, 1.f, sqnorms, s));
+  return DPCLIP_OK;
+}
+
+int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                              const float* sqnorms, float C, float sigma, uint64_t seed,
+                              uint64_t offset, float* grad, float* scales, uint8_t* clipped,
+                              void* ws, size_t ws_bytes, dpclip_stream_t stream) {
+  DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
+  if (!sqnorms || !grad) return DPCLIP_ERR_INVALID_ARG;
+  if (!(C > 0.f) || !std::isfinite(C)) return DPCLIP_ERR_INVALID_ARG;
+  if (!(sigma >= 0.f) || !std::isfinite(sigma)) return DPCLIP_ERR_INVALID_ARG;
+  if (!aligned(grad, dtype == DPCLIP_BF16 ? 16 : 4)) return DPCLIP_ERR_UNSUPPORTED;
+  Plan pl = plan_grad();
+  DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
+  cudaStream_t s = (cudaStream_t)stream;
+  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  if (dtype == DPCLIP_BF16) {
+    GemmDpParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!make_map(&gp.map_a, A, d, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
+    if (!make_map(&gp.map_g, G, p, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
+    gp.B = B;
+    gp.T = T;
+    gp.d = d;
+    gp.p = p;
+    gp.mtiles = cdiv(d, kDpTileM);
+    gp.ntiles = cdiv(p, kDpTileN);
+    gp.tblocks = cdiv(T, kBlockK);
+    gp.sqnorms = sqnorms;
+    gp.C = C;
+    gp.sigma = sigma;
+    gp.seed = seed;
+    gp.offset = offset;
+    gp.grad = grad;
+    gp.scales = scales;
+    gp.clipped = clipped;
+    gp.err = at<uint32_t>(ws, pl.ctrl);
+    const int ntiles = gp.mtiles * gp.ntiles;
+    DPCLIP_CUDA(launch_gemm_dp(gp, true, std::min(ntiles, num_sms()), s));
+    return DPCLIP_OK;
+  }
+  SimtParams sp = simt_base();
+  sp.X = static_cast<const float*>(A); sp.xb = (long long)T * d; sp.xm = 1; sp.xk = d;
+  sp.Y = static_cast<const float*>(G); sp.yb = (long long)T * p; sp.yk = p; sp.yn = 1;
+  sp.batch = B; sp.M = d; sp.N = p; sp.K = T;
+  sp.out = grad; sp.om = p; sp.on = 1;
+  sp.sqnorms = sqnorms;
+  sp.C = C;
+  DPCLIP_CUDA(launch_simt(sp, kSimtGrad, s, nullptr));
+  if (sigma > 0.f)
+    DPCLIP_CUDA(launch_noise_add(grad, (long long)d * p, sigma * C, seed, offset, s));
+  if (scales || clipped) DPCLIP_CUDA(launch_clip_scales(sqnorms, B, C, scales, clipped, s));
+  return DPCLIP_OK;
+}
+
+int dpclip_workspace_status(const void* ws, dpclip_stream_t stream) {
+  if (!ws) return DPCLIP_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return DPCLIP_ERR_CUDA;
+  }
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return DPCLIP_ERR_CUDA;
+  }
+  return (int)word;
+}
+
+int dpclip_selftest_wait_timeout(void* ws, size_t ws_bytes, int timeout_us, dpclip_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return DPCLIP_ERR_INVALID_ARG;
+  DPCLIP_TRY(check_ws(ws, ws_bytes, kAlign));
+  cudaStream_t s = (cudaStream_t)stream;
+  DPCLIP_CUDA(cudaMemsetAsync(ws, 0, kAlign, s));
+  DPCLIP_CUDA(launch_wait_selftest(static_cast<uint32_t*>(ws), (uint64_t)timeout_us * 1000ull, s));
+  return DPCLIP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,214 @@
+// Exact per-sample squared norms in the ghost form
+//   ||A_i^T G_i||_F^2 = sum_{t1,t2} (A_i A_i^T)[t1,t2] * (G_i G_i^T)[t1,t2],
+// the Gram-Hadamard rewrite of the trace identity in "Core mechanism" of the
+// randomized-clipping summary (the ghost-clipping baseline of its "Problem
+// definition": O(T^2) per sample, no d x p tile ever formed).
+//
+// Work unit = (sample i, token tiles a <= b of 128 tokens).  Two TMEM
+// accumulators of 128 x 128 fp32: X = A_a A_b^T (K = d) then Y = G_a G_b^T
+// (K = p), both K-major TMA tiles with 128-byte swizzle.  The epilogue forms
+// sum(X o Y), doubled off the diagonal (the (b, a) block is the transpose),
+// and writes one partial per unit and epilogue warp; a second small kernel
+// adds the partials of each sample in a fixed order.  Two accumulator pairs
+// (512 TMEM columns) alternate between units.
+//
+// Roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..9 = epilogue.
+#include "common.cuh"
+
+namespace dpclip {
+namespace {
+
+constexpr int kStages = 6;
+constexpr uint32_t kTileBytes = 128 * 128;   // 128 token rows x 128 B
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
+struct Ctl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem;
+  int abort_flag;
+  int issued;
+  int consumed;
+  int mma_units;
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * 2 * kTileBytes + sizeof(Ctl);
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// pair index -> (a, b), a <= b, enumerated row by row of the upper triangle.
+__device__ __forceinline__ void pair_of(int pr, int ntt, int& a, int& b) {
+  int row = 0, len = ntt;
+  while (pr >= len) {
+    pr -= len;
+    ++row;
+    --len;
+  }
+  a = row;
+  b = row + pr;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constant__ GhostParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sP = smem;                              // tile of block a
+  uint8_t* sQ = sP + kStages * kTileBytes;         // tile of block b
+  Ctl* ctl = reinterpret_cast<Ctl*>(sQ + kStages * kTileBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nunits = p.B * p.npairs;
+  const int kblocks = p.dblocks + p.pblocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctl->tfull[a], 1);
+      mbar_init(&ctl->tempty[a], 32 * kEpiWarps);
+    }
+    ctl->abort_flag = 0;
+    ctl->issued = 0;
+    ctl->consumed = 0;
+    ctl->mma_units = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&p.map_a);
+    tma_prefetch_map(&p.map_g);
+  }
+  if (warp == 1) tmem_alloc(&ctl->tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool run = true;
+      for (int u = blockIdx.x; run && u < nunits; u += gridDim.x) {
+        const int i = u / p.npairs;
+        int a, b;
+        pair_of(u % p.npairs, p.ntt, a, b);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) {
+            run = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctl->full[s], 2 * kTileBytes);
+          const bool on_a = kb < p.dblocks;
+          const CUtensorMap* map = on_a ? &p.map_a : &p.map_g;
+          const int k0 = (on_a ? kb : kb - p.dblocks) * kBlockK;
+          tma_load_3d(sP + s * kTileBytes, map, &ctl->full[s], k0, a * kGhostTile, i);
+          tma_load_3d(sQ + s * kTileBytes, map, &ctl->full[s], k0, b * kGhostTile, i);
+          ctl->issued = it + 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      int it = 0, lu = 0;
+      bool run = true;
+      for (int u = blockIdx.x; run && u < nunits; u += gridDim.x, ++lu) {
+        const int acc = lu & 1;
+        if (!mbar_wait(&ctl->tempty[acc], ((lu >> 1) & 1) ^ 1, wc)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) {
+            run = false;
+            break;
+          }
+          ctl->consumed = it + 1;
+          tc_fence_after();
+          const bool on_a = kb < p.dblocks;
+          const int kl = on_a ? kb : kb - p.dblocks;
+          const uint32_t dt = tmem + (uint32_t)acc * 256u + (on_a ? 0u : 128u);
+          const uint32_t a0 = smem_u32(sP + s * kTileBytes);
+          const uint32_t b0 = smem_u32(sQ + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(dt, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
+                      idesc, (kl | kk) != 0);
+          umma_commit(&ctl->empty[s]);
+        }
+        umma_commit(&ctl->tfull[acc]);
+        ctl->mma_units = lu + 1;
+      }
+    }
+  } else {
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    int lu = 0;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lu) {
+      const int acc = lu & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[acc], (lu >> 1) & 1, wc))) break;
+      tc_fence_after();
+      int a, b;
+      pair_of(u % p.npairs, p.ntt, a, b);
+      const uint32_t base =
+          tmem + (uint32_t)acc * 256u + (uint32_t)half * 64u + ((uint32_t)(quad * 32) << 16);
+      float s = 0.f;
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        float x[32], y[32];
+        tmem_ld32(base + c2 * 32, x);
+        tmem_ld32(base + 128 + c2 * 32, y);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s = fmaf(x[j], y[j], s);
+      }
+      tc_fence_before();
+      mbar_arrive(&ctl->tempty[acc]);
+      s = warp_sum(s);
+      if (lane == 0) p.part[(size_t)u * kEpiWarps + ew] = (a == b) ? s : 2.f * s;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort_flag && threadIdx.x == 0) {
+    const uint64_t lim = 100000000ull;
+    for (int it = ctl->consumed; it < ctl->issued; ++it) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&ctl->full[it % kStages], (uint32_t)(it / kStages) & 1u))
+        if (globaltimer_ns() - t0 > lim) break;
+    }
+    for (int a = 0; a < 2; ++a) {
+      const int last_u = ctl->mma_units - 1 - ((ctl->mma_units - 1 - a) & 1);
+      if (last_u < 0) continue;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&ctl->tfull[a], (uint32_t)(last_u >> 1) & 1u))
+        if (globaltimer_ns() - t0 > lim) break;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t ghost_smem() { return kSmemBytes; }
+
+cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(ghost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  ghost_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dpclip

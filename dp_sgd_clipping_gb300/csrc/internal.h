@@ -1,0 +1,166 @@
+// Internal interface between the C-ABI layer (dpclip.cu) and the kernel
+// translation units.  Host-side only types plus CUtensorMap.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dpclip.h"
+
+namespace dpclip {
+
+// ----------------------------------------------------------------------------
+// Tile geometry of the tensor-core kernels
+// ----------------------------------------------------------------------------
+constexpr int kTokTileM = 128;     // tokens per tok_gemm tile
+constexpr int kFeatTileM = 128;    // features per feat_gemm tile
+constexpr int kBlockK = 64;        // bf16 elements per 128-byte swizzled row
+constexpr int kDpTileM = 128;      // d rows per gradient / direct-norm tile
+constexpr int kDpTileN = 256;      // p columns per gradient / direct-norm tile
+constexpr int kGhostTile = 128;    // tokens per ghost Gram tile (both sides)
+constexpr int kEpiWarps = 8;       // epilogue warps of the persistent kernels
+constexpr int kMaxNP = 32;         // widest skinny operand (probe columns)
+
+// Skinny-GEMM epilogue modes of feat_gemm.
+enum FeatMode { kFeatOutF32 = 0, kFeatOutHiLo = 1, kFeatSqNorm = 2 };
+
+// tok_gemm:  out[i][j][t] = sum_f X[i][t][f] * W[w(i)][j][f]
+//   X: [B][T][F] bf16 (K-major operand), W: [Bw][NP][F] bf16 hi (+ lo).
+//   Output: hi/lo bf16 [B][NP][Tp], Tp = mtiles * 128 (rows >= T are zero).
+struct TokGemmParams {
+  CUtensorMap map_x;     // box {64, 128, 1}
+  CUtensorMap map_whi;   // box {64, NP, 1}
+  CUtensorMap map_wlo;   // box {64, NP, 1}
+  int B, T, F, NP;
+  int w_per_sample, has_lo;
+  int mtiles, kblocks, splits, kb_per_split, Tp;
+  __nv_bfloat16* out_hi;
+  __nv_bfloat16* out_lo;
+  float* part;           // [splits][B][NP][Tp] when splits > 1
+  uint32_t* counters;    // [B * mtiles]
+  uint32_t* err;
+};
+
+// feat_gemm: Z[i][f][j] = sum_t X[i][t][f] * Y[i][j][t]
+//   X: [B][T][F] bf16 (MN-major operand), Y: [B][NP][Tp] bf16 hi + lo.
+//   Modes: fp32 out [B][NP][F]; hi/lo bf16 out [B][NP][F];
+//          sqnorm: sq[i] = sum_{f,j} w[j] * Z[i][f][j]^2.
+struct FeatGemmParams {
+  CUtensorMap map_x;     // box {64, 64, 1}
+  CUtensorMap map_yhi;   // box {64, NP, 1}
+  CUtensorMap map_ylo;
+  int B, T, F, NP, Tp;
+  int ftiles, tblocks, splits, tb_per_split, Fp;
+  float w[kMaxNP];       // column weights for the sqnorm mode
+  float* out_f32;
+  __nv_bfloat16* out_hi;
+  __nv_bfloat16* out_lo;
+  float* sq;             // [B] output of the sqnorm mode
+  float* part;           // [splits][B][NP][Fp] when splits > 1
+  float* qpart;          // [B][ftiles]
+  uint32_t* counters;    // [B * ftiles] then [B]
+  uint32_t* err;
+};
+
+// gemm_dp: per output tile (128 d x 256 p) and sample i, acc_i = A_i^T G_i.
+//   grad mode:  grad = sum_i s_i acc_i + sigma*C*Z  (stored fp32 [d][p])
+//   norm mode:  part[(tile*B + i)*8 + w] = partial sum of acc_i^2
+struct GemmDpParams {
+  CUtensorMap map_a;     // A [B][T][d], box {64, 64, 1}
+  CUtensorMap map_g;     // G [B][T][p], box {64, 64, 1}
+  int B, T, d, p;
+  int mtiles, ntiles, tblocks;
+  const float* sqnorms;
+  float C, sigma;
+  uint64_t seed, offset;
+  float* grad;
+  float* scales;
+  uint8_t* clipped;
+  float* part;
+  uint32_t* err;
+};
+
+// ghost: per sample i and token tiles a <= b, sum((A_a A_b^T) o (G_a G_b^T)),
+//   weighted 2 off the diagonal; part[u*8 + w] per unit u = i*npairs + pair.
+struct GhostParams {
+  CUtensorMap map_a;     // box {64, 128, 1}
+  CUtensorMap map_g;     // box {64, 128, 1}
+  int B, T, d, p;
+  int ntt, npairs, dblocks, pblocks;
+  float* part;
+  uint32_t* err;
+};
+
+// Hutch++ middle step: per sample, orthonormal basis Q of V (p x r) by
+// pivoted CholeskyQR2 in fp64, W = G' - Q (Q^T G'), output [Q | W] padded
+// to 32 columns, as hi/lo bf16 or fp32, [B][32][p].
+struct HppQrParams {
+  const float* V;        // [B][ldv][p] fp32, columns j < r used
+  int ldv;
+  const void* Gp;        // [m][p], bf16 or fp32 (gp_bf16)
+  int gp_bf16;
+  int B, p, r, m;
+  double* Q1;            // [B][r][p] fp64 scratch
+  __nv_bfloat16* out_hi; // bf16 output (when out_f32 == nullptr)
+  __nv_bfloat16* out_lo;
+  float* out_f32;        // fp32 output [B][32][p]
+  uint32_t* err;
+};
+
+// Generic fp32 SIMT GEMM over a batch:  acc[b](m,n) = sum_k X[b](m,k) Y[b](k,n)
+// with arbitrary element strides; epilogue modes below.
+enum SimtMode { kSimtStore = 0, kSimtSqNorm = 1, kSimtDotWith = 2, kSimtGrad = 3 };
+struct SimtParams {
+  const float* X;
+  const float* Y;
+  long long xb, xm, xk;
+  long long yb, yk, yn;
+  int batch, M, N, K;
+  // store / dot-with operand
+  float* out;
+  long long ob, om, on;
+  // sqnorm / dot-with partials: part[b * nblocks + block]
+  float* part;
+  float w[64];            // column weights (sqnorm)
+  // grad
+  const float* sqnorms;
+  float C, sigma;
+  uint64_t seed, offset;
+  float* scales;
+  uint8_t* clipped;
+};
+
+// ----------------------------------------------------------------------------
+// Launchers (defined in the kernel translation units).  Each returns a
+// cudaError_t from the launch.
+// ----------------------------------------------------------------------------
+cudaError_t launch_tok_gemm(const TokGemmParams& p, cudaStream_t s);
+cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s);
+cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cudaStream_t s);
+cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s);
+cudaError_t launch_hpp_qr(const HppQrParams& p, cudaStream_t s);
+cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblocks_out);
+int simt_nblocks(int M, int N);
+
+cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
+                               bool bf16, uint64_t seed, uint32_t stream_id, uint64_t offset,
+                               cudaStream_t s);
+cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
+                               cudaStream_t s);
+// sq[i] = scale * sum_{u < nunits, w < nw} part[(u * su + i * si) * nw + w]
+cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long long su,
+                                  long long si, int nw, float scale, float* sq, cudaStream_t s);
+cudaError_t launch_noise_add(float* grad, long long n, float scale, uint64_t seed,
+                             uint64_t offset, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
+
+// Shared-memory footprint of each tensor-core kernel (bytes of dynamic smem).
+size_t tok_gemm_smem(int NP);
+size_t feat_gemm_smem(int NP);
+size_t gemm_dp_smem();
+size_t ghost_smem();
+
+}  // namespace dpclip

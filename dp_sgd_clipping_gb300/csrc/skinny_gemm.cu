@@ -1,0 +1,435 @@
+// Skinny tensor-core GEMMs of the randomized norm estimators.
+//
+// Hutch ("Core mechanism", item 1 of the randomized-clipping summary) needs,
+// per sample i, Y_i = G_i P (T x k) and Z_i = A_i^T Y_i (d x k), then
+// (1/k) ||Z_i||_F^2.  Both products stream one big operand (G or A) once and
+// meet a skinny one (k <= 32 columns), so they are HBM-bound (32 flop/byte):
+// the kernels below keep every SM's TMA queue deep and spend almost nothing
+// on the tensor core.  Hutch++ (item 2) reuses the same two kernels for its
+// three sweeps with other skinny operands.
+//
+//   tok_gemm:  out[i][j][t] = sum_f X[i][t][f] W[j][f]   (M = 128 tokens,
+//              N = NP probe columns, K = features; X K-major via TMA)
+//   feat_gemm: Z[i][f][j]   = sum_t X[i][t][f] Y[i][j][t] (M = 128 features,
+//              N = NP, K = tokens; X MN-major via TMA, Y K-major)
+//
+// Skinny operands are bf16 hi + lo pairs (two MMAs into one fp32 TMEM
+// accumulator), so a fp32 intermediate keeps ~16 significant bits.  A split
+// of the K range over several CTAs is reduced deterministically: partials go
+// to the workspace and the last CTA of a tile (found with an integer ticket)
+// adds them in split order.
+//
+// Warp roles (128 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
+// tcgen05.mma, then all four warps drain TMEM (warp w owns TMEM lanes
+// 32w..32w+31, i.e. tile rows 32w..32w+31).
+#include "common.cuh"
+
+namespace dpclip {
+namespace {
+
+constexpr int kStages = 4;   // 4 x 24 KB: two CTAs fit on one SM
+constexpr uint32_t kXTileBytes = 128 * kBlockK * 2;   // 16 KB: 128 rows x 128 B
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+struct SmemCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t done;
+  uint32_t tmem;
+  int abort_flag;
+  int is_last;
+  int issued;
+  int consumed;
+  float red[4];
+};
+
+template <int NP>
+__host__ __device__ constexpr uint32_t skinny_tile_bytes() {
+  return (uint32_t)NP * 128u;   // NP rows x 64 bf16
+}
+
+template <int NP>
+__host__ __device__ constexpr size_t skinny_smem_bytes() {
+  return 1024 + (size_t)kStages * (kXTileBytes + 2 * skinny_tile_bytes<NP>()) + sizeof(SmemCtl);
+}
+
+// Drain after an abort: wait (bounded, not abortable) for the TMA loads that
+// were issued but never consumed, and for the MMAs already issued, so that no
+// async write lands in shared or tensor memory after the CTA has left.
+__device__ void drain_after_abort(SmemCtl* ctl) {
+  const uint64_t lim = 100000000ull;  // 100 ms per wait
+  for (int it = ctl->consumed; it < ctl->issued; ++it) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(&ctl->full[it % kStages], (uint32_t)(it / kStages) & 1u))
+      if (globaltimer_ns() - t0 > lim) break;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(&ctl->done, 0))
+    if (globaltimer_ns() - t0 > lim) break;
+}
+
+// ---------------------------------------------------------------------------
+// tok_gemm
+// ---------------------------------------------------------------------------
+template <int NP>
+__global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant__ TokGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  constexpr uint32_t kWBytes = skinny_tile_bytes<NP>();
+  uint8_t* sX = smem;
+  uint8_t* sWhi = sX + kStages * kXTileBytes;
+  uint8_t* sWlo = sWhi + kStages * kWBytes;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sWlo + kStages * kWBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  const int i = tile / p.mtiles, mt = tile % p.mtiles;
+  const int split = blockIdx.y;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(kb0 + p.kb_per_split, p.kblocks);
+  const int nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    mbar_init(&ctl->done, 1);
+    ctl->abort_flag = 0;
+    ctl->issued = 0;
+    ctl->consumed = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&p.map_x);
+    tma_prefetch_map(&p.map_whi);
+    if (p.has_lo) tma_prefetch_map(&p.map_wlo);
+  }
+  if (warp == 1) tmem_alloc(&ctl->tmem, 32);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
+
+  if (warp == 0 && lane == 0) {
+    const uint32_t bytes = kXTileBytes + kWBytes * (p.has_lo ? 2u : 1u);
+    const int wz = p.w_per_sample ? i : 0;
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % kStages;
+      if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
+      mbar_arrive_expect_tx(&ctl->full[s], bytes);
+      const int f0 = (kb0 + it) * kBlockK;
+      tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, mt * kTokTileM, i);
+      tma_load_3d(sWhi + s * kWBytes, &p.map_whi, &ctl->full[s], f0, 0, wz);
+      if (p.has_lo) tma_load_3d(sWlo + s * kWBytes, &p.map_wlo, &ctl->full[s], f0, 0, wz);
+      ctl->issued = it + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, NP, false, false);
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % kStages;
+      if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) break;
+      ctl->consumed = it + 1;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sX + s * kXTileBytes);
+      const uint32_t b0 = smem_u32(sWhi + s * kWBytes);
+      const uint32_t c0 = smem_u32(sWlo + s * kWBytes);
+#pragma unroll
+      for (int kk = 0; kk < kBlockK / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+        umma_bf16(tmem, ad, sdesc_sw128(b0 + kk * 32, 16, 1024), idesc, (it | kk) != 0);
+        if (p.has_lo) umma_bf16(tmem, ad, sdesc_sw128(c0 + kk * 32, 16, 1024), idesc, 1);
+      }
+      umma_commit(&ctl->empty[s]);
+    }
+    umma_commit(&ctl->done);
+  }
+  __syncwarp();
+
+  // ---- epilogue: all 4 warps, thread = one token row of the tile
+  const int row = warp * 32 + lane;
+  const int t = mt * kTokTileM + row;
+  const size_t plane = (size_t)NP * p.Tp;
+  // tcgen05.ld is warp-collective: decide per warp
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->done, 0, wc));
+  if (ok) {
+    tc_fence_after();
+    float y[32];
+    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), y);
+    if (p.splits == 1) {
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        __nv_bfloat16 hi, lo;
+        split_hilo(y[j], hi, lo);
+        p.out_hi[(size_t)i * plane + (size_t)j * p.Tp + t] = hi;
+        p.out_lo[(size_t)i * plane + (size_t)j * p.Tp + t] = lo;
+      }
+    } else {
+      float* part = p.part + ((size_t)split * p.B + i) * plane;
+#pragma unroll
+      for (int j = 0; j < NP; ++j) part[(size_t)j * p.Tp + t] = y[j];
+      __threadfence();
+    }
+  }
+  if (p.splits > 1) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t prev = atomicAdd(&p.counters[tile], 1u);
+      ctl->is_last = (prev == (uint32_t)p.splits - 1u);
+    }
+    __syncthreads();
+    if (ctl->is_last) {
+      __threadfence();
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        float acc = 0.f;
+        for (int s = 0; s < p.splits; ++s)
+          acc += __ldcg(p.part + ((size_t)s * p.B + i) * plane + (size_t)j * p.Tp + t);
+        __nv_bfloat16 hi, lo;
+        split_hilo(acc, hi, lo);
+        p.out_hi[(size_t)i * plane + (size_t)j * p.Tp + t] = hi;
+        p.out_lo[(size_t)i * plane + (size_t)j * p.Tp + t] = lo;
+      }
+      if (threadIdx.x == 0) p.counters[tile] = 0u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort_flag && threadIdx.x == 0) drain_after_abort(ctl);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// feat_gemm
+// ---------------------------------------------------------------------------
+template <int NP, int MODE>
+__global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant__ FeatGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  constexpr uint32_t kYBytes = skinny_tile_bytes<NP>();
+  constexpr uint32_t kHalf = 64 * 128;   // one 64-feature x 64-token box
+  uint8_t* sX = smem;
+  uint8_t* sYhi = sX + kStages * kXTileBytes;
+  uint8_t* sYlo = sYhi + kStages * kYBytes;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sYlo + kStages * kYBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  const int i = tile / p.ftiles, ft = tile % p.ftiles;
+  const int split = blockIdx.y;
+  const int tb0 = split * p.tb_per_split;
+  const int tb1 = min(tb0 + p.tb_per_split, p.tblocks);
+  const int ntb = tb1 - tb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    mbar_init(&ctl->done, 1);
+    ctl->abort_flag = 0;
+    ctl->issued = 0;
+    ctl->consumed = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&p.map_x);
+    tma_prefetch_map(&p.map_yhi);
+    tma_prefetch_map(&p.map_ylo);
+  }
+  if (warp == 1) tmem_alloc(&ctl->tmem, 32);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem;
+  const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
+
+  if (warp == 0 && lane == 0) {
+    const uint32_t bytes = kXTileBytes + 2 * kYBytes;
+    for (int it = 0; it < ntb; ++it) {
+      const int s = it % kStages;
+      if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
+      mbar_arrive_expect_tx(&ctl->full[s], bytes);
+      const int t0 = (tb0 + it) * kBlockK;
+      const int f0 = ft * kFeatTileM;
+      tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, t0, i);
+      tma_load_3d(sX + s * kXTileBytes + kHalf, &p.map_x, &ctl->full[s], f0 + 64, t0, i);
+      tma_load_3d(sYhi + s * kYBytes, &p.map_yhi, &ctl->full[s], t0, 0, i);
+      tma_load_3d(sYlo + s * kYBytes, &p.map_ylo, &ctl->full[s], t0, 0, i);
+      ctl->issued = it + 1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, NP, true, false);
+    for (int it = 0; it < ntb; ++it) {
+      const int s = it % kStages;
+      if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) break;
+      ctl->consumed = it + 1;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sX + s * kXTileBytes);
+      const uint32_t b0 = smem_u32(sYhi + s * kYBytes);
+      const uint32_t c0 = smem_u32(sYlo + s * kYBytes);
+#pragma unroll
+      for (int kk = 0; kk < kBlockK / 16; ++kk) {
+        // MN-major A: 16 tokens = two 8-row groups of 1024 B; the two
+        // 64-feature halves sit kHalf bytes apart.
+        const uint64_t ad = sdesc_sw128(a0 + kk * 2048, kHalf, 1024);
+        umma_bf16(tmem, ad, sdesc_sw128(b0 + kk * 32, 16, 1024), idesc, (it | kk) != 0);
+        umma_bf16(tmem, ad, sdesc_sw128(c0 + kk * 32, 16, 1024), idesc, 1);
+      }
+      umma_commit(&ctl->empty[s]);
+    }
+    umma_commit(&ctl->done);
+  }
+  __syncwarp();
+
+  // ---- epilogue: thread = one feature row of the tile
+  const int row = warp * 32 + lane;
+  const int f = ft * kFeatTileM + row;
+  const size_t plane = (size_t)NP * p.Fp;
+  float z[32];
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->done, 0, wc));
+  if (ok) {
+    tc_fence_after();
+    tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), z);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z[j] = 0.f;
+  }
+  bool have_final = true;
+  if (p.splits > 1) {
+    float* part = p.part + ((size_t)split * p.B + i) * plane;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) part[(size_t)j * p.Fp + f] = z[j];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t prev = atomicAdd(&p.counters[tile], 1u);
+      ctl->is_last = (prev == (uint32_t)p.splits - 1u);
+    }
+    __syncthreads();
+    have_final = ctl->is_last != 0;
+    if (have_final) {
+      __threadfence();
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        float acc = 0.f;
+        for (int s = 0; s < p.splits; ++s)
+          acc += __ldcg(p.part + ((size_t)s * p.B + i) * plane + (size_t)j * p.Fp + f);
+        z[j] = acc;
+      }
+      if (threadIdx.x == 0) p.counters[tile] = 0u;
+    }
+  }
+  if (have_final) {
+    if (MODE == kFeatOutF32) {
+      if (f < p.F) {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) p.out_f32[((size_t)i * NP + j) * p.F + f] = z[j];
+      }
+    } else if (MODE == kFeatOutHiLo) {
+      if (f < p.F) {
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+          __nv_bfloat16 hi, lo;
+          split_hilo(z[j], hi, lo);
+          p.out_hi[((size_t)i * NP + j) * p.F + f] = hi;
+          p.out_lo[((size_t)i * NP + j) * p.F + f] = lo;
+        }
+      }
+    } else {
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < NP; ++j) v += p.w[j] * z[j] * z[j];
+      v = warp_sum(v);
+      if (lane == 0) ctl->red[warp] = v;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const float tile_sum = ((ctl->red[0] + ctl->red[1]) + ctl->red[2]) + ctl->red[3];
+        p.qpart[(size_t)i * p.ftiles + ft] = tile_sum;
+        __threadfence();
+        uint32_t* cnt = p.counters + (size_t)p.B * p.ftiles + i;
+        const uint32_t prev = atomicAdd(cnt, 1u);
+        if (prev == (uint32_t)p.ftiles - 1u) {
+          __threadfence();
+          float q = 0.f;
+          for (int u = 0; u < p.ftiles; ++u) q += __ldcg(p.qpart + (size_t)i * p.ftiles + u);
+          p.sq[i] = q;
+          *cnt = 0u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (ctl->abort_flag && threadIdx.x == 0) drain_after_abort(ctl);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+size_t tok_gemm_smem(int NP) {
+  return NP <= 16 ? skinny_smem_bytes<16>() : skinny_smem_bytes<32>();
+}
+size_t feat_gemm_smem(int NP) { return tok_gemm_smem(NP); }
+
+cudaError_t launch_tok_gemm(const TokGemmParams& p, cudaStream_t s) {
+  const dim3 grid(p.B * p.mtiles, p.splits);
+  cudaError_t e;
+  if (p.NP == 16) {
+    const size_t sm = skinny_smem_bytes<16>();
+    if ((e = set_smem(tok_gemm_kernel<16>, sm)) != cudaSuccess) return e;
+    tok_gemm_kernel<16><<<grid, 128, sm, s>>>(p);
+  } else if (p.NP == 32) {
+    const size_t sm = skinny_smem_bytes<32>();
+    if ((e = set_smem(tok_gemm_kernel<32>, sm)) != cudaSuccess) return e;
+    tok_gemm_kernel<32><<<grid, 128, sm, s>>>(p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <int NP, int MODE>
+static cudaError_t launch_feat_t(const FeatGemmParams& p, cudaStream_t s) {
+  const dim3 grid(p.B * p.ftiles, p.splits);
+  const size_t sm = skinny_smem_bytes<NP>();
+  cudaError_t e = set_smem(feat_gemm_kernel<NP, MODE>, sm);
+  if (e != cudaSuccess) return e;
+  feat_gemm_kernel<NP, MODE><<<grid, 128, sm, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s) {
+  if (p.NP == 16) {
+    if (mode == kFeatOutF32) return launch_feat_t<16, kFeatOutF32>(p, s);
+    if (mode == kFeatOutHiLo) return launch_feat_t<16, kFeatOutHiLo>(p, s);
+    return launch_feat_t<16, kFeatSqNorm>(p, s);
+  }
+  if (p.NP == 32) {
+    if (mode == kFeatOutF32) return launch_feat_t<32, kFeatOutF32>(p, s);
+    if (mode == kFeatOutHiLo) return launch_feat_t<32, kFeatOutHiLo>(p, s);
+    return launch_feat_t<32, kFeatSqNorm>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dpclip

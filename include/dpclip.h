@@ -1,0 +1,166 @@
+/*
+ * dpclip -- per-linear-layer DP-SGD clipping path for one GB300 (sm_103a).
+ *
+ * C ABI of libdpclip.so.  For one linear layer and a batch of B sequences of T
+ * tokens, sample i has input activations A_i (T x d) and output gradients G_i
+ * (T x p); its weight gradient is M_i = A_i^T G_i (d x p).  The library
+ * computes
+ *   - per-sample squared norms ||M_i||_F^2, exactly or with the randomized
+ *     trace estimators Hutch and Hutch++,
+ *   - clip scales s_i = min(1, C / n_i) with n_i the square root of a norm,
+ *   - the clipped, noised sum  sum_i s_i M_i + N(0, sigma^2 C^2 I).
+ *
+ * Sources: "Technical summary: efficient DP-SGD for LLMs with randomized
+ * clipping" (gist.science summary of arXiv 2605.24879), sections "Core
+ * mechanism" and "Algorithmic flow"; the "DP-SGD" glossary entry of jisaku.com,
+ * section "DP-SGD algorithm".
+ *
+ * Common conventions
+ *   Layout   A is [B][T][d] and G is [B][T][p], row-major and contiguous.  The
+ *            gradient output is [d][p] row-major fp32 (the transpose of a
+ *            PyTorch nn.Linear weight gradient).
+ *   dtype    DPCLIP_F32: A, G are float.  DPCLIP_BF16: A, G are bfloat16 and
+ *            every product is accumulated in fp32; bf16 needs d % 8 == 0 and
+ *            p % 8 == 0 (16-byte rows for the tensor-memory-access engine).
+ *   Memory   every pointer argument is device memory owned by the caller and
+ *            must stay valid until the stream reaches the work; A, G, grad and
+ *            the workspace must be 16-byte aligned, the workspace 256-byte
+ *            aligned.  The library never allocates, frees or synchronises
+ *            (except dpclip_workspace_status, which synchronises by design).
+ *            Scratch memory comes only from the caller's workspace, sized by
+ *            dpclip_workspace_size; one workspace must not be used by two
+ *            calls that can run at the same time.
+ *   Streams  work is enqueued asynchronously on `stream` (NULL: legacy default
+ *            stream) of the current CUDA device.
+ *   Errors   arguments are checked on the host before anything is enqueued:
+ *            a bad argument returns a negative status and enqueues nothing.
+ *            Launch failures return DPCLIP_ERR_CUDA.  Device-side waits are
+ *            bounded: a wait that expires makes the kernels stop early and
+ *            records DPCLIP_ERR_TIMEOUT in the workspace, readable with
+ *            dpclip_workspace_status.  No C++ exception crosses this ABI.
+ *   Random   probes and noise come from Philox-4x32-10 (Salmon et al., SC'11)
+ *            keyed by `seed`; element e of stream s uses counter
+ *            (e / 4, s, offset_lo, offset_hi) and lane e % 4 through a
+ *            Box-Muller transform.  Streams: 0 = Hutch probe P, 1 = Hutch++
+ *            sketch S, 2 = Hutch++ tail probes G', 3 = gradient noise.  The
+ *            same (seed, offset) always gives the same numbers; pass the step
+ *            index as `offset`.
+ */
+#ifndef DPCLIP_H
+#define DPCLIP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dpclip_stream_t;   /* same type as cudaStream_t */
+
+enum dpclip_status {
+  DPCLIP_OK = 0,
+  DPCLIP_ERR_INVALID_ARG = -1,   /* null pointer, non-positive size, bad enum */
+  DPCLIP_ERR_UNSUPPORTED = -2,   /* valid but not supported: alignment, k range */
+  DPCLIP_ERR_WORKSPACE = -3,     /* workspace missing, misaligned or too small */
+  DPCLIP_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
+  DPCLIP_ERR_TIMEOUT = -5        /* a device-side wait expired (see status) */
+};
+
+enum dpclip_dtype { DPCLIP_F32 = 0, DPCLIP_BF16 = 1 };
+
+enum dpclip_exact_method {
+  DPCLIP_EXACT_AUTO = 0,    /* direct when T*(d+p) > d*p, else ghost */
+  DPCLIP_EXACT_GHOST = 1,   /* sum((A_i A_i^T) o (G_i G_i^T)) */
+  DPCLIP_EXACT_DIRECT = 2   /* ||A_i^T G_i||_F^2, tile by tile, never stored */
+};
+
+enum dpclip_op {
+  DPCLIP_OP_NORMS_EXACT = 0,
+  DPCLIP_OP_NORMS_HUTCH = 1,
+  DPCLIP_OP_NORMS_HUTCHPP = 2,
+  DPCLIP_OP_CLIPPED_NOISY_GRAD = 3
+};
+
+/* Largest probe count k for Hutch (k <= 32) and Hutch++ (k - floor(k/3) <= 32). */
+#define DPCLIP_HUTCH_MAX_K 32
+#define DPCLIP_HUTCHPP_MAX_K 48
+
+/* Workspace bytes for one call of `op` on these sizes.  `param` is k for the
+ * Hutch/Hutch++ ops, the dpclip_exact_method for DPCLIP_OP_NORMS_EXACT and
+ * ignored for the gradient.  Writes *bytes; returns a status. */
+int dpclip_workspace_size(int op, int B, int T, int d, int p, int dtype, int param,
+                          size_t* bytes);
+
+/* Exact per-sample squared norms sqnorms[i] = ||A_i^T G_i||_F^2 (fp32 [B]).
+ * Ghost form: "Problem definition" (ghost clipping, T^2 memory) and the trace
+ * identity of "Core mechanism"; direct form: the per-sample gradient itself,
+ * reduced tile by tile. */
+int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                       int method, float* sqnorms, void* ws, size_t ws_bytes,
+                       dpclip_stream_t stream);
+
+/* Hutch estimate ("Core mechanism", item 1): with P (p x k) i.i.d. N(0,1),
+ * one P per call shared by all samples, sqnorms[i] = (1/k) ||A_i^T (G_i P)||_F^2.
+ * bf16: P is rounded to bfloat16.  1 <= k <= DPCLIP_HUTCH_MAX_K. */
+int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                       int k, uint64_t seed, uint64_t offset, float* sqnorms, void* ws,
+                       size_t ws_bytes, dpclip_stream_t stream);
+
+/* Hutch++ estimate ("Core mechanism", item 2) with a budget of k products:
+ * r = floor(k/3) sketch columns S, Q = orthonormal basis of O_i S (computed
+ * per sample), head = trace(Q^T O_i Q), W = (I - Q Q^T) G' with m = k - 2r
+ * tail probes, sqnorms[i] = head + trace(W^T O_i W) / m, where
+ * O_i = G_i^T A_i A_i^T G_i.  3 <= k <= DPCLIP_HUTCHPP_MAX_K. */
+int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                         int k, uint64_t seed, uint64_t offset, float* sqnorms, void* ws,
+                         size_t ws_bytes, dpclip_stream_t stream);
+
+/* Clipped noisy gradient ("DP-SGD algorithm" steps 3-4; "Algorithmic flow"
+ * steps 4-5):
+ *   s_i  = min(1, C / sqrt(sqnorms[i])), s_i = 1 when sqnorms[i] == 0,
+ *   grad = sum_i s_i A_i^T G_i + sigma * C * Z,   Z ~ N(0, I) from stream 3,
+ *          entry (r, c) of grad using element index r * p + c.
+ * sqnorms (fp32 [B], device) may be the sum over several layers.  grad is fp32
+ * [d][p].  scales (fp32 [B]) and clipped (uint8 [B], 1 when sqrt(sqnorms[i]) >
+ * C) are optional outputs (NULL to skip).  C > 0, sigma >= 0.  The 1/|B| of
+ * the SGD update is not applied. */
+int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d, int p,
+                              int dtype, const float* sqnorms, float C, float sigma,
+                              uint64_t seed, uint64_t offset, float* grad, float* scales,
+                              uint8_t* clipped, void* ws, size_t ws_bytes,
+                              dpclip_stream_t stream);
+
+/* Clip scales alone: scales[i] = min(1, C / sqrt(sqnorms[i])) (1 when the norm
+ * is 0) and clipped[i] = sqrt(sqnorms[i]) > C; either output may be NULL. */
+int dpclip_clip_scales(const float* sqnorms, int B, float C, float* scales, uint8_t* clipped,
+                       dpclip_stream_t stream);
+
+/* The n standard normals of one Philox stream (see "Random" above), written
+ * as float (dtype DPCLIP_F32) or rounded to bfloat16 (DPCLIP_BF16) into `out`
+ * (device, 4-byte aligned). */
+int dpclip_philox_normal(void* out, int64_t n, int dtype, uint64_t seed, uint32_t stream_id,
+                         uint64_t offset, dpclip_stream_t stream);
+
+/* Synchronises `stream`, then returns DPCLIP_OK or the error the device
+ * recorded in the workspace of the last call that used it
+ * (DPCLIP_ERR_TIMEOUT), or DPCLIP_ERR_CUDA if the synchronisation failed. */
+int dpclip_workspace_status(const void* ws, dpclip_stream_t stream);
+
+/* Test hook for the bounded-wait path: enqueues one kernel whose barrier wait
+ * is never satisfied, with a limit of `timeout_us` microseconds (1..10^6); the
+ * kernel gives up, records DPCLIP_ERR_TIMEOUT in `ws` and returns.  Follow
+ * with dpclip_workspace_status. */
+int dpclip_selftest_wait_timeout(void* ws, size_t ws_bytes, int timeout_us,
+                                 dpclip_stream_t stream);
+
+/* Human-readable name of a status code. */
+const char* dpclip_status_string(int status);
+
+/* Library version string. */
+const char* dpclip_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DPCLIP_H */

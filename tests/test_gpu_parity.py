@@ -1,0 +1,214 @@
+"""GPU path vs the fp64 oracle, element by element, through the C ABI.
+
+Tolerances: relative 1e-5 for fp32 inputs and 2e-2 for bf16 inputs with fp32
+accumulation (per-sample norms and scales; the gradient normwise and per
+entry against tol * (|ref| + sigma C)); clip flags bit-exact wherever the
+reference norm is more than 4 tol C away from C.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from dp_sgd_clipping_gb300 import workloads as W
+from gpu_util import TOL, assert_flags, assert_grad, assert_rel, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    import __graft_entry__
+    __graft_entry__.build()
+    from dp_sgd_clipping_gb300 import api as _api
+    return _api
+
+
+def oracle_all(inp, k=None, want=("direct", "hutch", "hutchpp")):
+    wl = inp.wl
+    Ms = list(O.per_sample_grads(inp.A, inp.G))
+    out = {"Ms": Ms, "direct": np.array([np.sum(M * M) for M in Ms])}
+    k = wl.k if k is None else k
+    if "hutch" in want:
+        out["hutch"] = O.sqnorms_hutch(None, None, O.hutch_probe(wl.p, k, wl.seed, 0, wl.dtype), Ms=Ms)
+    if "hutchpp" in want:
+        S, Gp = O.hutchpp_probes(wl.p, k, wl.seed, 0, wl.dtype)
+        out["hutchpp"] = O.sqnorms_hutchpp(None, None, S, Gp, Ms=Ms)
+    return out
+
+
+def check_grad(api, inp, A, G, q, C, sigma, Ms, offset=0):
+    wl = inp.wl
+    tol = TOL[wl.dtype]
+    qd = torch.tensor(q, dtype=torch.float32, device="cuda")
+    grad, scales, clipped = api.clipped_noisy_grad(A, G, qd, C, sigma, wl.seed, offset)
+    torch.cuda.synchronize()
+    q32 = qd.double().cpu().numpy()          # the sqnorms the GPU saw
+    D, s_ref, _ = O.clipped_noisy_grad(None, None, q32, C, sigma, wl.seed, offset, Ms=Ms)
+    assert_rel(host(scales), s_ref, 1e-6, "scales")
+    assert_flags(host(clipped), np.sqrt(q32), C, tol)
+    assert_grad(host(grad), D, tol, sigma * C)
+    return grad
+
+
+# ----------------------------------------------------------------------------- RNG
+
+def test_philox_normals_match_oracle(api):
+    n = (1 << 20) + 3
+    z = api.philox_normal(n, seed=0xD5C11F, stream_id=3, offset=7)
+    ref = O.philox_normals(n, 0xD5C11F, 3, 7)
+    assert np.max(np.abs(host(z) - ref)) < 2e-5
+    zb = api.philox_normal(n, seed=0xD5C11F, stream_id=0, offset=(1 << 33) + 5, dtype=torch.bfloat16)
+    refb = O.round_bf16(O.philox_normals(n, 0xD5C11F, 0, (1 << 33) + 5))
+    got = host(zb)
+    same = got == refb
+    assert same.mean() > 0.999
+    # the rare differences are one bf16 step at a rounding boundary
+    assert np.all(np.abs(got[~same] - refb[~same]) <= 2.0 ** -7 * np.abs(refb[~same]) + 1e-30)
+
+
+def test_clip_scales_kernel(api):
+    q = np.array([0.0, 1e-12, 0.24, 0.25, 0.26, 1.0, 4.0, 1e8], dtype=np.float32)
+    s, c = api.clip_scales(torch.tensor(q, device="cuda"), 0.5)
+    s_ref, c_ref = O.clip_scales(q.astype(np.float64), 0.5)
+    assert_rel(host(s), s_ref, 1e-6, "scales")
+    assert_flags(host(c), np.sqrt(q.astype(np.float64)), 0.5, 1e-6)
+
+
+# ----------------------------------------------------------------------------- fp32 tiny
+
+def test_tiny_f32_workload(api):
+    inp = W.make_inputs(W.get(1))
+    wl = inp.wl
+    A, G = to_dev(inp)
+    ref = oracle_all(inp)
+    tol = TOL["f32"]
+    assert_rel(host(api.norms_exact(A, G, method=2)), ref["direct"], tol, "direct")
+    assert_rel(host(api.norms_exact(A, G, method=1)), ref["direct"], tol, "ghost")
+    assert_rel(host(api.norms_exact(A, G, method=0)), ref["direct"], tol, "auto")
+    q_h = api.norms_hutch(A, G, wl.k, wl.seed, 0)
+    assert_rel(host(q_h), ref["hutch"], tol, "hutch")
+    assert_rel(host(api.norms_hutchpp(A, G, wl.k, wl.seed, 0)), ref["hutchpp"], tol, "hutch++")
+    # the workload as stated (every sample clips at C = 1), then C at the
+    # median norm so that about half clip, then sigma = 0
+    check_grad(api, inp, A, G, host(q_h), wl.C, wl.sigma, ref["Ms"])
+    C_med = float(np.median(np.sqrt(ref["direct"])))
+    check_grad(api, inp, A, G, ref["direct"], C_med, wl.sigma, ref["Ms"], offset=3)
+    check_grad(api, inp, A, G, ref["direct"], C_med, 0.0, ref["Ms"])
+
+
+# ----------------------------------------------------------------------------- bf16 ragged
+
+RAGGED = [
+    # B, T, d, p, k : several tiles of every kernel plus ragged tails
+    (3, 300, 200, 328, 32),
+    (2, 300, 200, 328, 12),
+    (2, 40, 64, 72, 8),        # T below one token tile
+    (1, 1, 8, 16, 4),          # single token, the narrowest rows
+    (2, 520, 136, 520, 20),
+]
+
+
+@pytest.mark.parametrize("B,T,d,p,k", RAGGED)
+def test_bf16_ragged_all_paths(api, B, T, d, p, k):
+    wl = W.Workload(100 + T, f"ragged_{B}_{T}_{d}_{p}", B, T, d, p, "bf16", 1e-2, 0.5, 0.8, k,
+                    ("exact", "hutch", "hutchpp", "grad"))
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    ref = oracle_all(inp, k=k, want=("hutch", "hutchpp") if k >= 3 else ("hutch",))
+    tol = TOL["bf16"]
+    assert_rel(host(api.norms_exact(A, G, method=2)), ref["direct"], tol, "direct")
+    assert_rel(host(api.norms_exact(A, G, method=1)), ref["direct"], tol, "ghost")
+    q_h = api.norms_hutch(A, G, k, wl.seed, 0)
+    assert_rel(host(q_h), ref["hutch"], tol, "hutch")
+    if k >= 3:
+        assert_rel(host(api.norms_hutchpp(A, G, k, wl.seed, 0)), ref["hutchpp"], tol, "hutch++")
+    check_grad(api, inp, A, G, host(q_h), wl.C, wl.sigma, ref["Ms"])
+    C_med = float(np.median(np.sqrt(ref["direct"])))
+    check_grad(api, inp, A, G, ref["direct"], C_med, 0.0, ref["Ms"])
+
+
+def test_hutchpp_exact_when_rank_deficient(api):
+    # T = 6 tokens < r = 10 head columns: rank(O_i) <= 6, Hutch++ is exact.
+    wl = W.Workload(120, "rankdef", 2, 6, 64, 96, "bf16", 1e-2, 1.0, 1.0, 32, ("hutchpp",))
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    q = host(api.norms_hutchpp(A, G, 32, wl.seed, 0))
+    assert_rel(q, O.sqnorms_direct(inp.A, inp.G), 2e-2, "hutch++ rank-deficient")
+
+
+def test_zero_gradients(api):
+    wl = W.Workload(121, "zeros", 2, 130, 64, 64, "bf16", 1e-2, 1.0, 1.0, 8, ())
+    A = torch.zeros(2, 130, 64, dtype=torch.bfloat16, device="cuda")
+    G = torch.zeros_like(A)
+    for q in (api.norms_exact(A, G, method=1), api.norms_exact(A, G, method=2),
+              api.norms_hutch(A, G, 8, 1, 0), api.norms_hutchpp(A, G, 8, 1, 0)):
+        assert np.all(host(q) == 0.0)
+    grad, s, c = api.clipped_noisy_grad(A, G, torch.zeros(2, device="cuda"), 1.0, 0.0, 1, 0)
+    assert np.all(host(grad) == 0.0) and np.all(host(s) == 1.0) and not host(c).any()
+
+
+def test_results_are_deterministic(api):
+    wl = W.Workload(122, "det", 3, 700, 256, 512, "bf16", 1e-2, 0.5, 1.0, 32, ())
+    A, G = to_dev(W.make_inputs(wl))
+    for f in (lambda: api.norms_hutch(A, G, 32, 5, 1), lambda: api.norms_hutchpp(A, G, 32, 5, 1),
+              lambda: api.norms_exact(A, G, method=1), lambda: api.norms_exact(A, G, method=2)):
+        assert torch.equal(f(), f())
+    q = api.norms_hutch(A, G, 32, 5, 1)
+    g1 = api.clipped_noisy_grad(A, G, q, 0.5, 1.0, 9, 4)[0]
+    g2 = api.clipped_noisy_grad(A, G, q, 0.5, 1.0, 9, 4)[0]
+    assert torch.equal(g1, g2)
+
+
+# ----------------------------------------------------------------------------- standard workloads
+
+def test_exact_workload_ghost_vs_direct(api):
+    inp = W.make_inputs(W.get(2))
+    wl = inp.wl
+    A, G = to_dev(inp)
+    ref = oracle_all(inp, want=())
+    tol = TOL["bf16"]
+    q_g = host(api.norms_exact(A, G, method=1))
+    q_d = host(api.norms_exact(A, G, method=2))
+    assert_rel(q_g, ref["direct"], tol, "ghost")
+    assert_rel(q_d, ref["direct"], tol, "direct")
+    assert_rel(q_g, q_d, 1e-3, "ghost vs direct")
+    check_grad(api, inp, A, G, q_d, wl.C, wl.sigma, ref["Ms"])
+    C_med = float(np.median(np.sqrt(ref["direct"])))
+    check_grad(api, inp, A, G, ref["direct"], C_med, 0.0, ref["Ms"])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("wid", [3, 4, 5])
+def test_full_size_workloads(api, wid):
+    inp = W.make_inputs(W.get(wid))
+    wl = inp.wl
+    A, G = to_dev(inp)
+    want = tuple(r for r in wl.runs if r in ("hutch", "hutchpp"))
+    ref = oracle_all(inp, want=want)
+    tol = TOL["bf16"]
+    q_h = api.norms_hutch(A, G, wl.k, wl.seed, 0)
+    assert_rel(host(q_h), ref["hutch"], tol, "hutch")
+    if "hutchpp" in wl.runs:
+        assert_rel(host(api.norms_hutchpp(A, G, wl.k, wl.seed, 0)), ref["hutchpp"], tol, "hutch++")
+    if "direct" in wl.runs:
+        assert_rel(host(api.norms_exact(A, G, method=2)), ref["direct"], tol, "direct")
+    check_grad(api, inp, A, G, host(q_h), wl.C, wl.sigma, ref["Ms"])
+
+
+# ----------------------------------------------------------------------------- failure path
+
+def test_bounded_wait_reports_timeout_and_context_survives(api):
+    from dp_sgd_clipping_gb300 import _lib as L
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    api.selftest_wait_timeout(ws, 20000)
+    assert api.workspace_status(ws) == L.ERR_TIMEOUT
+    # the context is still usable afterwards
+    z = api.philox_normal(1024, 1, 0, 0)
+    torch.cuda.synchronize()
+    assert torch.isfinite(z).all()
+    ws2 = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    A = torch.ones(1, 8, 8, dtype=torch.bfloat16, device="cuda")
+    q = api.norms_hutch(A, A, 4, 1, 0, ws=ws2)
+    assert api.workspace_status(ws2) == 0
+    assert torch.isfinite(q).all()
