@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the per-linear-layer DP-SGD clipping path on GB300.
+
+Workload: the MLP up_proj shape of a Llama-3.2-1B layer, B=4 sequences of
+T=4096 tokens, d=2048 inputs, p=8192 outputs, bf16 activations/gradients with
+fp32 accumulation, k=32 probes, C=0.5, sigma=0.8 (synthetic inputs from the
+seeded generator).  One step runs every row of the hot path once:
+  Hutch norms (probe generation, sketch G P, projection A^T(GP), reduction),
+  Hutch++ norms (3 sweeps + QR), exact direct norms, exact ghost norms,
+  clip scales + clipped noisy gradient (with the Hutch norms).
+Metric: tokens per second of that step (B*T tokens per step), whole job.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dpclip|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step), timing is the max over ranks and `value` sums
+the tokens of all ranks.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_ID = 4
+METRIC = "clip+noise tokens/s per linear layer (Hutch/Hutch++/exact); % bf16 tensor peak"
+ROWS = ("hutch", "hutchpp", "exact_direct", "exact_ghost", "clipped_noisy_grad")
+# kernels each ABI call launches for bf16 inputs (memsets of the control block excluded)
+LAUNCHES = {"hutch": 3, "hutchpp": 9, "exact_direct": 1, "exact_ghost": 1, "clipped_noisy_grad": 1}
+
+
+def algorithmic_work(wl):
+    """Per-call algorithmic work of each row: (amount, unit, bound).
+    Bytes are the compulsory HBM reads of A and G (bf16) plus outputs;
+    flops are 2 per multiply-add of the defining products."""
+    B, T, d, p, k = wl.B, wl.T, wl.d, wl.p, wl.k
+    ag = 2.0 * B * T * (d + p)
+    return {
+        "hutch": (ag + 2.0 * k * p, "bytes", "hbm"),
+        "hutchpp": (3.0 * ag, "bytes", "hbm"),
+        "exact_direct": (2.0 * B * T * d * p, "flops", "tensor"),
+        "exact_ghost": (1.0 * B * T * (T + 1) * (d + p), "flops", "tensor"),
+        "clipped_noisy_grad": (2.0 * B * T * d * p, "flops", "tensor"),
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clocks and throttle reasons."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[5:]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
+        use = inside or sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in use for j, v in enumerate(r[3][1:5]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_window": len(inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(wl, tokens: int, p_cols: int, reps: int = 1):
+    """Times the fp64 oracle (as it stands) on a bounded sample of the
+    workload: the first `tokens` tokens of sample 0 and the first `p_cols`
+    output columns, running every row.  Returns (tokens/s scaled to full
+    width, seconds, threads, sample description)."""
+    import oracle as O
+    from dp_sgd_clipping_gb300 import workloads as W
+    sub = wl.with_(B=1, T=tokens, p=p_cols)
+    inp = W.make_inputs(sub)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        Ms = list(O.per_sample_grads(inp.A, inp.G))
+        O.sqnorms_ghost(inp.A, inp.G)
+        q_exact = np.array([np.sum(M * M) for M in Ms])
+        P = O.hutch_probe(sub.p, sub.k, sub.seed, 0, "bf16")
+        q_h = O.sqnorms_hutch(None, None, P, Ms=Ms)
+        S, Gp = O.hutchpp_probes(sub.p, sub.k, sub.seed, 0, "bf16")
+        O.sqnorms_hutchpp(None, None, S, Gp, Ms=Ms)
+        O.clipped_noisy_grad(None, None, q_h, sub.C, sub.sigma, sub.seed, 0, Ms=Ms)
+        times.append(time.perf_counter() - t0)
+        del q_exact
+    t = statistics.median(times)
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    value = tokens * (p_cols / wl.p) / t
+    desc = (f"sample 0, first {tokens} of {wl.T} tokens, first {p_cols} of {wl.p} output columns, "
+            f"all rows (exact direct+ghost, Hutch, Hutch++, clip, noisy grad); tokens/s scaled "
+            f"by the column fraction; numpy fp64 with its BLAS on all host threads")
+    return value, t, threads, desc
+
+
+def run_reference(args, world, rank):
+    """The oracle arm: rank 0 times the fp64 CPU oracle; other ranks idle."""
+    from dp_sgd_clipping_gb300 import workloads as W
+    if rank != 0:
+        return
+    wl = W.get(WORKLOAD_ID)
+    tok, cols = 512, 1024
+    for _ in range(args.warmup):
+        cpu_baseline(wl, tok, cols)
+    t_total = 0.0
+    vals = []
+    for _ in range(args.steps):
+        v, t, threads, desc = cpu_baseline(wl, tok, cols)
+        t_total += t
+        vals.append(v)
+    value = tok * (cols / wl.p) * args.steps / t_total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "d": wl.d, "p": wl.p, "k": wl.k,
+            "C": wl.C, "sigma": wl.sigma, "step": list(ROWS),
+            "l2": "inputs larger than L2 (A+G = %.0f MB bf16 > 129 MB)"
+                  % (2 * wl.B * wl.T * (wl.d + wl.p) / 1e6),
+            "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="dpclip", choices=("dpclip", "reference"))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", default=",".join(ROWS),
+                    help="comma-separated subset of rows (default: all, the full step)")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from dp_sgd_clipping_gb300 import api
+    from dp_sgd_clipping_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    rows = tuple(r for r in args.rows.split(",") if r)
+    wl = W.get(WORKLOAD_ID)
+    inp = W.make_inputs(wl)
+    A_h = torch.from_numpy(inp.A_dev.view(np.int16)).view(torch.bfloat16).pin_memory()
+    G_h = torch.from_numpy(inp.G_dev.view(np.int16)).view(torch.bfloat16).pin_memory()
+    A = A_h.to(dev)
+    G = G_h.to(dev)
+    B, T, d, p, k = wl.B, wl.T, wl.d, wl.p, wl.k
+    f32 = dict(dtype=torch.float32, device=dev)
+    q_h, q_pp, q_d, q_g = (torch.empty(B, **f32) for _ in range(4))
+    grad = torch.empty(d, p, **f32)
+    scales = torch.empty(B, **f32)
+    clipped = torch.empty(B, dtype=torch.uint8, device=dev)
+    from dp_sgd_clipping_gb300 import _lib as L
+
+    def ws_for(op, param):
+        n = api.workspace_bytes(op, B, T, d, p, L.BF16, param)
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+
+    ws = {"hutch": ws_for(L.OP_NORMS_HUTCH, k), "hutchpp": ws_for(L.OP_NORMS_HUTCHPP, k),
+          "exact_direct": ws_for(L.OP_NORMS_EXACT, L.EXACT_DIRECT),
+          "exact_ghost": ws_for(L.OP_NORMS_EXACT, L.EXACT_GHOST),
+          "clipped_noisy_grad": ws_for(L.OP_CLIPPED_NOISY_GRAD, 0)}
+    stream = torch.cuda.current_stream(dev)
+
+    def row_fn(name, step):
+        if name == "hutch":
+            return lambda: api.norms_hutch(A, G, k, wl.seed, step, out=q_h, ws=ws[name])
+        if name == "hutchpp":
+            return lambda: api.norms_hutchpp(A, G, k, wl.seed, step, out=q_pp, ws=ws[name])
+        if name == "exact_direct":
+            return lambda: api.norms_exact(A, G, L.EXACT_DIRECT, out=q_d, ws=ws[name])
+        if name == "exact_ghost":
+            return lambda: api.norms_exact(A, G, L.EXACT_GHOST, out=q_g, ws=ws[name])
+        return lambda: api.clipped_noisy_grad(A, G, q_h, wl.C, wl.sigma, wl.seed, step, grad=grad,
+                                              scales=scales, clipped=clipped, ws=ws[name])
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---------------------------------------------------------------- device-resident timing
+    for s in range(args.warmup):
+        for r in rows:
+            row_fn(r, s)()
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    smi_index = int(vis[local]) if local < len(vis) and vis[local].strip().isdigit() else local
+    clocks = ClockSampler(smi_index)
+    if rank == 0:
+        clocks.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(rows) + 1)]
+          for _ in range(args.steps)]
+    barrier()
+    wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        for j, r in enumerate(rows):
+            row_fn(r, args.warmup + s)()
+            ev[s][j + 1].record(stream)
+    end.record(stream)
+    barrier()
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1) if rank == 0 else None
+    elapsed_ms = start.elapsed_time(end)
+    for name in rows:
+        st = api.workspace_status(ws[name])
+        if st != 0:
+            raise SystemExit(f"{name}: device reported status {st}")
+    row_ms = {r: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
+              for j, r in enumerate(rows)}
+    if pg is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # ---------------------------------------------------------------- end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        outs_h = {"q": torch.empty(4, B, dtype=torch.float32).pin_memory(),
+                  "grad": torch.empty(d, p, dtype=torch.float32).pin_memory(),
+                  "scales": torch.empty(B, dtype=torch.float32).pin_memory(),
+                  "clipped": torch.empty(B, dtype=torch.uint8).pin_memory()}
+        qs = torch.empty(4, B, **f32)
+
+        def e2e_step(s):
+            A.copy_(A_h, non_blocking=True)
+            G.copy_(G_h, non_blocking=True)
+            for r in rows:
+                row_fn(r, s)()
+            for j, q in enumerate((q_h, q_pp, q_d, q_g)):
+                qs[j].copy_(q)
+            outs_h["q"].copy_(qs, non_blocking=True)
+            outs_h["grad"].copy_(grad, non_blocking=True)
+            outs_h["scales"].copy_(scales, non_blocking=True)
+            outs_h["clipped"].copy_(clipped, non_blocking=True)
+
+        for s in range(args.warmup):
+            e2e_step(s)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(args.steps):
+            e2e_step(args.warmup + s)
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        if pg is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = A_h.numel() * 2 + G_h.numel() * 2
+        d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+        e2e = {"value": world * B * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    if rank != 0:
+        if pg is not None:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+
+    # ---------------------------------------------------------------- roofline and report
+    peaks = load_peaks()
+    work = algorithmic_work(wl)
+    breakdown = {}
+    for r in rows:
+        amount, unit, bound = work[r]
+        ms = row_ms[r]
+        if unit == "bytes":
+            ach, pk, u = amount / (ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            ach, pk, u = amount / (ms * 1e-3) / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+        breakdown[r] = {"ms": round(ms, 4), "tokens_per_s": B * T / (ms * 1e-3),
+                        "bound": bound, "achieved": round(ach, 2), "peak": pk, "unit": u,
+                        "frac": round(ach / pk, 4), "algorithmic": amount}
+    dom = max(rows, key=lambda r: row_ms[r])
+    traffic = _traffic_from_profiles(dom)
+    roof = dict(breakdown[dom])
+    roofline = {"kernel": dom, "bound": roof["bound"], "achieved": roof["achieved"],
+                "peak": roof["peak"], "unit": roof["unit"], "frac": roof["frac"],
+                "traffic": traffic, "peak_source": peaks["source"] + (
+                    " (sustained bf16)" if roof["unit"] == "TFLOP/s" else " (HBM copy)")}
+    ms_step = elapsed_ms / args.steps
+    line = {"metric": METRIC, "value": world * B * T * args.steps / (elapsed_ms / 1e3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl), "gpu_launches": args.steps * sum(LAUNCHES[r] for r in rows),
+            "roofline": roofline, "breakdown": breakdown, "clocks": clk, "e2e": e2e}
+    if world == 1 and not args.no_cpu_baseline:
+        v, t, threads, desc = cpu_baseline(wl, 1024, wl.p)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": round(t, 2)}
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def _traffic_from_profiles(row):
+    """DRAM bytes per launch of the row's main kernel from the committed ncu
+    summary (profiles/traffic.json), or None when no capture matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            return json.load(f).get(row)
+    except (OSError, ValueError):
+        return None
+
+
+if __name__ == "__main__":
+    main()

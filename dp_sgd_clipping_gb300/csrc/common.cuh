@@ -289,4 +289,49 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   return v;
 }
 
+// Grid-level reduction of per-unit partials, run by the last CTA of the grid
+// to finish:  sq[i] = scale * sum_{u < nunits, w < nw} part[(u*su + i*si)*nw + w].
+// Every thread of every CTA calls it once at the end of the kernel.  The
+// summation order is fixed (thread partition, 8-wide batches, shuffle tree,
+// warps in order), so results do not depend on CTA timing.  `ticket` must be
+// zero at launch; the last CTA resets it.
+__device__ __forceinline__ void reduce_partials_last_cta(const float* part, int B, int nunits,
+                                                         long long su, long long si, int nw,
+                                                         float scale, float* sq,
+                                                         uint32_t* ticket, float* red_smem,
+                                                         int* flag_smem) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *flag_smem = (atomicAdd(ticket, 1u) == gridDim.x - 1u) ? 1 : 0;
+  __syncthreads();
+  if (!*flag_smem) return;
+  __threadfence();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (int)(blockDim.x >> 5);
+  const long long n = (long long)nunits * nw;
+  for (int i = 0; i < B; ++i) {
+    float acc = 0.f;
+    for (long long e0 = threadIdx.x; e0 < n; e0 += 8ll * blockDim.x) {
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const long long e = e0 + (long long)q * blockDim.x;
+        v[q] = e < n ? __ldcg(part + ((e / nw) * su + (long long)i * si) * nw + (e % nw)) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc += v[q];
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) red_smem[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float s = 0.f;
+      for (int w = 0; w < nwarps; ++w) s += red_smem[w];
+      sq[i] = scale * s;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *ticket = 0u;
+}
+
 }  // namespace dpclip

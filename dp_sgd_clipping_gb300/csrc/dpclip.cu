@@ -194,7 +194,7 @@ Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
   pl.off[kQWlo] = c.take((size_t)B * 32 * p * 2);
   pl.off[kY3hi] = c.take((size_t)B * 32 * pl.Tp * 2);
   pl.off[kY3lo] = c.take((size_t)B * 32 * pl.Tp * 2);
-  pl.off[kQ1] = c.take((size_t)B * r * p * 8);
+  pl.off[kQ1] = c.take(hpp_qr_part_floats(B, p) * 4);
   pl.off[kHPart] = c.take(part);
   pl.off[kHQpart] = c.take((size_t)B * std::max(fd, fp) * 4);
   pl.total = c.total();
@@ -247,7 +247,7 @@ Plan plan_hutchpp_f32(int B, int T, int d, int p, int k) {
   pl.off[kFU] = c.take((size_t)B * T * r * 4);
   pl.off[kFV] = c.take((size_t)B * 16 * p * 4);
   pl.off[kFQW] = c.take((size_t)B * 32 * p * 4);
-  pl.off[kFQ1] = c.take((size_t)B * r * p * 8);
+  pl.off[kFQ1] = c.take(hpp_qr_part_floats(B, p) * 4);
   pl.off[kFY3] = c.take((size_t)B * T * (r + m) * 4);
   pl.off[kFPart] = c.take((size_t)B * simt_nblocks(d, r + m) * 4);
   pl.total = c.total();
@@ -480,10 +480,11 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gp.ntiles = cdiv(p, kDpTileN);
       gp.tblocks = cdiv(T, kBlockK);
       gp.part = at<float>(ws, pl.off[0]);
+      gp.sq = sqnorms;
+      gp.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gp.err = at<uint32_t>(ws, pl.ctrl);
       const int ntiles = gp.mtiles * gp.ntiles;
       DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min(ntiles, num_sms()), s));
-      DPCLIP_CUDA(launch_finalize_norms(gp.part, B, ntiles, B, 1, kEpiWarps, 1.f, sqnorms, s));
     } else {
       GhostParams gh;
       std::memset(&gh, 0, sizeof(gh));
@@ -498,10 +499,10 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gh.dblocks = cdiv(d, kBlockK);
       gh.pblocks = cdiv(p, kBlockK);
       gh.part = at<float>(ws, pl.off[0]);
+      gh.sq = sqnorms;
+      gh.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gh.err = at<uint32_t>(ws, pl.ctrl);
       DPCLIP_CUDA(launch_ghost(gh, std::min(B * gh.npairs, num_sms()), s));
-      DPCLIP_CUDA(launch_finalize_norms(gh.part, B, gh.npairs, 1, gh.npairs, kEpiWarps, 1.f,
-                                        sqnorms, s));
     }
     return DPCLIP_OK;
   }
@@ -622,7 +623,7 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
     hq.p = p;
     hq.r = r;
     hq.m = m;
-    hq.Q1 = at<double>(ws, pl.off[kQ1]);
+    hq.part = at<float>(ws, pl.off[kQ1]);
     hq.out_hi = static_cast<__nv_bfloat16*>(QWh);
     hq.out_lo = static_cast<__nv_bfloat16*>(QWl);
     hq.err = at<uint32_t>(ws, pl.ctrl);
@@ -684,7 +685,7 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
   hq.p = p;
   hq.r = r;
   hq.m = m;
-  hq.Q1 = at<double>(ws, pl.off[kFQ1]);
+  hq.part = at<float>(ws, pl.off[kFQ1]);
   hq.out_f32 = QW;
   hq.err = at<uint32_t>(ws, pl.ctrl);
   DPCLIP_CUDA(launch_hpp_qr(hq, s));

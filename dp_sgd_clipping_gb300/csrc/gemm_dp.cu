@@ -43,6 +43,8 @@ struct Ctl {
   int issued;
   int consumed;
   int mma_units;     // units whose MMAs were committed to tfull
+  int is_last;
+  float red[kThreads / 32];
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kABytes + kGBytes) + sizeof(Ctl);
@@ -244,6 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
       }
     }
   }
+
+  if (!kGrad)
+    reduce_partials_last_cta(p.part, p.B, ntiles_total, p.B, 1, kEpiWarps, 1.f, p.sq, p.ticket,
+                             ctl->red, &ctl->is_last);
 
   tc_fence_before();
   __syncthreads();

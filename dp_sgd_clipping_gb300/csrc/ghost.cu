@@ -8,7 +8,7 @@
 // accumulators of 128 x 128 fp32: X = A_a A_b^T (K = d) then Y = G_a G_b^T
 // (K = p), both K-major TMA tiles with 128-byte swizzle.  The epilogue forms
 // sum(X o Y), doubled off the diagonal (the (b, a) block is the transpose),
-// and writes one partial per unit and epilogue warp; a second small kernel
+// and writes one partial per unit and epilogue warp; the last CTA to finish
 // adds the partials of each sample in a fixed order.  Two accumulator pairs
 // (512 TMEM columns) alternate between units.
 //
@@ -33,6 +33,8 @@ struct Ctl {
   int issued;
   int consumed;
   int mma_units;
+  int is_last;
+  float red[kThreads / 32];
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * 2 * kTileBytes + sizeof(Ctl);
@@ -174,6 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       if (lane == 0) p.part[(size_t)u * kEpiWarps + ew] = (a == b) ? s : 2.f * s;
     }
   }
+
+  reduce_partials_last_cta(p.part, p.B, p.npairs, 1, p.npairs, kEpiWarps, 1.f, p.sq, p.ticket,
+                           ctl->red, &ctl->is_last);
 
   tc_fence_before();
   __syncthreads();

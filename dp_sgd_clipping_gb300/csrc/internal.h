@@ -80,6 +80,8 @@ struct GemmDpParams {
   float* scales;
   uint8_t* clipped;
   float* part;
+  float* sq;             // norm mode: per-sample result [B]
+  uint32_t* ticket;      // norm mode: zeroed grid ticket
   uint32_t* err;
 };
 
@@ -91,19 +93,22 @@ struct GhostParams {
   int B, T, d, p;
   int ntt, npairs, dblocks, pblocks;
   float* part;
+  float* sq;             // per-sample result [B]
+  uint32_t* ticket;      // zeroed grid ticket
   uint32_t* err;
 };
 
 // Hutch++ middle step: per sample, orthonormal basis Q of V (p x r) by
-// pivoted CholeskyQR2 in fp64, W = G' - Q (Q^T G'), output [Q | W] padded
-// to 32 columns, as hi/lo bf16 or fp32, [B][32][p].
+// pivoted CholeskyQR2 (fp32), W = G' - Q (Q^T G'), output [Q | W] padded to
+// 32 columns, as hi/lo bf16 or fp32, [B][32][p].  Cooperative launch.
 struct HppQrParams {
   const float* V;        // [B][ldv][p] fp32, columns j < r used
   int ldv;
   const void* Gp;        // [m][p], bf16 or fp32 (gp_bf16)
   int gp_bf16;
   int B, p, r, m;
-  double* Q1;            // [B][r][p] fp64 scratch
+  float* part;           // hpp_qr_part_floats(B, p) fp32 scratch
+  int cps, sample0;      // set by the launcher: CTAs per sample, first sample
   __nv_bfloat16* out_hi; // bf16 output (when out_f32 == nullptr)
   __nv_bfloat16* out_lo;
   float* out_f32;        // fp32 output [B][32][p]
@@ -142,6 +147,7 @@ cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s);
 cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cudaStream_t s);
 cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s);
 cudaError_t launch_hpp_qr(const HppQrParams& p, cudaStream_t s);
+size_t hpp_qr_part_floats(int B, int p);
 cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblocks_out);
 int simt_nblocks(int M, int N);
 

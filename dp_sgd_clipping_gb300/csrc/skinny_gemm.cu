@@ -71,6 +71,23 @@ __device__ void drain_after_abort(SmemCtl* ctl) {
     if (globaltimer_ns() - t0 > lim) break;
 }
 
+// Sum over the K-splits of one tile row: acc[j] = sum_s base[s*split_stride + j*ld].
+// Each split's NP loads are issued together (one L2 round trip per split,
+// not per element); splits are added in index order (deterministic).
+template <int NP>
+__device__ __forceinline__ void sum_split_partials(const float* base, size_t split_stride, int ld,
+                                                   int splits, float (&acc)[NP]) {
+#pragma unroll
+  for (int j = 0; j < NP; ++j) acc[j] = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    float v[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) v[j] = __ldcg(base + (size_t)s * split_stride + (size_t)j * ld);
+#pragma unroll
+    for (int j = 0; j < NP; ++j) acc[j] += v[j];
+  }
+}
+
 // ---------------------------------------------------------------------------
 // tok_gemm
 // ---------------------------------------------------------------------------
@@ -184,13 +201,12 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
     __syncthreads();
     if (ctl->is_last) {
       __threadfence();
+      float acc[NP];
+      sum_split_partials<NP>(p.part + (size_t)i * plane + t, (size_t)p.B * plane, p.Tp, p.splits, acc);
 #pragma unroll
       for (int j = 0; j < NP; ++j) {
-        float acc = 0.f;
-        for (int s = 0; s < p.splits; ++s)
-          acc += __ldcg(p.part + ((size_t)s * p.B + i) * plane + (size_t)j * p.Tp + t);
         __nv_bfloat16 hi, lo;
-        split_hilo(acc, hi, lo);
+        split_hilo(acc[j], hi, lo);
         p.out_hi[(size_t)i * plane + (size_t)j * p.Tp + t] = hi;
         p.out_lo[(size_t)i * plane + (size_t)j * p.Tp + t] = lo;
       }
@@ -319,13 +335,10 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
     have_final = ctl->is_last != 0;
     if (have_final) {
       __threadfence();
+      float acc[NP];
+      sum_split_partials<NP>(p.part + (size_t)i * plane + f, (size_t)p.B * plane, p.Fp, p.splits, acc);
 #pragma unroll
-      for (int j = 0; j < NP; ++j) {
-        float acc = 0.f;
-        for (int s = 0; s < p.splits; ++s)
-          acc += __ldcg(p.part + ((size_t)s * p.B + i) * plane + (size_t)j * p.Fp + f);
-        z[j] = acc;
-      }
+      for (int j = 0; j < NP; ++j) z[j] = acc[j];
       if (threadIdx.x == 0) p.counters[tile] = 0u;
     }
   }
@@ -352,16 +365,26 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
       v = warp_sum(v);
       if (lane == 0) ctl->red[warp] = v;
       __syncthreads();
+      uint32_t* cnt = p.counters + (size_t)p.B * p.ftiles + i;
       if (threadIdx.x == 0) {
         const float tile_sum = ((ctl->red[0] + ctl->red[1]) + ctl->red[2]) + ctl->red[3];
         p.qpart[(size_t)i * p.ftiles + ft] = tile_sum;
         __threadfence();
-        uint32_t* cnt = p.counters + (size_t)p.B * p.ftiles + i;
         const uint32_t prev = atomicAdd(cnt, 1u);
-        if (prev == (uint32_t)p.ftiles - 1u) {
-          __threadfence();
-          float q = 0.f;
-          for (int u = 0; u < p.ftiles; ++u) q += __ldcg(p.qpart + (size_t)i * p.ftiles + u);
+        ctl->is_last = (prev == (uint32_t)p.ftiles - 1u);
+      }
+      __syncthreads();
+      if (ctl->is_last && warp == 0) {
+        // the last tile of the sample adds the per-tile sums: lane-parallel
+        // loads, then a fixed shuffle tree (deterministic)
+        __threadfence();
+        float q = 0.f;
+        for (int u0 = 0; u0 < p.ftiles; u0 += 32) {
+          const int u = u0 + lane;
+          q += u < p.ftiles ? __ldcg(p.qpart + (size_t)i * p.ftiles + u) : 0.f;
+        }
+        q = warp_sum(q);
+        if (lane == 0) {
           p.sq[i] = q;
           *cnt = 0u;
         }

@@ -27,12 +27,25 @@ def assert_rel(got, ref, tol, what=""):
     assert np.all(rel <= tol), f"{what}: max rel err {rel.max():.3e} > {tol} (got {got}, ref {ref})"
 
 
-def assert_grad(got, ref, tol, sigmaC, what="grad"):
+def grad_magnitude(A, G, s):
+    """sum_i s_i |A_i|^T |G_i|: the sum of absolute terms behind each entry of
+    the clipped sum, which bounds the rounding error of a fp32 accumulation
+    (|error| <= K eps * sum |terms| for a dot product of length K)."""
+    mag = None
+    for i in range(A.shape[0]):
+        t = s[i] * (np.abs(A[i]).astype(np.float64).T @ np.abs(G[i]).astype(np.float64))
+        mag = t if mag is None else mag + t
+    return mag
+
+
+def assert_grad(got, ref, tol, sigmaC, what="grad", mag=None):
+    """Normwise max|err| / max|ref| <= tol, and per entry
+    |err| <= tol * (|ref| + sigma C + magnitude of the summed terms)."""
     got = np.asarray(got, dtype=np.float64)
     err = np.abs(got - ref)
     normwise = err.max() / np.abs(ref).max()
     assert normwise <= tol, f"{what}: normwise error {normwise:.3e} > {tol}"
-    bound = tol * (np.abs(ref) + sigmaC)
+    bound = tol * (np.abs(ref) + sigmaC + (0.0 if mag is None else mag))
     bad = err > bound
     assert not bad.any(), f"{what}: {bad.sum()} entries outside tol*(|ref|+sigma*C)"
 

@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 from dp_sgd_clipping_gb300 import workloads as W
-from gpu_util import TOL, assert_flags, assert_grad, assert_rel, host, to_dev
+from gpu_util import TOL, assert_flags, assert_grad, assert_rel, grad_magnitude, host, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def check_grad(api, inp, A, G, q, C, sigma, Ms, offset=0):
     D, s_ref, _ = O.clipped_noisy_grad(None, None, q32, C, sigma, wl.seed, offset, Ms=Ms)
     assert_rel(host(scales), s_ref, 1e-6, "scales")
     assert_flags(host(clipped), np.sqrt(q32), C, tol)
-    assert_grad(host(grad), D, tol, sigma * C)
+    assert_grad(host(grad), D, tol, sigma * C, mag=grad_magnitude(inp.A, inp.G, s_ref))
     return grad
 
 
