@@ -24,6 +24,7 @@ EXACT_AUTO, EXACT_GHOST, EXACT_DIRECT = 0, 1, 2
 OP_NORMS_EXACT, OP_NORMS_HUTCH, OP_NORMS_HUTCHPP, OP_CLIPPED_NOISY_GRAD = 0, 1, 2, 3
 HUTCH_MAX_K = 32
 HUTCHPP_MAX_K = 48
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _c = ctypes
 _vp, _i, _u64, _u32, _i64, _f = _c.c_void_p, _c.c_int, _c.c_uint64, _c.c_uint32, _c.c_int64, _c.c_float
@@ -38,6 +39,7 @@ SIGNATURES = {
     "dpclip_clipped_noisy_grad": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _f, _u64, _u64,
                                        _vp, _vp, _vp, _vp, _sz, _vp]),
     "dpclip_clip_scales": (_i, [_vp, _i, _f, _vp, _vp, _vp]),
+    "dpclip_norms_hutch_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp]),
     "dpclip_philox_normal": (_i, [_vp, _i64, _i, _u64, _u32, _u64, _vp]),
     "dpclip_workspace_status": (_i, [_vp, _vp]),
     "dpclip_selftest_wait_timeout": (_i, [_vp, _sz, _i, _vp]),

@@ -142,6 +142,31 @@ int dpclip_clip_scales(const float* sqnorms, int B, float C, float* scales, uint
 int dpclip_philox_normal(void* out, int64_t n, int dtype, uint64_t seed, uint32_t stream_id,
                          uint64_t offset, dpclip_stream_t stream);
 
+/* Size of the library-owned scratch array behind dpclip_norms_hutch_noalloc
+ * (16 MiB; covers Hutch with k <= 32 at B*T = 16384 tokens and d, p up to
+ * 2048 x 8192, for example). */
+#define DPCLIP_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* dpclip_norms_hutch without a caller workspace and without any allocation.
+ * The pages have no counterpart for this: it exists for callers that cannot
+ * allocate device memory where they need the norms (a host framework calling
+ * from a callback in which device allocation is forbidden after set-up, a
+ * process whose device memory is all handed out by another allocator, a
+ * latency-critical loop where an allocation could stall on the device).
+ * Arguments and result as dpclip_norms_hutch.  Scratch is a library-owned
+ * device array of DPCLIP_NOALLOC_SCRATCH_BYTES, created on every GPU that
+ * loads the library and held until the process exits.  Sizes whose Hutch
+ * workspace (dpclip_workspace_size) exceeds it return DPCLIP_ERR_WORKSPACE
+ * before anything is enqueued.  The first call on a device looks up the
+ * array's device address with that device current; make that first call
+ * before any stream capture.  Every call shares the array and it keeps the
+ * last call's contents (each call clears what must start at zero): calls that
+ * can overlap on the GPU race on it, so issue them on one stream.  Never calls
+ * cudaMalloc, cudaFree or any allocating routine. */
+int dpclip_norms_hutch_noalloc(const void* A, const void* G, int B, int T, int d, int p,
+                               int dtype, int k, uint64_t seed, uint64_t offset, float* sqnorms,
+                               dpclip_stream_t stream);
+
 /* Synchronises `stream`, then returns DPCLIP_OK or the error the device
  * recorded in the workspace of the last call that used it
  * (DPCLIP_ERR_TIMEOUT), or DPCLIP_ERR_CUDA if the synchronisation failed. */
