@@ -300,10 +300,7 @@ def main():
             raise SystemExit(f"{name}: device reported status {st}")
     row_ms = {r: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
               for j, r in enumerate(rows)}
-    if pg is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
 
     # ---------------------------------------------------------------- end to end, host buffers
     e2e = None
@@ -337,13 +334,10 @@ def main():
         e1.record(stream)
         barrier()
         e2e_ms = e0.elapsed_time(e1)
-        if pg is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, pg, dev)
         h2d = A_h.numel() * 2 + G_h.numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
-        e2e = {"value": world * B * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": job_tokens_per_s(world, B * T, args.steps, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps}
 
@@ -375,7 +369,7 @@ def main():
                 "traffic": traffic, "peak_source": peaks["source"] + (
                     " (sustained bf16)" if roof["unit"] == "TFLOP/s" else " (HBM copy)")}
     ms_step = elapsed_ms / args.steps
-    line = {"metric": METRIC, "value": world * B * T * args.steps / (elapsed_ms / 1e3),
+    line = {"metric": METRIC, "value": job_tokens_per_s(world, B * T, args.steps, elapsed_ms),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -391,15 +385,44 @@ def main():
         pg.destroy_process_group()
 
 
+def _sha256(path):
+    import hashlib
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
 def _traffic_from_profiles(row):
     """DRAM bytes per launch of the row's main kernel from the committed ncu
-    summary (profiles/traffic.json), or None when no capture matches."""
+    summary (profiles/traffic.json), or None when there is no capture or when
+    any source file of the kernel changed since the capture (hash mismatch)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(row)
+            entry = json.load(f).get(row)
     except (OSError, ValueError):
         return None
+    if not entry:
+        return None
+    for src, digest in entry.get("sources", {}).items():
+        p = os.path.join(ROOT, src)
+        if not os.path.exists(p) or _sha256(p) != digest:
+            return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """Largest `value` over all ranks (the job's time is its slowest rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank processes its own batch each step."""
+    return world * tokens_per_step * steps / (elapsed_ms / 1e3)
 
 
 if __name__ == "__main__":

@@ -202,9 +202,14 @@ Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
 }
 
 int dp_ntiles(int d, int p) { return cdiv(d, kDpTileM) * cdiv(p, kDpTileN); }
+// ghost units per sample: for each 256-token tile b', the 128-token tiles
+// a <= 2b'+1 (bounded by the tile count).
 int ghost_npairs(int T) {
-  const int n = cdiv(T, kGhostTile);
-  return n * (n + 1) / 2;
+  const int ntt = cdiv(T, kGhostTile);
+  const int ntb = cdiv(T, 2 * kGhostTile);
+  int n = 0;
+  for (int bb = 0; bb < ntb; ++bb) n += std::min(2 * bb + 2, ntt);
+  return n;
 }
 
 Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
@@ -484,7 +489,7 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gp.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gp.err = at<uint32_t>(ws, pl.ctrl);
       const int ntiles = gp.mtiles * gp.ntiles;
-      DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min(ntiles, num_sms()), s));
+      DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min(ntiles * B, num_sms()), s));
     } else {
       GhostParams gh;
       std::memset(&gh, 0, sizeof(gh));

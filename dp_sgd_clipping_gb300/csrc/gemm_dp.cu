@@ -10,8 +10,12 @@
 //               "Problem definition", reduced on chip): partial sums of
 //               (A_i^T G_i)^2, never storing the d x p tile.
 //
-// Work unit = (output tile of 128 d-rows x 256 p-columns, sample i).  The
-// K loop of a unit runs over that sample's T tokens in blocks of 64; both
+// Work unit = (output tile of 128 d-rows x 256 p-columns, sample i).  In
+// grad mode a CTA owns whole tiles (all B samples of a tile, which it folds
+// into one running sum); in norm mode units are independent and are dealt
+// out one by one (unit u = i * ntiles + tile, CTA c takes u = c, c + grid,
+// ...), which evens out the last wave.  The K loop of a unit runs over that
+// sample's T tokens in blocks of 64; both
 // operands are MN-major (tokens are the slow axis of A and G), loaded by TMA
 // with 128-byte swizzle.  The accumulator of a unit lives in TMEM (256
 // columns); two accumulators alternate, so the epilogue of unit u overlaps
@@ -63,6 +67,22 @@ __device__ __noinline__ void noise4(uint64_t seed, uint64_t offset, uint32_t blk
   *z = make_float4(v[0], v[1], v[2], v[3]);
 }
 
+// The k-th work unit of this CTA: (tile, sample).  Returns false past the end.
+template <bool kGrad>
+__device__ __forceinline__ bool unit_at(int k, int ntiles_total, int B, int& tile, int& i) {
+  if (kGrad) {
+    tile = (int)blockIdx.x + (k / B) * (int)gridDim.x;
+    i = k % B;
+    return tile < ntiles_total;
+  }
+  // sample-major: the CTAs running at the same time work on neighbouring
+  // tiles of one sample and share its A and G slabs in L2
+  const long long u = (long long)blockIdx.x + (long long)k * gridDim.x;
+  i = (int)(u / ntiles_total);
+  tile = (int)(u % ntiles_total);
+  return u < (long long)ntiles_total * B;
+}
+
 template <bool kGrad>
 __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_constant__ GemmDpParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -110,65 +130,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       int it = 0;
-      bool run = true;
-      for (int tile = blockIdx.x; run && tile < ntiles_total; tile += gridDim.x) {
+      int tile, i;
+      for (int k = 0; unit_at<kGrad>(k, ntiles_total, p.B, tile, i); ++k) {
         const int d0 = (tile % p.mtiles) * kDpTileM;
         const int p0 = (tile / p.mtiles) * kDpTileN;
-        for (int i = 0; run && i < p.B; ++i) {
-          for (int kb = 0; kb < p.tblocks; ++kb, ++it) {
-            const int s = it % kStages;
-            if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) {
-              run = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&ctl->full[s], kABytes + kGBytes);
-            const int t0 = kb * 64;
-            uint8_t* a = sA + s * kABytes;
-            uint8_t* g = sG + s * kGBytes;
-            tma_load_3d(a, &p.map_a, &ctl->full[s], d0, t0, i);
-            tma_load_3d(a + kBox, &p.map_a, &ctl->full[s], d0 + 64, t0, i);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              tma_load_3d(g + q * kBox, &p.map_g, &ctl->full[s], p0 + 64 * q, t0, i);
-            ctl->issued = it + 1;
+        bool run = true;
+        for (int kb = 0; kb < p.tblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) {
+            run = false;
+            break;
           }
+          mbar_arrive_expect_tx(&ctl->full[s], kABytes + kGBytes);
+          const int t0 = kb * 64;
+          uint8_t* a = sA + s * kABytes;
+          uint8_t* g = sG + s * kGBytes;
+          tma_load_3d(a, &p.map_a, &ctl->full[s], d0, t0, i);
+          tma_load_3d(a + kBox, &p.map_a, &ctl->full[s], d0 + 64, t0, i);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            tma_load_3d(g + q * kBox, &p.map_g, &ctl->full[s], p0 + 64 * q, t0, i);
+          ctl->issued = it + 1;
         }
+        if (!run) break;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 256, true, true);
-      int it = 0, u = 0;
-      bool run = true;
-      for (int tile = blockIdx.x; run && tile < ntiles_total; tile += gridDim.x) {
-        for (int i = 0; run && i < p.B; ++i, ++u) {
-          const int acc = u & 1;
-          if (!mbar_wait(&ctl->tempty[acc], ((u >> 1) & 1) ^ 1, wc)) {
+      int it = 0;
+      int tile, i;
+      for (int u = 0; unit_at<kGrad>(u, ntiles_total, p.B, tile, i); ++u) {
+        const int acc = u & 1;
+        if (!mbar_wait(&ctl->tempty[acc], ((u >> 1) & 1) ^ 1, wc)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)acc * 256u;
+        bool run = true;
+        for (int kb = 0; kb < p.tblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) {
             run = false;
             break;
           }
+          ctl->consumed = it + 1;
           tc_fence_after();
-          const uint32_t dt = tmem + (uint32_t)acc * 256u;
-          for (int kb = 0; kb < p.tblocks; ++kb, ++it) {
-            const int s = it % kStages;
-            if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) {
-              run = false;
-              break;
-            }
-            ctl->consumed = it + 1;
-            tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + s * kABytes);
-            const uint32_t g0 = smem_u32(sG + s * kGBytes);
+          const uint32_t a0 = smem_u32(sA + s * kABytes);
+          const uint32_t g0 = smem_u32(sG + s * kGBytes);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              umma_bf16(dt, sdesc_sw128(a0 + kk * 2048, kBox, 1024),
-                        sdesc_sw128(g0 + kk * 2048, kBox, 1024), idesc, (kb | kk) != 0);
-            }
-            umma_commit(&ctl->empty[s]);
+          for (int kk = 0; kk < 4; ++kk) {
+            umma_bf16(dt, sdesc_sw128(a0 + kk * 2048, kBox, 1024),
+                      sdesc_sw128(g0 + kk * 2048, kBox, 1024), idesc, (kb | kk) != 0);
           }
-          umma_commit(&ctl->tfull[acc]);
-          ctl->mma_units = u + 1;
+          umma_commit(&ctl->empty[s]);
         }
+        umma_commit(&ctl->tfull[acc]);
+        ctl->mma_units = u + 1;
+        if (!run) break;
       }
     }
   } else {
@@ -179,17 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     float tot[128];
 #pragma unroll
     for (int j = 0; j < 128; ++j) tot[j] = 0.f;
-    int u = 0;
-    bool run = true;
-    for (int tile = blockIdx.x; run && tile < ntiles_total; tile += gridDim.x) {
+    int tile, i;
+    for (int u = 0; unit_at<kGrad>(u, ntiles_total, p.B, tile, i); ++u) {
       const int d0 = (tile % p.mtiles) * kDpTileM;
       const int p0 = (tile / p.mtiles) * kDpTileN;
-      for (int i = 0; i < p.B; ++i, ++u) {
+      {
         const int acc = u & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[acc], (u >> 1) & 1, wc))) {
-          run = false;
-          break;
-        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[acc], (u >> 1) & 1, wc))) break;
         tc_fence_after();
         const uint32_t taddr =
             tmem + (uint32_t)acc * 256u + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);

@@ -4,13 +4,17 @@
 // randomized-clipping summary (the ghost-clipping baseline of its "Problem
 // definition": O(T^2) per sample, no d x p tile ever formed).
 //
-// Work unit = (sample i, token tiles a <= b of 128 tokens).  Two TMEM
-// accumulators of 128 x 128 fp32: X = A_a A_b^T (K = d) then Y = G_a G_b^T
-// (K = p), both K-major TMA tiles with 128-byte swizzle.  The epilogue forms
-// sum(X o Y), doubled off the diagonal (the (b, a) block is the transpose),
-// and writes one partial per unit and epilogue warp; the last CTA to finish
-// adds the partials of each sample in a fixed order.  Two accumulator pairs
-// (512 TMEM columns) alternate between units.
+// Work unit = (sample i, token tile a of 128 tokens, token tile b' of 256
+// tokens) covering the 128 x 128 blocks (a, 2b') and (a, 2b'+1) of the Gram
+// matrices; units with a <= 2b'+1 cover the upper triangle.  Two TMEM
+// accumulators of 128 x 256 fp32 (all 512 columns): X = A_a A_b'^T (K = d)
+// then Y = G_a G_b'^T (K = p), both K-major TMA tiles with 128-byte swizzle
+// (N = 256 keeps the tensor core's shared-memory reads at 96 B/clock; a
+// 128 x 128 tile needs 128 B/clock, the SM's limit).  The epilogue forms
+// sum(X o Y) per 128 x 128 block, weighted 2 above the diagonal (the mirrored
+// block), 1 on it, 0 below, and writes one partial per unit and epilogue
+// warp; the last CTA to finish adds the partials of each sample in a fixed
+// order.
 //
 // Roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
 // owner, warps 2..9 = epilogue.
@@ -19,8 +23,8 @@
 namespace dpclip {
 namespace {
 
-constexpr int kStages = 6;
-constexpr uint32_t kTileBytes = 128 * 128;   // 128 token rows x 128 B
+constexpr int kStages = 4;
+constexpr uint32_t kTileBytes = 128 * 128;   // 128 token rows x 128 B (one K block)
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 struct Ctl {
@@ -37,30 +41,32 @@ struct Ctl {
   float red[kThreads / 32];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * 2 * kTileBytes + sizeof(Ctl);
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * 3 * kTileBytes + sizeof(Ctl);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// pair index -> (a, b), a <= b, enumerated row by row of the upper triangle.
-__device__ __forceinline__ void pair_of(int pr, int ntt, int& a, int& b) {
-  int row = 0, len = ntt;
-  while (pr >= len) {
+// unit index within a sample -> (a, b'): for b' = 0, 1, ... the tiles
+// a = 0 .. min(2b'+1, ntt-1).
+__device__ __forceinline__ void pair_of(int pr, int ntt, int& a, int& bb) {
+  int col = 0;
+  while (true) {
+    const int len = min(2 * col + 2, ntt);
+    if (pr < len) break;
     pr -= len;
-    ++row;
-    --len;
+    ++col;
   }
-  a = row;
-  b = row + pr;
+  a = pr;
+  bb = col;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constant__ GhostParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sP = smem;                              // tile of block a
-  uint8_t* sQ = sP + kStages * kTileBytes;         // tile of block b
-  Ctl* ctl = reinterpret_cast<Ctl*>(sQ + kStages * kTileBytes);
+  uint8_t* sP = smem;                              // 128 tokens of tile a
+  uint8_t* sQ = sP + kStages * kTileBytes;         // 256 tokens of tile b'
+  Ctl* ctl = reinterpret_cast<Ctl*>(sQ + kStages * 2 * kTileBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nunits = p.B * p.npairs;
@@ -71,10 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], 32 * kEpiWarps);
-    }
+    mbar_init(&ctl->tfull[0], 1);
+    mbar_init(&ctl->tempty[0], 32 * kEpiWarps);
     ctl->abort_flag = 0;
     ctl->issued = 0;
     ctl->consumed = 0;
@@ -106,24 +110,25 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
             run = false;
             break;
           }
-          mbar_arrive_expect_tx(&ctl->full[s], 2 * kTileBytes);
+          mbar_arrive_expect_tx(&ctl->full[s], 3 * kTileBytes);
           const bool on_a = kb < p.dblocks;
           const CUtensorMap* map = on_a ? &p.map_a : &p.map_g;
           const int k0 = (on_a ? kb : kb - p.dblocks) * kBlockK;
+          uint8_t* q = sQ + s * 2 * kTileBytes;
           tma_load_3d(sP + s * kTileBytes, map, &ctl->full[s], k0, a * kGhostTile, i);
-          tma_load_3d(sQ + s * kTileBytes, map, &ctl->full[s], k0, b * kGhostTile, i);
+          tma_load_3d(q, map, &ctl->full[s], k0, 2 * b * kGhostTile, i);
+          tma_load_3d(q + kTileBytes, map, &ctl->full[s], k0, (2 * b + 1) * kGhostTile, i);
           ctl->issued = it + 1;
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
       int it = 0, lu = 0;
       bool run = true;
       for (int u = blockIdx.x; run && u < nunits; u += gridDim.x, ++lu) {
-        const int acc = lu & 1;
-        if (!mbar_wait(&ctl->tempty[acc], ((lu >> 1) & 1) ^ 1, wc)) break;
+        if (!mbar_wait(&ctl->tempty[0], (lu & 1) ^ 1, wc)) break;
         tc_fence_after();
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
@@ -135,16 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
           tc_fence_after();
           const bool on_a = kb < p.dblocks;
           const int kl = on_a ? kb : kb - p.dblocks;
-          const uint32_t dt = tmem + (uint32_t)acc * 256u + (on_a ? 0u : 128u);
+          const uint32_t dt = tmem + (on_a ? 0u : 256u);
           const uint32_t a0 = smem_u32(sP + s * kTileBytes);
-          const uint32_t b0 = smem_u32(sQ + s * kTileBytes);
+          const uint32_t b0 = smem_u32(sQ + s * 2 * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(dt, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
                       idesc, (kl | kk) != 0);
           umma_commit(&ctl->empty[s]);
         }
-        umma_commit(&ctl->tfull[acc]);
+        umma_commit(&ctl->tfull[0]);
         ctl->mma_units = lu + 1;
       }
     }
@@ -154,26 +159,26 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
     const int half = ew >> 2;
     int lu = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lu) {
-      const int acc = lu & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[acc], (lu >> 1) & 1, wc))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[0], lu & 1, wc))) break;
       tc_fence_after();
-      int a, b;
-      pair_of(u % p.npairs, p.ntt, a, b);
-      const uint32_t base =
-          tmem + (uint32_t)acc * 256u + (uint32_t)half * 64u + ((uint32_t)(quad * 32) << 16);
+      int a, bb;
+      pair_of(u % p.npairs, p.ntt, a, bb);
+      const int b = 2 * bb + half;                   // 128-token block of these columns
+      const float w = a < b ? 2.f : (a == b ? 1.f : 0.f);
+      const uint32_t base = tmem + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
       float s = 0.f;
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
+      for (int c4 = 0; c4 < 4; ++c4) {
         float x[32], y[32];
-        tmem_ld32(base + c2 * 32, x);
-        tmem_ld32(base + 128 + c2 * 32, y);
+        tmem_ld32(base + c4 * 32, x);
+        tmem_ld32(base + 256 + c4 * 32, y);
 #pragma unroll
         for (int j = 0; j < 32; ++j) s = fmaf(x[j], y[j], s);
       }
       tc_fence_before();
-      mbar_arrive(&ctl->tempty[acc]);
+      mbar_arrive(&ctl->tempty[0]);
       s = warp_sum(s);
-      if (lane == 0) p.part[(size_t)u * kEpiWarps + ew] = (a == b) ? s : 2.f * s;
+      if (lane == 0) p.part[(size_t)u * kEpiWarps + ew] = w * s;
     }
   }
 
@@ -189,11 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       while (!mbar_try_wait(&ctl->full[it % kStages], (uint32_t)(it / kStages) & 1u))
         if (globaltimer_ns() - t0 > lim) break;
     }
-    for (int a = 0; a < 2; ++a) {
-      const int last_u = ctl->mma_units - 1 - ((ctl->mma_units - 1 - a) & 1);
-      if (last_u < 0) continue;
+    if (ctl->mma_units > 0) {
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&ctl->tfull[a], (uint32_t)(last_u >> 1) & 1u))
+      while (!mbar_try_wait(&ctl->tfull[0], (uint32_t)(ctl->mma_units - 1) & 1u))
         if (globaltimer_ns() - t0 > lim) break;
     }
   }

@@ -221,22 +221,42 @@ __global__ void __launch_bounds__(kThreads) hpp_qr_kernel(const __grid_constant_
   float* part2 = p.part + ((size_t)1 * p.B + (active ? i : 0)) * cps * kMaxE;
   float* part3 = p.part + ((size_t)2 * p.B + (active ? i : 0)) * cps * kMaxE;
 
-  // ---- stage this CTA's rows of V (r columns) and G' (m columns)
-  for (int idx = threadIdx.x; idx < kMaxR * kRows; idx += kThreads) {
-    const int a = idx / kRows, c = idx % kRows;
-    float v = 0.f;
-    if (active && a < r && c0 + c < p.p) v = p.V[((size_t)i * p.ldv + a) * p.p + c0 + c];
-    sm.x[a][c] = v;
-  }
-  for (int idx = threadIdx.x; idx < kMaxM * kRows; idx += kThreads) {
-    const int l = idx / kRows, c = idx % kRows;
-    float v = 0.f;
-    if (active && l < m && c0 + c < p.p) {
-      const size_t o = (size_t)l * p.p + c0 + c;
-      v = p.gp_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.Gp)[o])
-                    : static_cast<const float*>(p.Gp)[o];
+  // ---- stage this CTA's rows of V (r columns) and G' (m columns); the loads
+  // of 16 consecutive elements per thread are issued before any is stored
+  constexpr int kBatch = 16;
+  for (int it0 = 0; it0 < kMaxR * kRows; it0 += kBatch * kThreads) {
+    float v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int idx = it0 + u * kThreads + threadIdx.x;
+      const int a = idx / kRows, c = idx % kRows;
+      v[u] = (active && a < r && c0 + c < p.p) ? p.V[((size_t)i * p.ldv + a) * p.p + c0 + c] : 0.f;
     }
-    sm.g[l][c] = v;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int idx = it0 + u * kThreads + threadIdx.x;
+      sm.x[idx / kRows][idx % kRows] = v[u];
+    }
+  }
+  for (int it0 = 0; it0 < kMaxM * kRows; it0 += kBatch * kThreads) {
+    float v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int idx = it0 + u * kThreads + threadIdx.x;
+      const int l = idx / kRows, c = idx % kRows;
+      float x = 0.f;
+      if (idx < kMaxM * kRows && active && l < m && c0 + c < p.p) {
+        const size_t o = (size_t)l * p.p + c0 + c;
+        x = p.gp_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.Gp)[o])
+                      : static_cast<const float*>(p.Gp)[o];
+      }
+      v[u] = x;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int idx = it0 + u * kThreads + threadIdx.x;
+      if (idx < kMaxM * kRows) sm.g[idx / kRows][idx % kRows] = v[u];
+    }
   }
   __syncthreads();
 
