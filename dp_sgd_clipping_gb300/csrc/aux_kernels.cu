@@ -1,6 +1,8 @@
 // Small kernels of the clipping path: Philox probe fill, clip scales,
 // deterministic reduction of per-tile norm partials, gradient noise for the
 // fp32 path and the bounded-wait self-test.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dpclip {
@@ -11,7 +13,13 @@ namespace {
 // e % 4), zeros below.  One thread per Philox block of four elements.
 template <bool kBf16>
 __global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
-                                   uint64_t seed, uint32_t stream_id, uint64_t offset) {
+                                   uint64_t seed, uint32_t stream_id, uint64_t offset,
+                                   uint32_t* zero, int zero_words) {
+  pdl_trigger();
+  pdl_wait();
+  if (zero)
+    for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < zero_words; w += gridDim.x * blockDim.x)
+      zero[w] = 0u;
   const int64_t nvalid = rows_valid * cols, ntotal = rows * cols;
   const int64_t nblk = (ntotal + 3) / 4;
   for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblk;
@@ -32,6 +40,8 @@ __global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_
 }
 
 __global__ void clip_scales_kernel(const float* sq, int B, float C, float* scales, uint8_t* clipped) {
+  pdl_trigger();
+  pdl_wait();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < B; i += gridDim.x * blockDim.x) {
     const float q = sq[i];
     if (scales) scales[i] = q > 0.f ? fminf(1.f, C / sqrtf(q)) : 1.f;
@@ -44,6 +54,8 @@ __global__ void clip_scales_kernel(const float* sq, int B, float C, float* scale
 __global__ void finalize_norms_kernel(const float* part, int nunits, long long su, long long si,
                                       int nw, float scale, float* sq) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x;
   const long long n = (long long)nunits * nw;
   float acc = 0.f;
@@ -63,6 +75,8 @@ __global__ void finalize_norms_kernel(const float* part, int nunits, long long s
 
 __global__ void noise_add_kernel(float* grad, long long n, float scale, uint64_t seed,
                                  uint64_t offset) {
+  pdl_trigger();
+  pdl_wait();
   const long long nblk = (n + 3) / 4;
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblk;
        b += (long long)gridDim.x * blockDim.x) {
@@ -96,30 +110,31 @@ __global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
 }  // namespace
 
 cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid, bool bf16,
-                               uint64_t seed, uint32_t stream_id, uint64_t offset, cudaStream_t s) {
+                               uint64_t seed, uint32_t stream_id, uint64_t offset, cudaStream_t s,
+                               uint32_t* zero, int zero_words) {
   const int64_t nblk = (rows * cols + 3) / 4;
   const int threads = 256;
-  const int grid = (int)std::min<int64_t>((nblk + threads - 1) / threads, 152 * 16);
-  if (grid <= 0) return cudaSuccess;
+  const int grid = (int)std::max<int64_t>(
+      1, std::min<int64_t>((nblk + threads - 1) / threads, 152 * 16));
   if (bf16)
-    philox_fill_kernel<true><<<grid, threads, 0, s>>>(out, rows, cols, rows_valid, seed, stream_id, offset);
-  else
-    philox_fill_kernel<false><<<grid, threads, 0, s>>>(out, rows, cols, rows_valid, seed, stream_id, offset);
-  return cudaGetLastError();
+    return launch_pdl(philox_fill_kernel<true>, dim3(grid), dim3(threads), 0, s, false, out, rows,
+                      cols, rows_valid, seed, stream_id, offset, zero, zero_words);
+  return launch_pdl(philox_fill_kernel<false>, dim3(grid), dim3(threads), 0, s, false, out, rows,
+                    cols, rows_valid, seed, stream_id, offset, zero, zero_words);
 }
 
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
                                cudaStream_t s) {
   const int threads = 256;
   const int grid = std::min((B + threads - 1) / threads, 1024);
-  clip_scales_kernel<<<grid, threads, 0, s>>>(sq, B, C, scales, clipped);
-  return cudaGetLastError();
+  return launch_pdl(clip_scales_kernel, dim3(grid), dim3(threads), 0, s, false, sq, B, C, scales,
+                    clipped);
 }
 
 cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long long su, long long si,
                                   int nw, float scale, float* sq, cudaStream_t s) {
-  finalize_norms_kernel<<<B, 256, 0, s>>>(part, nunits, su, si, nw, scale, sq);
-  return cudaGetLastError();
+  return launch_pdl(finalize_norms_kernel, dim3(B), dim3(256), 0, s, false, part, nunits, su, si,
+                    nw, scale, sq);
 }
 
 cudaError_t launch_noise_add(float* grad, long long n, float scale, uint64_t seed, uint64_t offset,
@@ -128,8 +143,8 @@ cudaError_t launch_noise_add(float* grad, long long n, float scale, uint64_t see
   const int threads = 256;
   const int grid = (int)std::min<long long>((nblk + threads - 1) / threads, 152 * 16);
   if (grid <= 0) return cudaSuccess;
-  noise_add_kernel<<<grid, threads, 0, s>>>(grad, n, scale, seed, offset);
-  return cudaGetLastError();
+  return launch_pdl(noise_add_kernel, dim3(grid), dim3(threads), 0, s, false, grad, n, scale, seed,
+                    offset);
 }
 
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s) {

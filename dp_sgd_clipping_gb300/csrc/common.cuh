@@ -96,6 +96,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel allows the next kernel of the
+// stream to be scheduled as soon as all of its CTAs are running
+// (pdl_trigger), and reads or writes global memory only after pdl_wait,
+// which returns once the previous kernel has completed and its writes are
+// visible.  Both are no-ops for launches without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------
 

@@ -548,11 +548,13 @@ int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p,
   DPCLIP_TRY(plan_for(DPCLIP_OP_NORMS_HUTCH, B, T, d, p, dtype, k, pl));
   DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
   cudaStream_t s = (cudaStream_t)stream;
-  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  // the first kernel clears the control block (error word, tickets)
+  uint32_t* ctrl = at<uint32_t>(ws, pl.ctrl);
+  const int ctrl_words = (int)(pl.ctrl_bytes / 4);
   if (dtype == DPCLIP_BF16) {
     const int NP = np_for(k);
     void* P = at<void>(ws, pl.off[kP]);
-    DPCLIP_CUDA(launch_philox_fill(P, NP, p, k, true, seed, 0u, offset, s));
+    DPCLIP_CUDA(launch_philox_fill(P, NP, p, k, true, seed, 0u, offset, s, ctrl, ctrl_words));
     void* Yhi = at<void>(ws, pl.off[kYhi]);
     void* Ylo = at<void>(ws, pl.off[kYlo]);
     DPCLIP_TRY(run_tok(G, B, T, p, P, nullptr, NP, false, pl, ws, pl.off[kPart], Yhi, Ylo, s));
@@ -566,7 +568,7 @@ int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p,
   const float* Gf = static_cast<const float*>(G);
   float* P = at<float>(ws, pl.off[kFP]);
   float* Y = at<float>(ws, pl.off[kFY]);
-  DPCLIP_CUDA(launch_philox_fill(P, k, p, k, false, seed, 0u, offset, s));
+  DPCLIP_CUDA(launch_philox_fill(P, k, p, k, false, seed, 0u, offset, s, ctrl, ctrl_words));
   SimtParams sp = simt_base();
   int nb = 0;
   sp.X = Gf; sp.xb = (long long)T * p; sp.xm = p; sp.xk = 1;        // G_i : (t, c)
@@ -594,13 +596,14 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
   DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
   const int r = k / 3, m = k - 2 * r;
   cudaStream_t s = (cudaStream_t)stream;
-  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  uint32_t* ctrl = at<uint32_t>(ws, pl.ctrl);
+  const int ctrl_words = (int)(pl.ctrl_bytes / 4);
   float w[kMaxNP];
   for (int j = 0; j < kMaxNP; ++j) w[j] = j < r ? 1.f : (j < r + m ? 1.f / (float)m : 0.f);
   if (dtype == DPCLIP_BF16) {
     void* S = at<void>(ws, pl.off[kS]);
     void* Gp = at<void>(ws, pl.off[kGp]);
-    DPCLIP_CUDA(launch_philox_fill(S, 16, p, r, true, seed, 1u, offset, s));
+    DPCLIP_CUDA(launch_philox_fill(S, 16, p, r, true, seed, 1u, offset, s, ctrl, ctrl_words));
     DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, true, seed, 2u, offset, s));
     void *Y1h = at<void>(ws, pl.off[kY1hi]), *Y1l = at<void>(ws, pl.off[kY1lo]);
     void *Z1h = at<void>(ws, pl.off[kZ1hi]), *Z1l = at<void>(ws, pl.off[kZ1lo]);
@@ -649,7 +652,7 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
   float* V = at<float>(ws, pl.off[kFV]);
   float* QW = at<float>(ws, pl.off[kFQW]);
   float* Y3 = at<float>(ws, pl.off[kFY3]);
-  DPCLIP_CUDA(launch_philox_fill(S, r, p, r, false, seed, 1u, offset, s));
+  DPCLIP_CUDA(launch_philox_fill(S, r, p, r, false, seed, 1u, offset, s, ctrl, ctrl_words));
   DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, false, seed, 2u, offset, s));
   int nb = 0;
   SimtParams sp = simt_base();

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
   uint8_t* sG = sA + kStages * kABytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(sG + kStages * kGBytes);
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles_total = p.mtiles * p.ntiles;
 
@@ -114,6 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     tma_prefetch_map(&p.map_g);
   }
   if (warp == 1) tmem_alloc(&ctl->tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();   // inputs (A, G, sqnorms) may come from the previous kernel
   if (kGrad && blockIdx.x == 0) {
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
       const float q = p.sqnorms[i];
@@ -121,9 +126,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
       if (p.clipped) p.clipped[i] = (uint8_t)(sqrtf(fmaxf(q, 0.f)) > p.C);
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = ctl->tmem;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
 
@@ -300,14 +302,12 @@ cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cuda
     if ((e = cudaFuncSetAttribute(gemm_dp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess)
       return e;
-    gemm_dp_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
-  } else {
-    if ((e = cudaFuncSetAttribute(gemm_dp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kSmemBytes)) != cudaSuccess)
-      return e;
-    gemm_dp_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
+    return launch_pdl(gemm_dp_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, false, p);
   }
-  return cudaGetLastError();
+  if ((e = cudaFuncSetAttribute(gemm_dp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBytes)) != cudaSuccess)
+    return e;
+  return launch_pdl(gemm_dp_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, false, p);
 }
 
 }  // namespace dpclip

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
   uint8_t* sQ = sP + kStages * kTileBytes;         // 256 tokens of tile b'
   Ctl* ctl = reinterpret_cast<Ctl*>(sQ + kStages * 2 * kTileBytes);
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nunits = p.B * p.npairs;
   const int kblocks = p.dblocks + p.pblocks;
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();   // inputs may come from the previous kernel
   const uint32_t tmem = ctl->tmem;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
 
@@ -215,8 +217,7 @@ cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(ghost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  ghost_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(ghost_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, false, p);
 }
 
 }  // namespace dpclip

@@ -211,6 +211,8 @@ __global__ void __launch_bounds__(kThreads) hpp_qr_kernel(const __grid_constant_
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   cg::grid_group grid = cg::this_grid();
+  pdl_trigger();
+  pdl_wait();
   const int cps = p.cps;
   const int i = p.sample0 + (int)blockIdx.x / cps;
   const int chunk = (int)blockIdx.x % cps;
@@ -340,9 +342,7 @@ cudaError_t launch_hpp_qr(const HppQrParams& p_in, cudaStream_t s) {
   for (int s0 = 0; s0 < p.B; s0 += per_launch) {
     p.sample0 = s0;
     const int nb = std::min(per_launch, p.B - s0);
-    void* args[] = {(void*)&p};
-    e = cudaLaunchCooperativeKernel((const void*)hpp_qr_kernel, dim3(nb * p.cps), dim3(kThreads),
-                                    args, smem, s);
+    e = launch_pdl(hpp_qr_kernel, dim3(nb * p.cps), dim3(kThreads), smem, s, true, p);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -8,9 +8,32 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dpclip.h"
 
 namespace dpclip {
+
+// Launches `kernel` with programmatic stream serialisation, so that its
+// prologue overlaps the tail of the previous kernel in the stream (the kernel
+// itself waits for that kernel before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, bool cooperative, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------------------
 // Tile geometry of the tensor-core kernels
@@ -151,9 +174,11 @@ size_t hpp_qr_part_floats(int B, int p);
 cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblocks_out);
 int simt_nblocks(int M, int N);
 
+// Also clears `zero_words` 32-bit words at `zero` (the control block of a
+// multi-kernel call) when zero != nullptr.
 cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
                                bool bf16, uint64_t seed, uint32_t stream_id, uint64_t offset,
-                               cudaStream_t s);
+                               cudaStream_t s, uint32_t* zero = nullptr, int zero_words = 0);
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
                                cudaStream_t s);
 // sq[i] = scale * sum_{u < nunits, w < nw} part[(u * su + i * si) * nw + w]

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ 
   __shared__ float xs[kKStep][kTile + 1];
   __shared__ float ys[kKStep][kTile + 1];
   __shared__ float red[8];
+  pdl_trigger();
+  pdl_wait();
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int m0 = blockIdx.y * kTile, n0 = blockIdx.x * kTile;
   const int nblocks = gridDim.x * gridDim.y;
@@ -118,8 +120,7 @@ cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblo
   const dim3 grid((p.N + kTile - 1) / kTile, (p.M + kTile - 1) / kTile,
                   mode == kSimtGrad ? 1 : p.batch);
   if (nblocks_out) *nblocks_out = (int)(grid.x * grid.y);
-  simt_gemm_kernel<<<grid, 256, 0, s>>>(p, mode);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm_kernel, grid, dim3(256), 0, s, false, p, mode);
 }
 
 }  // namespace dpclip

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
   uint8_t* sWlo = sWhi + kStages * kWBytes;
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sWlo + kStages * kWBytes);
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
   const int i = tile / p.mtiles, mt = tile % p.mtiles;
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();   // inputs of this call may come from the previous kernel
   const uint32_t tmem = ctl->tmem;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
 
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   uint8_t* sYlo = sYhi + kStages * kYBytes;
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sYlo + kStages * kYBytes);
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
   const int i = tile / p.ftiles, ft = tile % p.ftiles;
@@ -266,6 +269,7 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();   // inputs of this call may come from the previous kernel
   const uint32_t tmem = ctl->tmem;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
 
@@ -420,15 +424,13 @@ cudaError_t launch_tok_gemm(const TokGemmParams& p, cudaStream_t s) {
   if (p.NP == 16) {
     const size_t sm = skinny_smem_bytes<16>();
     if ((e = set_smem(tok_gemm_kernel<16>, sm)) != cudaSuccess) return e;
-    tok_gemm_kernel<16><<<grid, 128, sm, s>>>(p);
+    return launch_pdl(tok_gemm_kernel<16>, grid, dim3(128), sm, s, false, p);
   } else if (p.NP == 32) {
     const size_t sm = skinny_smem_bytes<32>();
     if ((e = set_smem(tok_gemm_kernel<32>, sm)) != cudaSuccess) return e;
-    tok_gemm_kernel<32><<<grid, 128, sm, s>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
+    return launch_pdl(tok_gemm_kernel<32>, grid, dim3(128), sm, s, false, p);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 template <int NP, int MODE>
@@ -437,8 +439,7 @@ static cudaError_t launch_feat_t(const FeatGemmParams& p, cudaStream_t s) {
   const size_t sm = skinny_smem_bytes<NP>();
   cudaError_t e = set_smem(feat_gemm_kernel<NP, MODE>, sm);
   if (e != cudaSuccess) return e;
-  feat_gemm_kernel<NP, MODE><<<grid, 128, sm, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(feat_gemm_kernel<NP, MODE>, grid, dim3(128), sm, s, false, p);
 }
 
 cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s) {
