@@ -274,11 +274,19 @@ Plan plan_exact_f32(int B, int T, int d, int p, int method) {
   return pl;
 }
 
-Plan plan_grad() {
+// Gradient: tile tickets in the control block, plus the partial-tile slots of
+// the balanced tail (bf16 only).
+Plan plan_grad(int d, int p, int dtype) {
   Plan pl;
   Carve c;
-  pl.ctrl_bytes = kAlign;
-  pl.ctrl = c.take(pl.ctrl_bytes);
+  if (dtype == DPCLIP_BF16) {
+    pl.ctrl_bytes = align_up(4 * (1 + (size_t)dp_ntiles(d, p)), kAlign);
+    pl.ctrl = c.take(pl.ctrl_bytes);
+    pl.off[0] = c.take(gemm_dp_slot_bytes(kMaxPersistentGrid));
+  } else {
+    pl.ctrl_bytes = kAlign;
+    pl.ctrl = c.take(pl.ctrl_bytes);
+  }
   pl.total = c.total();
   return pl;
 }
@@ -304,7 +312,7 @@ int plan_for(int op, int B, int T, int d, int p, int dtype, int param, Plan& pl)
                                 : plan_hutchpp_f32(B, T, d, p, param);
       return DPCLIP_OK;
     case DPCLIP_OP_CLIPPED_NOISY_GRAD:
-      pl = plan_grad();
+      pl = plan_grad(d, p, dtype);
       return DPCLIP_OK;
     default:
       return DPCLIP_ERR_INVALID_ARG;
@@ -489,7 +497,7 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gp.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gp.err = at<uint32_t>(ws, pl.ctrl);
       const int ntiles = gp.mtiles * gp.ntiles;
-      DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min(ntiles * B, num_sms()), s));
+      DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min({ntiles * B, num_sms(), kMaxPersistentGrid}), s));
     } else {
       GhostParams gh;
       std::memset(&gh, 0, sizeof(gh));
@@ -507,7 +515,7 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gh.sq = sqnorms;
       gh.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gh.err = at<uint32_t>(ws, pl.ctrl);
-      DPCLIP_CUDA(launch_ghost(gh, std::min(B * gh.npairs, num_sms()), s));
+      DPCLIP_CUDA(launch_ghost(gh, std::min({B * gh.npairs, num_sms(), kMaxPersistentGrid}), s));
     }
     return DPCLIP_OK;
   }
@@ -725,7 +733,7 @@ int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d,
   if (!(C > 0.f) || !std::isfinite(C)) return DPCLIP_ERR_INVALID_ARG;
   if (!(sigma >= 0.f) || !std::isfinite(sigma)) return DPCLIP_ERR_INVALID_ARG;
   if (!aligned(grad, dtype == DPCLIP_BF16 ? 16 : 4)) return DPCLIP_ERR_UNSUPPORTED;
-  Plan pl = plan_grad();
+  Plan pl = plan_grad(d, p, dtype);
   DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
   cudaStream_t s = (cudaStream_t)stream;
   DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
@@ -750,8 +758,14 @@ int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d,
     gp.scales = scales;
     gp.clipped = clipped;
     gp.err = at<uint32_t>(ws, pl.ctrl);
+    gp.tickets = at<uint32_t>(ws, pl.ctrl + 4);
+    gp.slots = at<float>(ws, pl.off[0]);
     const int ntiles = gp.mtiles * gp.ntiles;
-    DPCLIP_CUDA(launch_gemm_dp(gp, true, std::min(ntiles, num_sms()), s));
+    // one CTA per SM, fewer when there is little work
+    const int grid = std::max(1, std::min({num_sms(), kMaxPersistentGrid, ntiles * B * 4}));
+    plan_grad_schedule(ntiles, B, gp.tblocks, grid, gp.waves, gp.ksplit, gp.kb_per_chunk,
+                       gp.vtotal);
+    DPCLIP_CUDA(launch_gemm_dp(gp, true, grid, s));
     return DPCLIP_OK;
   }
   SimtParams sp = simt_base();

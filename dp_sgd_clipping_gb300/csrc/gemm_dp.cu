@@ -10,22 +10,34 @@
 //               "Problem definition", reduced on chip): partial sums of
 //               (A_i^T G_i)^2, never storing the d x p tile.
 //
-// Work unit = (output tile of 128 d-rows x 256 p-columns, sample i).  In
-// grad mode a CTA owns whole tiles (all B samples of a tile, which it folds
-// into one running sum); in norm mode units are independent and are dealt
-// out one by one (unit u = i * ntiles + tile, CTA c takes u = c, c + grid,
-// ...), which evens out the last wave.  The K loop of a unit runs over that
-// sample's T tokens in blocks of 64; both
-// operands are MN-major (tokens are the slow axis of A and G), loaded by TMA
-// with 128-byte swizzle.  The accumulator of a unit lives in TMEM (256
-// columns); two accumulators alternate, so the epilogue of unit u overlaps
-// the mainloop of unit u+1.  In grad mode the epilogue folds s_i * acc_i into
-// a register-resident running sum (exact fp32 per-sample scaling) and, after
-// the last sample of a tile, adds Philox noise and stores the tile.
+// Output tiles are 128 d-rows x 256 p-columns; both operands are MN-major
+// (tokens are the slow axis of A and G), loaded by TMA with 128-byte swizzle.
+// A work item is (tile, sample i, a range of that sample's 64-token
+// K-blocks); its accumulator lives in TMEM (256 columns) and two accumulators
+// alternate, so the epilogue of one item overlaps the mainloop of the next.
 //
-// Roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2..9 = epilogue (warp w reads TMEM lanes 32*(w%4).., columns
-// 128*((w-2)/4)..).
+// Item sequences of a CTA (blockIdx c, grid G):
+//   norm mode: items are whole (tile, sample) units dealt one by one,
+//     sample-major (u = i * ntiles + tile; CTA c takes u = c, c + G, ...), so
+//     the CTAs running together share one sample's A and G slabs in L2.
+//   grad mode: first `waves` full waves of whole tiles (CTA c owns tiles
+//     c, c + G, ...: all B samples of a tile, folded into a register running
+//     sum s_0 acc_0 + s_1 acc_1 + ... in fp32), then the remaining tiles are
+//     cut into (tile, sample, K-chunk) sub-units dealt in contiguous ranges,
+//     one range per CTA, so that every CTA gets the same amount of work.  A
+//     range covers whole tiles (finished directly) plus at most one partial
+//     tile at each end; a CTA writes each partial tile to its own workspace
+//     slot, takes an integer ticket on the tile, and the last CTA to arrive
+//     adds the slots of the tile in CTA order (a fixed order), adds the noise
+//     and stores.  No CTA ever waits on another.
+//
+// Roles (384 threads, three warpgroups): warp 0 = TMA producer, warp 1 = MMA
+// issuer and TMEM owner, warps 2-3 idle; warps 4..11 = epilogue (warp w reads
+// TMEM lanes 32*(w%4).., columns 128*((w-4)/4)..).  The grad epilogue keeps a
+// 128-float running sum per thread, so registers move from the first
+// warpgroup to the epilogue warpgroups (setmaxnreg: 40 and 232 per thread,
+// which adds up to the 168 per thread the block is launched with; the host
+// checks the compiled count before every launch).
 #include "common.cuh"
 
 namespace dpclip {
@@ -35,7 +47,14 @@ constexpr int kStages = 4;
 constexpr uint32_t kBox = 64 * 128;              // 64 tokens x 128 B (64 bf16)
 constexpr uint32_t kABytes = 2 * kBox;           // 128 d-columns
 constexpr uint32_t kGBytes = 4 * kBox;           // 256 p-columns
-constexpr int kThreads = 64 + 32 * kEpiWarps;    // 320
+constexpr int kThreads = 128 + 32 * kEpiWarps;   // 384: producer warpgroup + 2 epilogue
+constexpr int kEpiThreads = 32 * kEpiWarps;      // 256
+constexpr int kEpiWarp0 = 4;                     // first epilogue warp
+constexpr int kRegsProducer = 40;                // setmaxnreg shares (per thread)
+constexpr int kRegsEpilogue = 232;
+constexpr int kRegsAtLaunch = 168;               // needed: 128*40 + 256*232 <= 384*168
+static_assert(128 * kRegsProducer + kEpiThreads * kRegsEpilogue <= kThreads * kRegsAtLaunch,
+              "register split exceeds the block's allocation");
 
 struct Ctl {
   uint64_t full[kStages];
@@ -46,8 +65,9 @@ struct Ctl {
   int abort_flag;
   int issued;
   int consumed;
-  int mma_units;     // units whose MMAs were committed to tfull
+  int mma_units;     // items whose MMAs were committed to tfull
   int is_last;
+  int combine;
   float red[kThreads / 32];
 };
 
@@ -67,20 +87,125 @@ __device__ __noinline__ void noise4(uint64_t seed, uint64_t offset, uint32_t blk
   *z = make_float4(v[0], v[1], v[2], v[3]);
 }
 
-// The k-th work unit of this CTA: (tile, sample).  Returns false past the end.
+// Barrier among the 256 epilogue threads only (named barrier 1).
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
+// Same barrier, returning true iff `ok` holds in every epilogue thread (keeps
+// the epilogue warps in step when one of them gives up on a wait).
+__device__ __forceinline__ bool epi_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "n"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+
+struct Item {
+  int tile, i, kb0, kb1;
+  bool seg_first;   // first item of this CTA's part of the tile: reset the sum
+  bool seg_last;    // last item of this CTA's part of the tile: finish it
+  bool whole;       // this CTA holds every item of the tile
+};
+
+// Stream-K range of the tail: sub-units [vb(c), vb(c+1)).
+__device__ __forceinline__ long long tail_begin(const GemmDpParams& p, int c) {
+  return (long long)c * p.vtotal / gridDim.x;
+}
+// CTA whose tail range holds sub-unit v.
+__device__ __forceinline__ int tail_owner(const GemmDpParams& p, long long v) {
+  const long long G = gridDim.x;
+  return (int)(((v + 1) * G + p.vtotal - 1) / p.vtotal - 1);
+}
+__device__ __forceinline__ bool tail_nonempty(const GemmDpParams& p, int c) {
+  return tail_begin(p, c) < tail_begin(p, c + 1);
+}
+// Workspace slot of CTA c's partial of tail tile tt (its first or last tile).
+__device__ __forceinline__ int tail_slot(const GemmDpParams& p, int c, int tt) {
+  const long long per_tile = (long long)p.B * p.ksplit;
+  return 2 * c + ((int)(tail_begin(p, c) / per_tile) == tt ? 0 : 1);
+}
+
+// The k-th item of this CTA; false past the end.
 template <bool kGrad>
-__device__ __forceinline__ bool unit_at(int k, int ntiles_total, int B, int& tile, int& i) {
-  if (kGrad) {
-    tile = (int)blockIdx.x + (k / B) * (int)gridDim.x;
-    i = k % B;
-    return tile < ntiles_total;
+__device__ __forceinline__ bool item_at(const GemmDpParams& p, int k, Item& it) {
+  const int G = gridDim.x, c = blockIdx.x, B = p.B;
+  const int ntiles = p.mtiles * p.ntiles;
+  if (!kGrad) {
+    const long long u = (long long)c + (long long)k * G;
+    if (u >= (long long)ntiles * B) return false;
+    it.i = (int)(u / ntiles);
+    it.tile = (int)(u % ntiles);
+    it.kb0 = 0;
+    it.kb1 = p.tblocks;
+    it.seg_first = it.seg_last = it.whole = true;
+    return true;
   }
-  // sample-major: the CTAs running at the same time work on neighbouring
-  // tiles of one sample and share its A and G slabs in L2
-  const long long u = (long long)blockIdx.x + (long long)k * gridDim.x;
-  i = (int)(u / ntiles_total);
-  tile = (int)(u % ntiles_total);
-  return u < (long long)ntiles_total * B;
+  if (k < p.waves * B) {
+    it.tile = c + (k / B) * G;
+    it.i = k % B;
+    it.kb0 = 0;
+    it.kb1 = p.tblocks;
+    it.seg_first = it.i == 0;
+    it.seg_last = it.i == B - 1;
+    it.whole = true;
+    return true;
+  }
+  const long long vb0 = tail_begin(p, c), vb1 = tail_begin(p, c + 1);
+  const long long v = vb0 + (k - (long long)p.waves * B);
+  if (v >= vb1) return false;
+  const long long per_tile = (long long)B * p.ksplit;
+  const int tt = (int)(v / per_tile);
+  const int rem = (int)(v % per_tile);
+  it.tile = p.waves * G + tt;
+  it.i = rem / p.ksplit;
+  const int ch = rem % p.ksplit;
+  it.kb0 = ch * p.kb_per_chunk;
+  it.kb1 = min(it.kb0 + p.kb_per_chunk, p.tblocks);
+  it.seg_first = v == vb0 || rem == 0;
+  it.seg_last = v == vb1 - 1 || rem == per_tile - 1;
+  it.whole = (long long)tt * per_tile >= vb0 && (long long)(tt + 1) * per_tile <= vb1;
+  return true;
+}
+
+// Adds sigma C z to the running sum of one thread's 128 columns of row r and
+// stores them (columns beyond p are skipped; p is a multiple of 8).
+__device__ __forceinline__ void store_with_noise(const GemmDpParams& p, int r, int cb,
+                                                 const float (&tot)[128]) {
+  if (r >= p.d) return;
+  const float nscale = p.sigma * p.C;
+  float* rowp = p.grad + (size_t)r * p.p;
+#pragma unroll
+  for (int jb = 0; jb < 32; ++jb) {
+    const int c = cb + 4 * jb;
+    if (c < p.p) {
+      float4 o = make_float4(tot[4 * jb], tot[4 * jb + 1], tot[4 * jb + 2], tot[4 * jb + 3]);
+      if (nscale != 0.f) {
+        float4 z;
+        noise4(p.seed, p.offset, (uint32_t)(((size_t)r * p.p + c) >> 2), &z);
+        o.x = fmaf(nscale, z.x, o.x);
+        o.y = fmaf(nscale, z.y, o.y);
+        o.z = fmaf(nscale, z.z, o.z);
+        o.w = fmaf(nscale, z.w, o.w);
+      }
+      *reinterpret_cast<float4*>(rowp + c) = o;
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 template <bool kGrad>
@@ -102,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], 32 * kEpiWarps);
+      mbar_init(&ctl->tempty[a], kEpiThreads);
     }
     ctl->abort_flag = 0;
     ctl->issued = 0;
@@ -128,16 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
   }
   const uint32_t tmem = ctl->tmem;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
-
+  if (warp < kEpiWarp0) {
+    regs_dec<kRegsProducer>();
   if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int it = 0;
-      int tile, i;
-      for (int k = 0; unit_at<kGrad>(k, ntiles_total, p.B, tile, i); ++k) {
-        const int d0 = (tile % p.mtiles) * kDpTileM;
-        const int p0 = (tile / p.mtiles) * kDpTileN;
-        bool run = true;
-        for (int kb = 0; kb < p.tblocks; ++kb, ++it) {
+      Item itm;
+      bool run = true;
+      for (int k = 0; run && item_at<kGrad>(p, k, itm); ++k) {
+        const int d0 = (itm.tile % p.mtiles) * kDpTileM;
+        const int p0 = (itm.tile / p.mtiles) * kDpTileN;
+        for (int kb = itm.kb0; kb < itm.kb1; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) {
             run = false;
@@ -147,28 +274,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
           const int t0 = kb * 64;
           uint8_t* a = sA + s * kABytes;
           uint8_t* g = sG + s * kGBytes;
-          tma_load_3d(a, &p.map_a, &ctl->full[s], d0, t0, i);
-          tma_load_3d(a + kBox, &p.map_a, &ctl->full[s], d0 + 64, t0, i);
+          tma_load_3d(a, &p.map_a, &ctl->full[s], d0, t0, itm.i);
+          tma_load_3d(a + kBox, &p.map_a, &ctl->full[s], d0 + 64, t0, itm.i);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            tma_load_3d(g + q * kBox, &p.map_g, &ctl->full[s], p0 + 64 * q, t0, i);
+            tma_load_3d(g + q * kBox, &p.map_g, &ctl->full[s], p0 + 64 * q, t0, itm.i);
           ctl->issued = it + 1;
         }
-        if (!run) break;
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 256, true, true);
       int it = 0;
-      int tile, i;
-      for (int u = 0; unit_at<kGrad>(u, ntiles_total, p.B, tile, i); ++u) {
+      Item itm;
+      bool run = true;
+      for (int u = 0; run && item_at<kGrad>(p, u, itm); ++u) {
         const int acc = u & 1;
         if (!mbar_wait(&ctl->tempty[acc], ((u >> 1) & 1) ^ 1, wc)) break;
         tc_fence_after();
         const uint32_t dt = tmem + (uint32_t)acc * 256u;
-        bool run = true;
-        for (int kb = 0; kb < p.tblocks; ++kb, ++it) {
+        for (int kb = itm.kb0; kb < itm.kb1; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) {
             run = false;
@@ -181,83 +308,109 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             umma_bf16(dt, sdesc_sw128(a0 + kk * 2048, kBox, 1024),
-                      sdesc_sw128(g0 + kk * 2048, kBox, 1024), idesc, (kb | kk) != 0);
+                      sdesc_sw128(g0 + kk * 2048, kBox, 1024), idesc,
+                      (kb != itm.kb0 || kk != 0) ? 1u : 0u);
           }
           umma_commit(&ctl->empty[s]);
         }
         umma_commit(&ctl->tfull[acc]);
         ctl->mma_units = u + 1;
-        if (!run) break;
       }
     }
+  }
   } else {
-    // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;
+    regs_inc<kRegsEpilogue>();
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kEpiWarp0;
     const int quad = warp & 3;
     const int half = ew >> 2;
+    const int etid = ew * 32 + lane;   // 0..255, same role in every CTA
     float tot[128];
 #pragma unroll
     for (int j = 0; j < 128; ++j) tot[j] = 0.f;
-    int tile, i;
-    for (int u = 0; unit_at<kGrad>(u, ntiles_total, p.B, tile, i); ++u) {
-      const int d0 = (tile % p.mtiles) * kDpTileM;
-      const int p0 = (tile / p.mtiles) * kDpTileN;
-      {
-        const int acc = u & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[acc], (u >> 1) & 1, wc))) break;
-        tc_fence_after();
-        const uint32_t taddr =
-            tmem + (uint32_t)acc * 256u + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
-        if (kGrad) {
-          const float si = clip_scale(p.sqnorms[i], p.C);
+    Item itm;
+    for (int u = 0; item_at<kGrad>(p, u, itm); ++u) {
+      const int acc = u & 1;
+      if (!epi_all(mbar_wait(&ctl->tfull[acc], (u >> 1) & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem + (uint32_t)acc * 256u + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
+      if (kGrad) {
+        const float si = clip_scale(p.sqnorms[itm.i], p.C);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            float v[32];
-            tmem_ld32(taddr + c4 * 32, v);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float v[32];
+          tmem_ld32(taddr + c4 * 32, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              tot[c4 * 32 + j] = (i == 0) ? si * v[j] : fmaf(si, v[j], tot[c4 * 32 + j]);
-          }
-          tc_fence_before();
-          mbar_arrive(&ctl->tempty[acc]);
-        } else {
-          float ss = 0.f;
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            float v[32];
-            tmem_ld32(taddr + c4 * 32, v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
-          }
-          tc_fence_before();
-          mbar_arrive(&ctl->tempty[acc]);
-          ss = warp_sum(ss);
-          if (lane == 0) p.part[((size_t)tile * p.B + i) * kEpiWarps + ew] = ss;
+          for (int j = 0; j < 32; ++j)
+            tot[c4 * 32 + j] = itm.seg_first ? si * v[j] : fmaf(si, v[j], tot[c4 * 32 + j]);
         }
-        if (kGrad && i == p.B - 1) {
-          const int r = d0 + quad * 32 + lane;
-          const int cb = p0 + half * 128;
-          if (r < p.d) {
-            const float nscale = p.sigma * p.C;
-            float* rowp = p.grad + (size_t)r * p.p;
+        tc_fence_before();
+        mbar_arrive(&ctl->tempty[acc]);
+        bool do_store = false;
+        if (itm.seg_last) {
+          do_store = itm.whole;
+          if (!itm.whole) {
+            // partial tile: publish this CTA's part; the last CTA to arrive
+            // adds every participant's part, in CTA order, and stores
+            const int tt = itm.tile - p.waves * (int)gridDim.x;
+            float4* slot = reinterpret_cast<float4*>(p.slots) +
+                           (size_t)tail_slot(p, blockIdx.x, tt) * (32 * kEpiThreads);
 #pragma unroll
-            for (int jb = 0; jb < 32; ++jb) {
-              const int c = cb + 4 * jb;
-              if (c < p.p) {
-                float4 o = make_float4(tot[4 * jb], tot[4 * jb + 1], tot[4 * jb + 2], tot[4 * jb + 3]);
-                if (nscale != 0.f) {
-                  float4 z;
-                  noise4(p.seed, p.offset, (uint32_t)(((size_t)r * p.p + c) >> 2), &z);
-                  o.x = fmaf(nscale, z.x, o.x);
-                  o.y = fmaf(nscale, z.y, o.y);
-                  o.z = fmaf(nscale, z.z, o.z);
-                  o.w = fmaf(nscale, z.w, o.w);
+            for (int jb = 0; jb < 32; ++jb)
+              __stcg(slot + jb * kEpiThreads + etid,
+                     make_float4(tot[4 * jb], tot[4 * jb + 1], tot[4 * jb + 2], tot[4 * jb + 3]));
+            __threadfence();
+            epi_sync();
+            // participants: the CTAs from the owner of the tile's first
+            // sub-unit to the owner of its last, skipping empty ranges
+            const long long per_tile = (long long)p.B * p.ksplit;
+            const int c_lo = tail_owner(p, (long long)tt * per_tile);
+            const int c_hi = tail_owner(p, (long long)(tt + 1) * per_tile - 1);
+            if (etid == 0) {
+              int parts = 0;
+              for (int cc = c_lo; cc <= c_hi; ++cc) parts += tail_nonempty(p, cc) ? 1 : 0;
+              const uint32_t prev = atomicAdd(&p.tickets[itm.tile], 1u);
+              ctl->combine = prev == (uint32_t)(parts - 1);
+            }
+            epi_sync();
+            if (ctl->combine) {
+              __threadfence();
+#pragma unroll
+              for (int j = 0; j < 128; ++j) tot[j] = 0.f;
+              for (int cc = c_lo; cc <= c_hi; ++cc) {
+                if (!tail_nonempty(p, cc)) continue;
+                const float4* src = reinterpret_cast<const float4*>(p.slots) +
+                                    (size_t)tail_slot(p, cc, tt) * (32 * kEpiThreads);
+#pragma unroll
+                for (int jb = 0; jb < 32; ++jb) {
+                  const float4 v = __ldcg(src + jb * kEpiThreads + etid);
+                  tot[4 * jb] += v.x;
+                  tot[4 * jb + 1] += v.y;
+                  tot[4 * jb + 2] += v.z;
+                  tot[4 * jb + 3] += v.w;
                 }
-                *reinterpret_cast<float4*>(rowp + c) = o;
               }
+              do_store = true;
             }
           }
         }
+        if (do_store)
+          store_with_noise(p, (itm.tile % p.mtiles) * kDpTileM + quad * 32 + lane,
+                           (itm.tile / p.mtiles) * kDpTileN + half * 128, tot);
+      } else {
+        float ss = 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float v[32];
+          tmem_ld32(taddr + c4 * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+        }
+        tc_fence_before();
+        mbar_arrive(&ctl->tempty[acc]);
+        ss = warp_sum(ss);
+        if (lane == 0) p.part[((size_t)itm.tile * p.B + itm.i) * kEpiWarps + ew] = ss;
       }
     }
   }
@@ -296,8 +449,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 
 size_t gemm_dp_smem() { return kSmemBytes; }
 
+size_t gemm_dp_slot_bytes(int max_grid) { return (size_t)2 * max_grid * 32 * kEpiThreads * 16; }
+
+// Grad-mode schedule: full waves of whole tiles, then the K-split of the
+// remaining tiles (1, 2 or 4 chunks per sample) that best evens out the
+// per-CTA work.
+void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ksplit,
+                        int& kb_per_chunk, long long& vtotal) {
+  waves = ntiles / grid;
+  const int tail = ntiles - waves * grid;
+  ksplit = 1;
+  double best = 1e30;
+  for (int want : {1, 2, 4}) {
+    const int kbc = (tblocks + want - 1) / want;
+    const int ks = (tblocks + kbc - 1) / kbc;   // chunks actually used: none is empty
+    const long long v = (long long)tail * B * ks;
+    // the busiest CTA's work in K-blocks
+    const double span = (double)waves * B * tblocks + (double)((v + grid - 1) / grid) * kbc;
+    if (span < best - 1e-9) {
+      best = span;
+      ksplit = ks;
+    }
+  }
+  kb_per_chunk = (tblocks + ksplit - 1) / ksplit;
+  vtotal = (long long)tail * B * ksplit;
+}
+
+// The register split above is only safe when the compiled kernel is launched
+// with at least kRegsAtLaunch registers per thread.
+template <typename K>
+cudaError_t check_regs(K kernel) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  return fa.numRegs >= kRegsAtLaunch ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cudaStream_t s) {
   cudaError_t e;
+  if ((e = check_regs(grad_mode ? gemm_dp_kernel<true> : gemm_dp_kernel<false>)) != cudaSuccess)
+    return e;
   if (grad_mode) {
     if ((e = cudaFuncSetAttribute(gemm_dp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess)

@@ -96,6 +96,11 @@ struct GemmDpParams {
   CUtensorMap map_g;     // G [B][T][p], box {64, 64, 1}
   int B, T, d, p;
   int mtiles, ntiles, tblocks;
+  // grad-mode schedule (plan_grad_schedule)
+  int waves, ksplit, kb_per_chunk;
+  long long vtotal;
+  float* slots;          // 2 * grid partial tiles of 128 x 256 fp32
+  uint32_t* tickets;     // [mtiles * ntiles], zero at launch
   const float* sqnorms;
   float C, sigma;
   uint64_t seed, offset;
@@ -192,6 +197,10 @@ cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t 
 size_t tok_gemm_smem(int NP);
 size_t feat_gemm_smem(int NP);
 size_t gemm_dp_smem();
+size_t gemm_dp_slot_bytes(int max_grid);
+void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ksplit,
+                        int& kb_per_chunk, long long& vtotal);
+constexpr int kMaxPersistentGrid = 160;   // CTAs of the persistent kernels (<= SMs)
 size_t ghost_smem();
 
 }  // namespace dpclip
