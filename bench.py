@@ -250,17 +250,22 @@ def main():
           "clipped_noisy_grad": ws_for(L.OP_CLIPPED_NOISY_GRAD, 0)}
     stream = torch.cuda.current_stream(dev)
 
-    def row_fn(name, step):
+    def row_fn(name, step, bufs=None):
+        """The ABI call of one row of the step on a set of buffers."""
+        b = bufs or {"A": A, "G": G, "q_h": q_h, "q_pp": q_pp, "q_d": q_d, "q_g": q_g,
+                     "grad": grad, "scales": scales, "clipped": clipped}
         if name == "hutch":
-            return lambda: api.norms_hutch(A, G, k, wl.seed, step, out=q_h, ws=ws[name])
+            return lambda: api.norms_hutch(b["A"], b["G"], k, wl.seed, step, out=b["q_h"], ws=ws[name])
         if name == "hutchpp":
-            return lambda: api.norms_hutchpp(A, G, k, wl.seed, step, out=q_pp, ws=ws[name])
+            return lambda: api.norms_hutchpp(b["A"], b["G"], k, wl.seed, step, out=b["q_pp"],
+                                             ws=ws[name])
         if name == "exact_direct":
-            return lambda: api.norms_exact(A, G, L.EXACT_DIRECT, out=q_d, ws=ws[name])
+            return lambda: api.norms_exact(b["A"], b["G"], L.EXACT_DIRECT, out=b["q_d"], ws=ws[name])
         if name == "exact_ghost":
-            return lambda: api.norms_exact(A, G, L.EXACT_GHOST, out=q_g, ws=ws[name])
-        return lambda: api.clipped_noisy_grad(A, G, q_h, wl.C, wl.sigma, wl.seed, step, grad=grad,
-                                              scales=scales, clipped=clipped, ws=ws[name])
+            return lambda: api.norms_exact(b["A"], b["G"], L.EXACT_GHOST, out=b["q_g"], ws=ws[name])
+        return lambda: api.clipped_noisy_grad(b["A"], b["G"], b["q_h"], wl.C, wl.sigma, wl.seed, step,
+                                              grad=b["grad"], scales=b["scales"],
+                                              clipped=b["clipped"], ws=ws[name])
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -303,43 +308,86 @@ def main():
     elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
 
     # ---------------------------------------------------------------- end to end, host buffers
+    # Every step copies its inputs from pinned host memory and its results
+    # (the four norm vectors, the gradient, scales, flags) back to pinned host
+    # memory.  Steps are pipelined the way a training loop would run them:
+    # two device buffer sets; step s+1's inputs travel on a copy stream and
+    # step s-1's results on another while step s computes.
     e2e = None
     if not args.no_e2e:
-        outs_h = {"q": torch.empty(4, B, dtype=torch.float32).pin_memory(),
-                  "grad": torch.empty(d, p, dtype=torch.float32).pin_memory(),
-                  "scales": torch.empty(B, dtype=torch.float32).pin_memory(),
-                  "clipped": torch.empty(B, dtype=torch.uint8).pin_memory()}
-        qs = torch.empty(4, B, **f32)
+        def buffer_set():
+            return {"A": torch.empty_like(A), "G": torch.empty_like(G),
+                    "q_h": torch.empty(B, **f32), "q_pp": torch.empty(B, **f32),
+                    "q_d": torch.empty(B, **f32), "q_g": torch.empty(B, **f32),
+                    "grad": torch.empty(d, p, **f32), "scales": torch.empty(B, **f32),
+                    "clipped": torch.empty(B, dtype=torch.uint8, device=dev)}
 
-        def e2e_step(s):
-            A.copy_(A_h, non_blocking=True)
-            G.copy_(G_h, non_blocking=True)
+        def host_set():
+            return {"q": torch.empty(4, B, dtype=torch.float32).pin_memory(),
+                    "grad": torch.empty(d, p, dtype=torch.float32).pin_memory(),
+                    "scales": torch.empty(B, dtype=torch.float32).pin_memory(),
+                    "clipped": torch.empty(B, dtype=torch.uint8).pin_memory()}
+
+        bufs = [buffer_set(), buffer_set()]
+        hosts = [host_set(), host_set()]
+        qs = [torch.empty(4, B, **f32), torch.empty(4, B, **f32)]
+        s_h2d = torch.cuda.Stream(dev)
+        s_d2h = torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()
+        h2d_done = [ev(), ev()]
+        comp_done = [ev(), ev()]
+        d2h_done = [ev(), ev()]
+        for e in comp_done + d2h_done:
+            e.record(stream)
+
+        def e2e_step(sidx):
+            bi = sidx % 2
+            bset, hset = bufs[bi], hosts[bi]
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(comp_done[bi])        # step sidx-2 no longer reads them
+                bset["A"].copy_(A_h, non_blocking=True)
+                bset["G"].copy_(G_h, non_blocking=True)
+                h2d_done[bi].record(s_h2d)
+            stream.wait_event(h2d_done[bi])
+            stream.wait_event(d2h_done[bi])            # step sidx-2's results are out
             for r in rows:
-                row_fn(r, s)()
-            for j, q in enumerate((q_h, q_pp, q_d, q_g)):
-                qs[j].copy_(q)
-            outs_h["q"].copy_(qs, non_blocking=True)
-            outs_h["grad"].copy_(grad, non_blocking=True)
-            outs_h["scales"].copy_(scales, non_blocking=True)
-            outs_h["clipped"].copy_(clipped, non_blocking=True)
+                row_fn(r, sidx, bset)()
+            for j, key in enumerate(("q_h", "q_pp", "q_d", "q_g")):
+                qs[bi][j].copy_(bset[key])
+            comp_done[bi].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(comp_done[bi])
+                hset["q"].copy_(qs[bi], non_blocking=True)
+                hset["grad"].copy_(bset["grad"], non_blocking=True)
+                hset["scales"].copy_(bset["scales"], non_blocking=True)
+                hset["clipped"].copy_(bset["clipped"], non_blocking=True)
+                d2h_done[bi].record(s_d2h)
 
-        for s in range(args.warmup):
-            e2e_step(s)
+        for sidx in range(args.warmup):
+            e2e_step(sidx)
+        stream.wait_event(d2h_done[0])
+        stream.wait_event(d2h_done[1])
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for s in range(args.steps):
-            e2e_step(args.warmup + s)
+        for e in comp_done + d2h_done:          # the copy streams start after e0
+            e.record(stream)
+        for sidx in range(args.steps):
+            e2e_step(args.warmup + sidx)
+        stream.wait_event(d2h_done[0])
+        stream.wait_event(d2h_done[1])
         e1.record(stream)
         barrier()
         e2e_ms = e0.elapsed_time(e1)
         e2e_ms = max_over_ranks(e2e_ms, pg, dev)
         h2d = A_h.numel() * 2 + G_h.numel() * 2
-        d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+        d2h = sum(t.numel() * t.element_size() for t in hosts[0].values())
         e2e = {"value": job_tokens_per_s(world, B * T, args.steps, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms / args.steps}
+               "ms_per_step": e2e_ms / args.steps,
+               "pipelining": "inputs of step s+1 and results of step s-1 copied on two "
+                             "copy streams while step s computes"}
 
     if rank != 0:
         if pg is not None:
