@@ -70,7 +70,7 @@ enum dpclip_status {
 enum dpclip_dtype { DPCLIP_F32 = 0, DPCLIP_BF16 = 1 };
 
 enum dpclip_exact_method {
-  DPCLIP_EXACT_AUTO = 0,    /* direct when T*(d+p) > d*p, else ghost */
+  DPCLIP_EXACT_AUTO = 0,    /* direct when 2*d*p < T*(d+p) (fewer flops), else ghost */
   DPCLIP_EXACT_GHOST = 1,   /* sum((A_i A_i^T) o (G_i G_i^T)) */
   DPCLIP_EXACT_DIRECT = 2   /* ||A_i^T G_i||_F^2, tile by tile, never stored */
 };
