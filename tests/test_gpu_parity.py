@@ -212,3 +212,64 @@ def test_bounded_wait_reports_timeout_and_context_survives(api):
     q = api.norms_hutch(A, A, 4, 1, 0, ws=ws2)
     assert api.workspace_status(ws2) == 0
     assert torch.isfinite(q).all()
+
+
+# ----------------------------------------------------------------------------- shape boundaries
+
+def _run_all(api, wl, paths=("direct", "ghost", "hutch", "hutchpp", "grad")):
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    want = tuple(x for x in ("hutch", "hutchpp") if x in paths and (x != "hutchpp" or wl.k >= 3))
+    ref = oracle_all(inp, want=want)
+    tol = TOL[wl.dtype]
+    if "direct" in paths:
+        assert_rel(host(api.norms_exact(A, G, method=2)), ref["direct"], tol, "direct")
+    if "ghost" in paths:
+        assert_rel(host(api.norms_exact(A, G, method=1)), ref["direct"], tol, "ghost")
+    if "hutch" in paths:
+        assert_rel(host(api.norms_hutch(A, G, wl.k, wl.seed, 0)), ref["hutch"], tol, "hutch")
+    if "hutchpp" in want:
+        assert_rel(host(api.norms_hutchpp(A, G, wl.k, wl.seed, 0)), ref["hutchpp"], tol, "hutch++")
+    if "grad" in paths:
+        C_med = float(np.median(np.sqrt(ref["direct"])))
+        check_grad(api, inp, A, G, ref["direct"], C_med, wl.sigma, ref["Ms"], offset=5)
+
+
+@pytest.mark.parametrize("k", [1, 2, 15, 16, 17, 31, 32])
+def test_hutch_probe_widths(api, k):
+    # k <= 16 runs the 16-column skinny kernels, k > 16 the 32-column ones
+    wl = W.Workload(140 + k, f"kwidth_{k}", 2, 200, 64, 136, "bf16", 1e-2, 1.0, 1.0, k, ())
+    _run_all(api, wl, paths=("hutch",))
+
+
+@pytest.mark.parametrize("k", [3, 4, 5, 46, 47, 48])
+def test_hutchpp_budgets(api, k):
+    # r = k // 3 head columns, m = k - 2r tail probes; k = 48 fills all 32 columns
+    wl = W.Workload(160 + k, f"hpp_{k}", 2, 260, 96, 192, "bf16", 1e-2, 1.0, 1.0, k, ())
+    _run_all(api, wl, paths=("hutchpp",))
+
+
+def test_f32_odd_shapes(api):
+    wl = W.Workload(170, "f32_odd", 3, 37, 29, 50, "f32", 1.0, 1.0, 1.0, 7, ())
+    _run_all(api, wl)
+
+
+def test_many_samples_per_tile(api):
+    # 33 samples: the gradient's tiles are split over many CTAs by sample
+    wl = W.Workload(171, "many_samples", 33, 24, 64, 64, "bf16", 1e-2, 0.5, 1.0, 8, ())
+    _run_all(api, wl)
+
+
+def test_long_sequence_narrow_layer(api):
+    wl = W.Workload(172, "long_narrow", 1, 5000, 8, 16, "bf16", 1e-2, 0.5, 1.0, 6, ())
+    _run_all(api, wl)
+
+
+def test_grad_tail_split_over_k(api):
+    # several full waves of tiles plus a remainder split by sample and K
+    wl = W.Workload(173, "waves", 2, 1100, 1024, 4096, "bf16", 1e-3, 0.5, 0.0, 8, ())
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    Ms = list(O.per_sample_grads(inp.A, inp.G))
+    q = np.array([np.sum(M * M) for M in Ms])
+    check_grad(api, inp, A, G, q, float(np.sqrt(q).min()), 0.0, Ms)
