@@ -217,8 +217,11 @@ Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
   Carve c;
   pl.ctrl_bytes = kAlign;
   pl.ctrl = c.take(pl.ctrl_bytes);
-  const size_t units = method == DPCLIP_EXACT_DIRECT ? (size_t)dp_ntiles(d, p) * B
-                                                     : (size_t)ghost_npairs(T) * B;
+  // ghost: whole units plus at most 8 sub-units for each unit of the last
+  // round (fewer than kMaxPersistentGrid units)
+  const size_t units = method == DPCLIP_EXACT_DIRECT
+                           ? (size_t)dp_ntiles(d, p) * B
+                           : (size_t)ghost_npairs(T) * B + 8 * (size_t)kMaxPersistentGrid;
   pl.off[0] = c.take(units * kEpiWarps * 4);
   pl.total = c.total();
   return pl;
@@ -515,7 +518,9 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gh.sq = sqnorms;
       gh.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gh.err = at<uint32_t>(ws, pl.ctrl);
-      DPCLIP_CUDA(launch_ghost(gh, std::min({B * gh.npairs, num_sms(), kMaxPersistentGrid}), s));
+      const int grid = std::min({B * gh.npairs, num_sms(), kMaxPersistentGrid});
+      plan_ghost_schedule(gh, grid);
+      DPCLIP_CUDA(launch_ghost(gh, grid, s));
     }
     return DPCLIP_OK;
   }

@@ -16,6 +16,13 @@
 // warp; the last CTA to finish adds the partials of each sample in a fixed
 // order.
 //
+// Units are dealt round-robin (unit u to CTA u mod G).  All units cost the
+// same, so when their count is not a multiple of the grid the last round is
+// only partly busy; the units of that last round are therefore cut along p
+// into `tail_split` sub-units that each recompute X over all of d but only
+// a slice of Y's K range.  Because sum(X o Y) is linear in Y, the sub-units'
+// partial sums simply add up: no combine step is needed.
+//
 // Roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
 // owner, warps 2..9 = epilogue.
 #include "common.cuh"
@@ -61,6 +68,29 @@ __device__ __forceinline__ void pair_of(int pr, int ntt, int& a, int& bb) {
   bb = col;
 }
 
+// Work item g -> (sample, unit index within the sample, p-block range).
+struct GhostItem {
+  int i, pr, pb0, pb1;
+};
+__device__ __forceinline__ bool ghost_item(const GhostParams& p, int g, GhostItem& it) {
+  int u;
+  if (g < p.nfull) {
+    u = g;
+    it.pb0 = 0;
+    it.pb1 = p.pblocks;
+  } else {
+    const int t = g - p.nfull;
+    if (t >= (p.B * p.npairs - p.nfull) * p.tail_split) return false;
+    u = p.nfull + t / p.tail_split;
+    const int c = t % p.tail_split;
+    it.pb0 = c * p.pb_per_split;
+    it.pb1 = min(it.pb0 + p.pb_per_split, p.pblocks);
+  }
+  it.i = u / p.npairs;
+  it.pr = u % p.npairs;
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constant__ GhostParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -70,8 +100,6 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nunits = p.B * p.npairs;
-  const int kblocks = p.dblocks + p.pblocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -102,10 +130,12 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
     if (lane == 0) {
       int it = 0;
       bool run = true;
-      for (int u = blockIdx.x; run && u < nunits; u += gridDim.x) {
-        const int i = u / p.npairs;
+      GhostItem itm;
+      for (int g = blockIdx.x; run && ghost_item(p, g, itm); g += gridDim.x) {
+        const int i = itm.i;
         int a, b;
-        pair_of(u % p.npairs, p.ntt, a, b);
+        pair_of(itm.pr, p.ntt, a, b);
+        const int kblocks = p.dblocks + (itm.pb1 - itm.pb0);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) {
@@ -115,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
           mbar_arrive_expect_tx(&ctl->full[s], 3 * kTileBytes);
           const bool on_a = kb < p.dblocks;
           const CUtensorMap* map = on_a ? &p.map_a : &p.map_g;
-          const int k0 = (on_a ? kb : kb - p.dblocks) * kBlockK;
+          const int k0 = (on_a ? kb : itm.pb0 + kb - p.dblocks) * kBlockK;
           uint8_t* q = sQ + s * 2 * kTileBytes;
           tma_load_3d(sP + s * kTileBytes, map, &ctl->full[s], k0, a * kGhostTile, i);
           tma_load_3d(q, map, &ctl->full[s], k0, 2 * b * kGhostTile, i);
@@ -129,9 +159,11 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
       int it = 0, lu = 0;
       bool run = true;
-      for (int u = blockIdx.x; run && u < nunits; u += gridDim.x, ++lu) {
+      GhostItem itm;
+      for (int g = blockIdx.x; run && ghost_item(p, g, itm); g += gridDim.x, ++lu) {
         if (!mbar_wait(&ctl->tempty[0], (lu & 1) ^ 1, wc)) break;
         tc_fence_after();
+        const int kblocks = p.dblocks + (itm.pb1 - itm.pb0);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) {
@@ -160,11 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
     const int quad = warp & 3;
     const int half = ew >> 2;
     int lu = 0;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++lu) {
+    GhostItem itm;
+    for (int g = blockIdx.x; ghost_item(p, g, itm); g += gridDim.x, ++lu) {
       if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[0], lu & 1, wc))) break;
       tc_fence_after();
       int a, bb;
-      pair_of(u % p.npairs, p.ntt, a, bb);
+      pair_of(itm.pr, p.ntt, a, bb);
       const int b = 2 * bb + half;                   // 128-token block of these columns
       const float w = a < b ? 2.f : (a == b ? 1.f : 0.f);
       const uint32_t base = tmem + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
@@ -180,12 +213,49 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       tc_fence_before();
       mbar_arrive(&ctl->tempty[0]);
       s = warp_sum(s);
-      if (lane == 0) p.part[(size_t)u * kEpiWarps + ew] = w * s;
+      if (lane == 0) p.part[(size_t)g * kEpiWarps + ew] = w * s;
     }
   }
 
-  reduce_partials_last_cta(p.part, p.B, p.npairs, 1, p.npairs, kEpiWarps, 1.f, p.sq, p.ticket,
-                           ctl->red, &ctl->is_last);
+  // per sample: its whole units [i*np, (i+1)*np) below nfull, then the
+  // sub-units of its units above nfull (item order = sample order)
+  {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) ctl->is_last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1u) ? 1 : 0;
+    __syncthreads();
+    if (ctl->is_last) {
+      __threadfence();
+      const int np = p.npairs, nf = p.nfull, ts = p.tail_split;
+      for (int i = 0; i < p.B; ++i) {
+        const int f0 = min(i * np, nf), f1 = min((i + 1) * np, nf);
+        const int s0 = nf + (max(i * np, nf) - nf) * ts, s1 = nf + (max((i + 1) * np, nf) - nf) * ts;
+        const long long n1 = (long long)(f1 - f0) * kEpiWarps, n2 = (long long)(s1 - s0) * kEpiWarps;
+        float acc = 0.f;
+        for (long long e0 = threadIdx.x; e0 < n1 + n2; e0 += 8ll * blockDim.x) {
+          float v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const long long e = e0 + (long long)q * blockDim.x;
+            v[q] = e < n1 ? __ldcg(p.part + (size_t)f0 * kEpiWarps + e)
+                          : (e < n1 + n2 ? __ldcg(p.part + (size_t)s0 * kEpiWarps + (e - n1)) : 0.f);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc += v[q];
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) ctl->red[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          float sum = 0.f;
+          for (int w = 0; w < kThreads / 32; ++w) sum += ctl->red[w];
+          p.sq[i] = sum;
+        }
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) *p.ticket = 0u;
+    }
+  }
 
   tc_fence_before();
   __syncthreads();
@@ -212,6 +282,29 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
 }  // namespace
 
 size_t ghost_smem() { return kSmemBytes; }
+
+void plan_ghost_schedule(GhostParams& p, int grid) {
+  const int units = p.B * p.npairs;
+  const int rounds = units / grid;
+  p.nfull = rounds * grid;
+  const int tail = units - p.nfull;
+  p.tail_split = 1;
+  p.pb_per_split = p.pblocks;
+  if (tail == 0) return;
+  // cost of the last round in K-blocks; a unit is dblocks + pblocks
+  double best = (double)p.dblocks + p.pblocks;
+  for (int want = 2; want <= 8; ++want) {
+    const int pbc = (p.pblocks + want - 1) / want;
+    const int s = (p.pblocks + pbc - 1) / pbc;   // no empty slice
+    const int extra_rounds = (tail * s + grid - 1) / grid;
+    const double cost = (double)extra_rounds * (p.dblocks + pbc);
+    if (cost < best - 1e-9) {
+      best = cost;
+      p.tail_split = s;
+      p.pb_per_split = pbc;
+    }
+  }
+}
 
 cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(ghost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -120,7 +120,9 @@ struct GhostParams {
   CUtensorMap map_g;     // box {64, 128, 1}
   int B, T, d, p;
   int ntt, npairs, dblocks, pblocks;
-  float* part;
+  int nfull;             // units dealt whole (a multiple of the grid)
+  int tail_split, pb_per_split;   // the remaining units cut along p
+  float* part;           // [nfull + (B*npairs - nfull) * tail_split][8]
   float* sq;             // per-sample result [B]
   uint32_t* ticket;      // zeroed grid ticket
   uint32_t* err;
@@ -202,5 +204,7 @@ void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, in
                         int& kb_per_chunk, long long& vtotal);
 constexpr int kMaxPersistentGrid = 160;   // CTAs of the persistent kernels (<= SMs)
 size_t ghost_smem();
+// Tail split of the ghost units for a grid: sets nfull, tail_split, pb_per_split.
+void plan_ghost_schedule(GhostParams& p, int grid);
 
 }  // namespace dpclip
