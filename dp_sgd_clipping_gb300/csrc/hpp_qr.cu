@@ -1,7 +1,7 @@
 // Hutch++ middle step ("Core mechanism", item 2 of the randomized-clipping
 // summary: a QR-based low-rank head plus a Hutchinson tail):
 //   V = O_i S (p x r, fp32, from the first two sweeps)
-//   Q = orthonormal basis of range(V)        -- pivoted CholeskyQR2
+//   Q = orthonormal basis of range(V)        -- CholeskyQR2 with column drop
 //   W = G' - Q (Q^T G')                      -- tail probes projected off Q
 //   out = [Q | 0 | W | 0] padded to 32 columns ([B][32][p], hi/lo bf16 for
 //         the tensor-core sweep, or fp32)
@@ -11,20 +11,22 @@
 //
 // CholeskyQR2: Gram H = V^T V, Cholesky H = R^T R, Q1 = V R^-1, then once more
 // on Q1 (whose Gram is close to the identity).  Everything runs in fp32: this
-// GPU's fp64 pipe is a small fraction of its fp32 rate.  The first Cholesky is
-// pivoted and stops at pivots below 1e-5 of the largest diagonal entry (a
-// singular-value ratio of ~3e-3): such directions carry almost no energy of
-// O_i (T < r makes rank(O_i) < r, for instance), so Q keeps fewer columns and
-// the tail estimates the rest.  With them dropped the kept Gram has condition
-// number below ~1e5, within fp32 Cholesky's reach, and the second pass
-// restores orthogonality to fp32 level.
+// GPU's fp64 pipe is a small fraction of its fp32 rate.  A Cholesky pivot
+// below 1e-5 of the largest diagonal entry (a singular-value ratio of ~3e-3)
+// marks its column as dependent on the earlier ones: that column of Q is set
+// to zero, so Q spans the rest and the tail estimates what is left (T < r
+// makes rank(O_i) < r, for instance).  With those columns dropped the kept
+// Gram has condition number below ~1e5, within fp32 Cholesky's reach, and the
+// second pass restores orthogonality to fp32 level.
 //
 // Parallel layout: a cooperative grid of B x ceil(p / 512) CTAs; each CTA
 // keeps its 512 rows of V (then Q) and G' in shared memory for the whole
-// kernel.  Each of the three p-long reductions (V^T V, Q1^T Q1, Q^T G') writes
-// one partial per CTA; after a grid-wide barrier every CTA of the sample adds
-// the partials of its sample in the same fixed order, so all of them hold the
-// same bits and factorise identically (one warp, lane j owns column j).
+// kernel.  Two p-long reductions: V^T V, then Q1^T Q1 together with
+// Q1^T G' (Q^T G' = R2^-T Q1^T G' needs no third pass).  Each writes one
+// partial per CTA; after a grid-wide barrier every CTA of the sample adds the
+// partials of its sample in the same fixed order, so all of them hold the
+// same bits and factorise identically (one thread, the r x r factor fully in
+// registers; rows apply R^-1 by forward substitution).
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -40,18 +42,20 @@ constexpr int kThreads = 256;
 constexpr int kRows = 512;           // rows of p per CTA
 constexpr int kMaxR = 16;            // r = floor(k/3) <= 16 for k <= 48
 constexpr int kMaxM = 18;            // m = k - 2r <= 18 for k <= 48
-constexpr int kMaxE = kMaxR * kMaxM; // entries of the largest cross product
+constexpr int kSym = kMaxR * (kMaxR + 1) / 2;     // 136 upper-triangle entries
+constexpr int kPartStride = 512;     // floats per CTA partial
+static_assert(kSym + kMaxR * kMaxM <= kPartStride, "partials of pass 2 must fit");
 constexpr float kDropTol = 1e-5f;
 
 struct Smem {
   float x[kMaxR][kRows + 1];       // rows of V, then Q1, then Q
   float g[kMaxM][kRows + 1];       // rows of G'
-  float H[kMaxE];                  // summed cross products, row-major
-  float Aw[kMaxR][kMaxR + 1];      // Cholesky workspace
-  float R[kMaxR][kMaxR + 1];
-  float Rinv[kMaxR][kMaxR + 1];
-  int perm[kMaxR];
-  int rank;
+  float S[kPartStride];            // summed partials of the current pass
+  float H[kMaxR][kMaxR + 1];       // Gram matrix of the current pass
+  float K[kMaxR][kMaxM];           // Q1^T G'
+  float Cm[kMaxR][kMaxM];          // Q^T G' = R2^-T K (zero rows for dropped columns)
+  float R[kMaxR][kMaxR + 1];       // Cholesky factor (zero rows for dropped columns)
+  float rdiag[kMaxR];              // 1 / R[k][k], or 0 for a dropped column
 };
 
 __device__ __forceinline__ void sym_entry(int e, int n, int& a, int& b) {
@@ -91,119 +95,82 @@ __device__ void partial_cross(const float (*X)[kRows + 1], int na, const float (
   }
 }
 
-// Sums the per-CTA partials of this sample (chunk order) into sm.H, expanding
-// the upper triangle when sym.
-__device__ void sum_partials(Smem& sm, const float* parts, int cps, int na, int nb, bool sym) {
-  const int ne = sym ? na * (na + 1) / 2 : na * nb;
+// sm.S[e] = sum of the per-CTA partials of this sample (chunk order), e < ne.
+__device__ void sum_partials(Smem& sm, const float* parts, int cps, int ne) {
   for (int e = threadIdx.x; e < ne; e += kThreads) {
     float s = 0.f;
     for (int q0 = 0; q0 < cps; q0 += 8) {   // 8 loads in flight, added in chunk order
       float v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = q0 + u < cps ? __ldcg(parts + (size_t)(q0 + u) * kMaxE + e) : 0.f;
+      for (int u = 0; u < 8; ++u)
+        v[u] = q0 + u < cps ? __ldcg(parts + (size_t)(q0 + u) * kPartStride + e) : 0.f;
 #pragma unroll
       for (int u = 0; u < 8; ++u) s += v[u];
     }
-    if (sym) {
-      int a, b;
-      sym_entry(e, na, a, b);
-      sm.H[a * nb + b] = s;
-      sm.H[b * nb + a] = s;
-    } else {
-      sm.H[e] = s;
-    }
+    sm.S[e] = s;
   }
 }
 
-// One warp: Cholesky of the n x n Gram in sm.H (row-major, leading dim n),
-// optionally with symmetric pivoting and a relative drop tolerance.  Leaves
-// sm.perm, sm.rank and Rinv = R^-1 (upper triangular, rank x rank).
-__device__ void warp_cholesky_inverse(Smem& sm, int n, bool pivot) {
-  const int lane = threadIdx.x & 31;
-  for (int idx = lane; idx < kMaxR * kMaxR; idx += 32) {
-    const int a = idx / kMaxR, b = idx % kMaxR;
-    sm.Aw[a][b] = (a < n && b < n) ? sm.H[a * n + b] : 0.f;
-    sm.R[a][b] = 0.f;
-    sm.Rinv[a][b] = 0.f;
+// sm.H (n x n) from the upper-triangle sums in sm.S[0 .. n(n+1)/2).
+__device__ void expand_sym(Smem& sm, int n) {
+  for (int e = threadIdx.x; e < n * (n + 1) / 2; e += kThreads) {
+    int a, b;
+    sym_entry(e, n, a, b);
+    sm.H[a][b] = sm.S[e];
+    sm.H[b][a] = sm.S[e];
   }
-  if (lane < kMaxR) sm.perm[lane] = lane;
-  __syncwarp();
-  float dmax = 0.f;
-  for (int a = 0; a < n; ++a) dmax = fmaxf(dmax, sm.Aw[a][a]);
-  const float tol = pivot ? kDropTol * dmax : 0.f;
-  int rank = 0;
-  for (int kk = 0; kk < n; ++kk) {
-    int piv = kk;
-    if (pivot)
-      for (int j = kk + 1; j < n; ++j)
-        if (sm.Aw[j][j] > sm.Aw[piv][piv]) piv = j;
-    if (!(sm.Aw[piv][piv] > tol) || !(dmax > 0.f)) break;
-    if (piv != kk) {
-      // swap rows and columns kk <-> piv of the working matrix, the columns of
-      // the finished rows of R, and the permutation
-      if (lane < n) {
-        const float t0 = sm.Aw[kk][lane];
-        sm.Aw[kk][lane] = sm.Aw[piv][lane];
-        sm.Aw[piv][lane] = t0;
-      }
-      __syncwarp();
-      if (lane < n) {
-        const float t0 = sm.Aw[lane][kk];
-        sm.Aw[lane][kk] = sm.Aw[lane][piv];
-        sm.Aw[lane][piv] = t0;
-      }
-      if (lane < kk) {
-        const float t0 = sm.R[lane][kk];
-        sm.R[lane][kk] = sm.R[lane][piv];
-        sm.R[lane][piv] = t0;
-      }
-      if (lane == 0) {
-        const int tp = sm.perm[kk];
-        sm.perm[kk] = sm.perm[piv];
-        sm.perm[piv] = tp;
-      }
-      __syncwarp();
-    }
-    const float rkk = sqrtf(sm.Aw[kk][kk]);
-    if (lane >= kk && lane < n) sm.R[kk][lane] = lane == kk ? rkk : sm.Aw[kk][lane] / rkk;
-    __syncwarp();
-    // trailing update: Aw[a][b] -= R[kk][a] R[kk][b] for a, b > kk
-    for (int idx = lane; idx < kMaxR * kMaxR; idx += 32) {
-      const int a = idx / kMaxR, b = idx % kMaxR;
-      if (a > kk && b > kk && a < n && b < n) sm.Aw[a][b] -= sm.R[kk][a] * sm.R[kk][b];
-    }
-    __syncwarp();
-    ++rank;
-  }
-  // R^-1 by back substitution, one column per lane
-  if (lane < rank) {
-    const int j = lane;
-    sm.Rinv[j][j] = 1.f / sm.R[j][j];
-    for (int a = j - 1; a >= 0; --a) {
-      float s = 0.f;
-      for (int l = a + 1; l <= j; ++l) s = fmaf(sm.R[a][l], sm.Rinv[l][j], s);
-      sm.Rinv[a][j] = -s / sm.R[a][a];
-    }
-  }
-  if (lane == 0) sm.rank = rank;
-  __syncwarp();
 }
 
-// In place on the shared rows: x[:, b] <- sum_{a <= b} x[:, perm[a]] Rinv[a][b]
-// for b < rank, zero beyond.  Thread t owns rows t, t + 256.
-__device__ void apply_rinv(Smem& sm, int ncols) {
-  const int rank = sm.rank;
-  for (int c = threadIdx.x; c < kRows; c += kThreads) {
-    float v[kMaxR];
+// One thread: Cholesky H = R^T R of the n x n Gram in sm.H, fully unrolled in
+// registers.  A pivot below kDropTol times the largest diagonal entry marks
+// its column as dependent on the earlier ones: its row of R and its entry of
+// rdiag (= 1 / R[k][k]) are zero, so the matching column of Q comes out zero
+// and drops out of both the head and the tail projection.
+__device__ void serial_cholesky(Smem& sm, int n) {
+  float a[kMaxR][kMaxR];
 #pragma unroll
-    for (int a = 0; a < kMaxR; ++a) v[a] = (a < rank && a < ncols) ? sm.x[sm.perm[a]][c] : 0.f;
+  for (int i = 0; i < kMaxR; ++i)
+#pragma unroll
+    for (int j = i; j < kMaxR; ++j) a[i][j] = (i < n && j < n) ? sm.H[i][j] : 0.f;
+  float dmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxR; ++i) dmax = fmaxf(dmax, a[i][i]);
+  const float tol = kDropTol * dmax;
+#pragma unroll
+  for (int k = 0; k < kMaxR; ++k) {
+    const bool keep = k < n && a[k][k] > tol && dmax > 0.f;
+    const float rkk = keep ? sqrtf(a[k][k]) : 0.f;
+    const float inv = keep ? 1.f / rkk : 0.f;
+    sm.rdiag[k] = inv;
+    a[k][k] = rkk;
+#pragma unroll
+    for (int j = k + 1; j < kMaxR; ++j) a[k][j] *= inv;
+#pragma unroll
+    for (int i = k + 1; i < kMaxR; ++i)
+#pragma unroll
+      for (int j = i; j < kMaxR; ++j) a[i][j] = fmaf(-a[k][i], a[k][j], a[i][j]);
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxR; ++i)
+#pragma unroll
+    for (int j = 0; j < kMaxR; ++j) sm.R[i][j] = j >= i ? a[i][j] : 0.f;
+}
+
+// In place on the shared rows: x[c, :] <- x[c, :] R^-1 by forward
+// substitution, q[b] = (x[b] - sum_{a<b} q[a] R[a][b]) / R[b][b] (zero for a
+// dropped column).  Thread t owns rows t, t + 256.
+__device__ void apply_rinv(Smem& sm, int n) {
+  for (int c = threadIdx.x; c < kRows; c += kThreads) {
+    float q[kMaxR];
 #pragma unroll
     for (int b = 0; b < kMaxR; ++b) {
-      float s = 0.f;
+      float s = b < n ? sm.x[b][c] : 0.f;
 #pragma unroll
-      for (int a = 0; a <= b; ++a) s = fmaf(v[a], sm.Rinv[a][b], s);
-      sm.x[b][c] = b < rank ? s : 0.f;
+      for (int a = 0; a < b; ++a) s = fmaf(-q[a], sm.R[a][b], s);
+      q[b] = s * sm.rdiag[b];
     }
+#pragma unroll
+    for (int b = 0; b < kMaxR; ++b) sm.x[b][c] = q[b];
   }
 }
 
@@ -219,9 +186,9 @@ __global__ void __launch_bounds__(kThreads) hpp_qr_kernel(const __grid_constant_
   const int c0 = chunk * kRows;
   const int r = p.r, m = p.m;
   const bool active = i < p.B;   // grids are whole samples; guard anyway
-  float* part1 = p.part + ((size_t)0 * p.B + (active ? i : 0)) * cps * kMaxE;
-  float* part2 = p.part + ((size_t)1 * p.B + (active ? i : 0)) * cps * kMaxE;
-  float* part3 = p.part + ((size_t)2 * p.B + (active ? i : 0)) * cps * kMaxE;
+  const int ia = active ? i : 0;
+  float* part1 = p.part + ((size_t)0 * p.B + ia) * cps * kPartStride;
+  float* part2 = p.part + ((size_t)1 * p.B + ia) * cps * kPartStride;
 
   // ---- stage this CTA's rows of V (r columns) and G' (m columns); the loads
   // of 16 consecutive elements per thread are issued before any is stored
@@ -262,64 +229,89 @@ __global__ void __launch_bounds__(kThreads) hpp_qr_kernel(const __grid_constant_
   }
   __syncthreads();
 
-  // ---- pass 1: pivoted Cholesky of V^T V; Q1 = V P R^-1
-  if (active) partial_cross(sm.x, r, sm.x, r, true, part1 + (size_t)chunk * kMaxE);
+  // ---- pass 1: Cholesky of V^T V; Q1 = V R1^-1
+  const int ne = r * (r + 1) / 2;
+  if (active) partial_cross(sm.x, r, sm.x, r, true, part1 + (size_t)chunk * kPartStride);
   __threadfence();
   grid.sync();
-  if (active) sum_partials(sm, part1, cps, r, r, true);
+  if (active) sum_partials(sm, part1, cps, ne);
   __syncthreads();
-  if (threadIdx.x < 32) warp_cholesky_inverse(sm, r, true);
+  expand_sym(sm, r);
+  __syncthreads();
+  if (threadIdx.x == 0) serial_cholesky(sm, r);
   __syncthreads();
   apply_rinv(sm, r);
   __syncthreads();
-  const int rank1 = sm.rank;
 
-  // ---- pass 2: Cholesky of Q1^T Q1 (close to the identity); Q = Q1 R2^-1
-  if (active) partial_cross(sm.x, rank1, sm.x, rank1, true, part2 + (size_t)chunk * kMaxE);
+  // ---- pass 2, one reduction for both: Q1^T Q1 (close to the identity) and
+  // K = Q1^T G'.  Then Q = Q1 R2^-1 and Q^T G' = R2^-T K.
+  if (active) {
+    float* mine = part2 + (size_t)chunk * kPartStride;
+    partial_cross(sm.x, r, sm.x, r, true, mine);
+    partial_cross(sm.x, r, sm.g, m, false, mine + ne);
+  }
   __threadfence();
   grid.sync();
-  if (active) sum_partials(sm, part2, cps, rank1, rank1, true);
+  if (active) sum_partials(sm, part2, cps, ne + r * m);
   __syncthreads();
-  if (threadIdx.x < 32) warp_cholesky_inverse(sm, rank1, false);
+  expand_sym(sm, r);
+  for (int e = threadIdx.x; e < r * m; e += kThreads) sm.K[e / m][e % m] = sm.S[ne + e];
   __syncthreads();
-  apply_rinv(sm, rank1);
+  if (threadIdx.x == 0) serial_cholesky(sm, r);
   __syncthreads();
-  const int rank = sm.rank;
-
-  // ---- tail probes: C = Q^T G' (rank x m), W = G' - Q C
-  if (active) partial_cross(sm.x, rank, sm.g, m, false, part3 + (size_t)chunk * kMaxE);
-  __threadfence();
-  grid.sync();
-  if (active) sum_partials(sm, part3, cps, rank, m, false);
+  // C = R2^-T K by forward substitution, one tail column per thread
+  if (threadIdx.x < m) {
+    const int l = threadIdx.x;
+    float cc[kMaxR];
+#pragma unroll
+    for (int b = 0; b < kMaxR; ++b) {
+      float s = b < r ? sm.K[b][l] : 0.f;
+#pragma unroll
+      for (int a = 0; a < b; ++a) s = fmaf(-sm.R[a][b], cc[a], s);
+      cc[b] = s * sm.rdiag[b];
+      sm.Cm[b][l] = cc[b];
+    }
+  }
+  apply_rinv(sm, r);
   __syncthreads();
   if (!active) return;
-  for (int idx = threadIdx.x; idx < kMaxNP * kRows; idx += kThreads) {
-    const int j = idx / kRows, c = idx % kRows;
-    if (c0 + c >= p.p) continue;
-    float val = 0.f;
-    if (j < rank) {
-      val = sm.x[j][c];
-    } else if (j >= r && j < r + m) {
-      const int l = j - r;
-      float s = sm.g[l][c];
-      for (int a = 0; a < rank; ++a) s = fmaf(-sm.x[a][c], sm.H[a * m + l], s);
-      val = s;
-    }
-    const size_t o = ((size_t)i * kMaxNP + j) * p.p + c0 + c;
-    if (p.out_f32) {
-      p.out_f32[o] = val;
-    } else {
-      __nv_bfloat16 hi, lo;
-      split_hilo(val, hi, lo);
-      p.out_hi[o] = hi;
-      p.out_lo[o] = lo;
+
+  // ---- outputs [Q | W | 0], W = G' - Q (Q^T G'); each thread owns rows
+  for (int c = threadIdx.x; c < kRows; c += kThreads) {
+    if (c0 + c >= p.p) break;
+    float qrow[kMaxR];
+#pragma unroll
+    for (int a = 0; a < kMaxR; ++a) qrow[a] = sm.x[a][c];
+#pragma unroll
+    for (int j = 0; j < kMaxNP; ++j) {
+      float val = 0.f;
+      if (j < kMaxR && j < r) {
+        val = qrow[j < kMaxR ? j : 0];
+      } else if (j >= r && j < r + m) {
+        const int l = j - r;
+        float s = sm.g[l][c];
+#pragma unroll
+        for (int a = 0; a < kMaxR; ++a) s = fmaf(-qrow[a], sm.Cm[a][l], s);
+        val = s;
+      }
+      const size_t o = ((size_t)i * kMaxNP + j) * p.p + c0 + c;
+      if (p.out_f32) {
+        p.out_f32[o] = val;
+      } else {
+        __nv_bfloat16 hi, lo;
+        split_hilo(val, hi, lo);
+        p.out_hi[o] = hi;
+        p.out_lo[o] = lo;
+      }
     }
   }
 }
 
 }  // namespace
 
-size_t hpp_qr_part_floats(int B, int p) { return (size_t)3 * B * ((p + kRows - 1) / kRows) * kMaxE; }
+size_t hpp_qr_part_floats(int B, int p) {
+  return (size_t)2 * B * ((p + kRows - 1) / kRows) * kPartStride;
+}
 
 cudaError_t launch_hpp_qr(const HppQrParams& p_in, cudaStream_t s) {
   if (p_in.r > kMaxR || p_in.m > kMaxM || p_in.r + p_in.m > kMaxNP) return cudaErrorInvalidValue;

@@ -129,7 +129,7 @@ struct GhostParams {
 };
 
 // Hutch++ middle step: per sample, orthonormal basis Q of V (p x r) by
-// pivoted CholeskyQR2 (fp32), W = G' - Q (Q^T G'), output [Q | W] padded to
+// CholeskyQR2 (fp32, dependent columns dropped), W = G' - Q (Q^T G'), output [Q | W] padded to
 // 32 columns, as hi/lo bf16 or fp32, [B][32][p].  Cooperative launch.
 struct HppQrParams {
   const float* V;        // [B][ldv][p] fp32, columns j < r used
