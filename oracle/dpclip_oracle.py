@@ -38,6 +38,10 @@ in the design notes):
     lanes 0/1 = sqrt(-2 ln u(w0)) cos/sin(2 pi v(w1)), lanes 2/3 the same from
     words 2 and 3.
   * bf16 workloads use probes rounded to bfloat16 (nearest even).
+  * Rademacher probes (the {+-1} sketches the summary names as future work,
+    "Empirical results" / claims): element e is +1 when the top bit of word
+    e % 4 of Philox block e // 4 is clear, -1 when it is set (same counters
+    as the normals).
   * Noise N(0, sigma^2 C^2 I) is added once to the clipped sum; the 1/|B| of
     the SGD update (GL step 5) is not applied.
 """
@@ -47,7 +51,7 @@ import numpy as np
 
 __all__ = [
     "STREAM_P", "STREAM_S", "STREAM_GP", "STREAM_NOISE",
-    "philox4x32_10", "philox_normals", "round_bf16", "probe_rows",
+    "philox4x32_10", "philox_normals", "philox_rademacher", "round_bf16", "probe_rows",
     "per_sample_grads", "sqnorms_direct", "sqnorms_trace", "sqnorms_ghost",
     "sqnorms_outer_bruteforce",
     "hutch_probe", "sqnorms_hutch", "hutchpp_split", "hutchpp_probes",
@@ -114,6 +118,21 @@ def philox_normals(n: int, seed: int, stream: int, offset: int, start: int = 0) 
     return z.reshape(-1)[idx]
 
 
+def philox_rademacher(n: int, seed: int, stream: int, offset: int, start: int = 0) -> np.ndarray:
+    """Rademacher values r[start : start + n] of one Philox stream (fp64):
+    +1 or -1 from the top bit of word e % 4 of Philox block e // 4."""
+    e = np.arange(start, start + n, dtype=np.uint64)
+    blocks = np.unique(e >> np.uint64(2))
+    words = philox4x32_10(
+        (blocks, np.full_like(blocks, stream), np.full_like(blocks, offset & 0xFFFFFFFF),
+         np.full_like(blocks, (offset >> 32) & 0xFFFFFFFF)),
+        (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
+    top = (words >> np.uint32(31)).astype(np.float64)       # 0 or 1
+    vals = 1.0 - 2.0 * top
+    idx = (e - (blocks[0] << np.uint64(2))).astype(np.int64)
+    return vals.reshape(-1)[idx]
+
+
 def round_bf16(x: np.ndarray) -> np.ndarray:
     """Round fp64 values to the nearest bfloat16 value (8 significant bits,
     ties to even), returned as fp64.  Values here are finite and normal."""
@@ -122,9 +141,15 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     return np.ldexp(np.rint(mant * 256.0), expo - 8)
 
 
-def probe_rows(rows: int, cols: int, seed: int, stream: int, offset: int, dtype: str) -> np.ndarray:
+def probe_rows(rows: int, cols: int, seed: int, stream: int, offset: int, dtype: str,
+               kind: str = "gaussian") -> np.ndarray:
     """rows x cols matrix of stream `stream`, element (j, c) at index j*cols + c.
-    bf16 workloads round every value to bfloat16."""
+    Gaussian probes of bf16 workloads are rounded to bfloat16; Rademacher
+    values are exact in every format."""
+    if kind == "rademacher":
+        return philox_rademacher(rows * cols, seed, stream, offset).reshape(rows, cols)
+    if kind != "gaussian":
+        raise ValueError(f"unknown probe kind {kind!r}")
     z = philox_normals(rows * cols, seed, stream, offset).reshape(rows, cols)
     return round_bf16(z) if dtype == "bf16" else z
 
@@ -188,10 +213,11 @@ def sqnorms_outer_bruteforce(A, G) -> np.ndarray:
 # Hutch (RC, Core mechanism, item 1)
 # --------------------------------------------------------------------------
 
-def hutch_probe(p: int, k: int, seed: int, offset: int, dtype: str) -> np.ndarray:
-    """The p x k Gaussian probe matrix P (stored by the GPU path as k rows of
-    length p, element (j, c) at j*p + c of stream 0)."""
-    return probe_rows(k, p, seed, STREAM_P, offset, dtype).T
+def hutch_probe(p: int, k: int, seed: int, offset: int, dtype: str,
+                kind: str = "gaussian") -> np.ndarray:
+    """The p x k probe matrix P (stored by the GPU path as k rows of length p,
+    element (j, c) at j*p + c of stream 0); Gaussian or Rademacher."""
+    return probe_rows(k, p, seed, STREAM_P, offset, dtype, kind).T
 
 
 def sqnorms_hutch(A, G, P: np.ndarray, Ms=None) -> np.ndarray:
@@ -224,11 +250,11 @@ def hutchpp_split(k: int):
     return r, m
 
 
-def hutchpp_probes(p: int, k: int, seed: int, offset: int, dtype: str):
+def hutchpp_probes(p: int, k: int, seed: int, offset: int, dtype: str, kind: str = "gaussian"):
     """S (p x r, stream 1) and G' (p x m, stream 2), stored row-per-column like P."""
     r, m = hutchpp_split(k)
-    S = probe_rows(r, p, seed, STREAM_S, offset, dtype).T
-    Gp = probe_rows(m, p, seed, STREAM_GP, offset, dtype).T
+    S = probe_rows(r, p, seed, STREAM_S, offset, dtype, kind).T
+    Gp = probe_rows(m, p, seed, STREAM_GP, offset, dtype, kind).T
     return S, Gp
 
 

@@ -263,3 +263,60 @@ def test_noise_law_and_determinism():
     assert scipy.stats.kstest(z, "norm").pvalue > 1e-4
     D2, _, _ = O.clipped_noisy_grad(A, G, q, C, sigma, seed=3, offset=4)
     assert np.array_equal(D1, D2)                  # same (seed, offset): same noise
+
+
+# --------------------------------------------------------------- Rademacher probes
+
+def test_rademacher_values_and_balance():
+    r = O.philox_rademacher(1 << 20, seed=77, stream=0, offset=3)
+    assert set(np.unique(r)) == {-1.0, 1.0}
+    n = r.size
+    assert abs(r.mean()) < 5 / math.sqrt(n)
+    pairs = r.reshape(-1, 2)
+    assert abs(np.mean(pairs[:, 0] * pairs[:, 1])) < 5 / math.sqrt(n / 2)
+    # same counters as the normals: the sign bit of the word behind each element
+    part = O.philox_rademacher(50, seed=77, stream=0, offset=3, start=1001)
+    assert np.array_equal(part, r[1001:1051])
+    w = O.philox4x32_10((250, 0, 3, 0), (77, 0))          # block 250 = elements 1000..1003
+    assert [1.0 - 2.0 * (int(x) >> 31) for x in w] == list(r[1000:1004])
+
+
+def test_rademacher_hutch_exact_for_diagonal_O():
+    # G_i = I (T = p) and A_i with orthogonal rows: O_i = A_i A_i^T is diagonal,
+    # so every Rademacher probe z gives z^T O z = trace(O) exactly.
+    p, d = 6, 9
+    A = np.zeros((2, p, d))
+    A[0, :, :p] = np.diag([1.0, 2.0, 0.5, 3.0, 1.5, 0.25])
+    A[1, :, 2:2 + p] = np.diag([2.0, 1.0, 1.0, 0.5, 4.0, 1.0])
+    G = np.stack([np.eye(p), np.eye(p)])
+    exact = O.sqnorms_direct(A, G)
+    for off in range(20):
+        P = O.hutch_probe(p, 3, seed=5, offset=off, dtype="f32", kind="rademacher")
+        np.testing.assert_allclose(O.sqnorms_hutch(A, G, P), exact, rtol=1e-13)
+    # Gaussian probes are not exact there
+    P = O.hutch_probe(p, 3, seed=5, offset=0, dtype="f32")
+    assert not np.allclose(O.sqnorms_hutch(A, G, P), exact, rtol=1e-3)
+
+
+def test_rademacher_hutch_unbiased_with_closed_form_variance():
+    A, G = _tiny(B=1, T=12, d=6, p=10, seed=9)
+    M = A[0].T @ G[0]
+    Om = M.T @ M
+    exact = np.trace(Om)
+    k, N = 4, 4000
+    est = np.array([O.sqnorms_hutch(None, None, O.hutch_probe(10, k, 78, off, "f32", "rademacher"),
+                                    Ms=[M])[0] for off in range(N)])
+    assert abs(est.mean() - exact) < 4 * est.std(ddof=1) / math.sqrt(N)
+    var_true = 2.0 * (np.sum(Om * Om) - np.sum(np.diag(Om) ** 2)) / k
+    assert abs(est.var(ddof=1) / var_true - 1.0) < 0.15
+
+
+def test_rademacher_hutchpp_exact_at_low_rank_and_unbiased():
+    A, G = _tiny(B=2, T=4, d=9, p=12, seed=10)
+    S, Gp = O.hutchpp_probes(12, 15, seed=3, offset=0, dtype="f32", kind="rademacher")
+    np.testing.assert_allclose(O.sqnorms_hutchpp(A, G, S, Gp), O.sqnorms_direct(A, G), rtol=1e-10)
+    A, G = _tiny(B=1, T=30, d=7, p=11, seed=12)
+    M = A[0].T @ G[0]
+    est = np.array([O.sqnorms_hutchpp(None, None, *O.hutchpp_probes(11, 6, 31, off, "f32", "rademacher"),
+                                      Ms=[M])[0] for off in range(1500)])
+    assert abs(est.mean() - np.sum(M * M)) < 4 * est.std(ddof=1) / math.sqrt(1500)
