@@ -36,6 +36,8 @@ sys.path.insert(0, ROOT)
 WORKLOAD_ID = 4
 METRIC = "clip+noise tokens/s per linear layer (Hutch/Hutch++/exact); % bf16 tensor peak"
 ROWS = ("hutch", "hutchpp", "exact_direct", "exact_ghost", "clipped_noisy_grad")
+# measured after the step, not part of it: the Rademacher-probe variants
+EXTRA_ROWS = ("hutch_rademacher", "hutchpp_rademacher")
 # kernels each ABI call launches for bf16 inputs (memsets of the control block excluded)
 LAUNCHES = {"hutch": 3, "hutchpp": 9, "exact_direct": 1, "exact_ghost": 1, "clipped_noisy_grad": 1}
 
@@ -49,6 +51,8 @@ def algorithmic_work(wl):
     return {
         "hutch": (ag + 2.0 * k * p, "bytes", "hbm"),
         "hutchpp": (3.0 * ag, "bytes", "hbm"),
+        "hutch_rademacher": (ag + 2.0 * k * p, "bytes", "hbm"),
+        "hutchpp_rademacher": (3.0 * ag, "bytes", "hbm"),
         "exact_direct": (2.0 * B * T * d * p, "flops", "tensor"),
         "exact_ghost": (1.0 * B * T * (T + 1) * (d + p), "flops", "tensor"),
         "clipped_noisy_grad": (2.0 * B * T * d * p, "flops", "tensor"),
@@ -202,6 +206,7 @@ def main():
     ap.add_argument("--impl", default="dpclip", choices=("dpclip", "reference"))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the extra (non-step) rows")
     ap.add_argument("--rows", default=",".join(ROWS),
                     help="comma-separated subset of rows (default: all, the full step)")
     args = ap.parse_args()
@@ -259,6 +264,12 @@ def main():
         if name == "hutchpp":
             return lambda: api.norms_hutchpp(b["A"], b["G"], k, wl.seed, step, out=b["q_pp"],
                                              ws=ws[name])
+        if name == "hutch_rademacher":
+            return lambda: api.norms_hutch(b["A"], b["G"], k, wl.seed, step, out=b["q_h"],
+                                           ws=ws["hutch"], probe="rademacher")
+        if name == "hutchpp_rademacher":
+            return lambda: api.norms_hutchpp(b["A"], b["G"], k, wl.seed, step, out=b["q_pp"],
+                                             ws=ws["hutchpp"], probe="rademacher")
         if name == "exact_direct":
             return lambda: api.norms_exact(b["A"], b["G"], L.EXACT_DIRECT, out=b["q_d"], ws=ws[name])
         if name == "exact_ghost":
@@ -389,6 +400,22 @@ def main():
                "pipelining": "inputs of step s+1 and results of step s-1 copied on two "
                              "copy streams while step s computes"}
 
+    # ---------------------------------------------------------------- extra rows (not in the step)
+    extra_ms = {}
+    if not args.no_extra:
+        for r in EXTRA_ROWS:
+            for s_ in range(args.warmup):
+                row_fn(r, s_)()
+            barrier()
+            x0 = torch.cuda.Event(enable_timing=True)
+            x1 = torch.cuda.Event(enable_timing=True)
+            x0.record(stream)
+            for s_ in range(args.steps):
+                row_fn(r, args.warmup + s_)()
+            x1.record(stream)
+            barrier()
+            extra_ms[r] = x0.elapsed_time(x1) / args.steps
+
     if rank != 0:
         if pg is not None:
             pg.barrier()
@@ -409,6 +436,12 @@ def main():
         breakdown[r] = {"ms": round(ms, 4), "tokens_per_s": B * T / (ms * 1e-3),
                         "bound": bound, "achieved": round(ach, 2), "peak": pk, "unit": u,
                         "frac": round(ach / pk, 4), "algorithmic": amount}
+    extra = {}
+    for r, ms in extra_ms.items():
+        amount, unit, bound = work[r]
+        ach, pk, u = amount / (ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        extra[r] = {"ms": round(ms, 4), "tokens_per_s": B * T / (ms * 1e-3), "bound": bound,
+                    "achieved": round(ach, 2), "peak": pk, "unit": u, "frac": round(ach / pk, 4)}
     dom = max(rows, key=lambda r: row_ms[r])
     traffic = _traffic_from_profiles(dom)
     roof = dict(breakdown[dom])
@@ -422,7 +455,8 @@ def main():
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(wl), "gpu_launches": args.steps * sum(LAUNCHES[r] for r in rows),
-            "roofline": roofline, "breakdown": breakdown, "clocks": clk, "e2e": e2e}
+            "roofline": roofline, "breakdown": breakdown, "extra_rows": extra, "clocks": clk,
+            "e2e": e2e}
     if world == 1 and not args.no_cpu_baseline:
         v, t, threads, desc = cpu_baseline(wl, 1024, wl.p)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": threads,

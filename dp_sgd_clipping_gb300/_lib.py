@@ -21,6 +21,8 @@ F32 = 0
 BF16 = 1
 
 EXACT_AUTO, EXACT_GHOST, EXACT_DIRECT = 0, 1, 2
+PROBE_GAUSSIAN, PROBE_RADEMACHER = 0, 1
+PROBES = {"gaussian": PROBE_GAUSSIAN, "rademacher": PROBE_RADEMACHER}
 OP_NORMS_EXACT, OP_NORMS_HUTCH, OP_NORMS_HUTCHPP, OP_CLIPPED_NOISY_GRAD = 0, 1, 2, 3
 HUTCH_MAX_K = 32
 HUTCHPP_MAX_K = 48
@@ -36,6 +38,11 @@ SIGNATURES = {
     "dpclip_norms_exact": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "dpclip_norms_hutch": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp, _sz, _vp]),
     "dpclip_norms_hutchpp": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp, _sz, _vp]),
+    "dpclip_norms_hutch_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp, _sz,
+                                   _vp]),
+    "dpclip_norms_hutchpp_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp,
+                                     _sz, _vp]),
+    "dpclip_philox_rademacher": (_i, [_vp, _i64, _i, _u64, _u32, _u64, _vp]),
     "dpclip_clipped_noisy_grad": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _f, _u64, _u64,
                                        _vp, _vp, _vp, _vp, _sz, _vp]),
     "dpclip_clip_scales": (_i, [_vp, _i, _f, _vp, _vp, _vp]),

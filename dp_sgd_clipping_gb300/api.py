@@ -12,7 +12,8 @@ import torch
 from . import _lib as L
 
 __all__ = ["norms_exact", "norms_hutch", "norms_hutchpp", "clipped_noisy_grad", "clip_scales",
-           "philox_normal", "workspace_bytes", "workspace_status", "selftest_wait_timeout"]
+           "philox_normal", "philox_rademacher", "workspace_bytes", "workspace_status",
+           "selftest_wait_timeout"]
 
 _DT = {torch.float32: L.F32, torch.bfloat16: L.BF16}
 
@@ -58,25 +59,27 @@ def norms_exact(A, G, method: int = L.EXACT_AUTO, out=None, ws=None, stream=None
     return out
 
 
-def norms_hutch(A, G, k: int, seed: int, offset: int = 0, out=None, ws=None, stream=None):
+def norms_hutch(A, G, k: int, seed: int, offset: int = 0, out=None, ws=None, stream=None,
+                probe: str = "gaussian"):
     B, T, d, p, dt = _check_pair(A, G)
     nb = workspace_bytes(L.OP_NORMS_HUTCH, B, T, d, p, dt, k)
     ws = _workspace(nb, A.device, ws)
     out = torch.empty(B, dtype=torch.float32, device=A.device) if out is None else out
-    L.check("dpclip_norms_hutch", L.lib.dpclip_norms_hutch(
-        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, k, seed, offset, out.data_ptr(),
-        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    L.check("dpclip_norms_hutch_ex", L.lib.dpclip_norms_hutch_ex(
+        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, k, L.PROBES[probe], seed, offset,
+        out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
     return out
 
 
-def norms_hutchpp(A, G, k: int, seed: int, offset: int = 0, out=None, ws=None, stream=None):
+def norms_hutchpp(A, G, k: int, seed: int, offset: int = 0, out=None, ws=None, stream=None,
+                  probe: str = "gaussian"):
     B, T, d, p, dt = _check_pair(A, G)
     nb = workspace_bytes(L.OP_NORMS_HUTCHPP, B, T, d, p, dt, k)
     ws = _workspace(nb, A.device, ws)
     out = torch.empty(B, dtype=torch.float32, device=A.device) if out is None else out
-    L.check("dpclip_norms_hutchpp", L.lib.dpclip_norms_hutchpp(
-        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, k, seed, offset, out.data_ptr(),
-        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    L.check("dpclip_norms_hutchpp_ex", L.lib.dpclip_norms_hutchpp_ex(
+        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, k, L.PROBES[probe], seed, offset,
+        out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
     return out
 
 
@@ -114,6 +117,14 @@ def philox_normal(n: int, seed: int, stream_id: int, offset: int = 0, dtype=torc
                   device="cuda", stream=None):
     out = torch.empty(n, dtype=dtype, device=device)
     L.check("dpclip_philox_normal", L.lib.dpclip_philox_normal(
+        out.data_ptr(), n, _DT[dtype], seed, stream_id, offset, _stream(stream)))
+    return out
+
+
+def philox_rademacher(n: int, seed: int, stream_id: int, offset: int = 0, dtype=torch.float32,
+                      device="cuda", stream=None):
+    out = torch.empty(n, dtype=dtype, device=device)
+    L.check("dpclip_philox_rademacher", L.lib.dpclip_philox_rademacher(
         out.data_ptr(), n, _DT[dtype], seed, stream_id, offset, _stream(stream)))
     return out
 

@@ -8,13 +8,15 @@
 namespace dpclip {
 namespace {
 
-// out (rows x cols, row-major) = normals of one Philox stream for the first
+// out (rows x cols, row-major) = probes of one Philox stream for the first
 // rows_valid rows (element e = j * cols + c uses Philox block e / 4, lane
-// e % 4), zeros below.  One thread per Philox block of four elements.
+// e % 4), zeros below.  kind 0: standard normals (Box-Muller); kind 1:
+// Rademacher values, +1 / -1 by the top bit of the lane's word.  One thread
+// per Philox block of four elements.
 template <bool kBf16>
 __global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
                                    uint64_t seed, uint32_t stream_id, uint64_t offset,
-                                   uint32_t* zero, int zero_words) {
+                                   uint32_t* zero, int zero_words, int kind) {
   pdl_trigger();
   pdl_wait();
   if (zero)
@@ -25,7 +27,19 @@ __global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_
   for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblk;
        b += (int64_t)gridDim.x * blockDim.x) {
     float z[4] = {0.f, 0.f, 0.f, 0.f};
-    if (4 * b < nvalid) philox_normal4(seed, stream_id, offset, (uint32_t)b, z);
+    if (4 * b < nvalid) {
+      if (kind == 1) {
+        const U4 x = philox4x32_10(U4{(uint32_t)b, stream_id, (uint32_t)offset,
+                                      (uint32_t)(offset >> 32)},
+                                   (uint32_t)seed, (uint32_t)(seed >> 32));
+        z[0] = (x.x >> 31) ? -1.f : 1.f;
+        z[1] = (x.y >> 31) ? -1.f : 1.f;
+        z[2] = (x.z >> 31) ? -1.f : 1.f;
+        z[3] = (x.w >> 31) ? -1.f : 1.f;
+      } else {
+        philox_normal4(seed, stream_id, offset, (uint32_t)b, z);
+      }
+    }
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
       const int64_t e = 4 * b + l;
@@ -111,16 +125,16 @@ __global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
 
 cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid, bool bf16,
                                uint64_t seed, uint32_t stream_id, uint64_t offset, cudaStream_t s,
-                               uint32_t* zero, int zero_words) {
+                               uint32_t* zero, int zero_words, int kind) {
   const int64_t nblk = (rows * cols + 3) / 4;
   const int threads = 256;
   const int grid = (int)std::max<int64_t>(
       1, std::min<int64_t>((nblk + threads - 1) / threads, 152 * 16));
   if (bf16)
     return launch_pdl(philox_fill_kernel<true>, dim3(grid), dim3(threads), 0, s, false, out, rows,
-                      cols, rows_valid, seed, stream_id, offset, zero, zero_words);
+                      cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
   return launch_pdl(philox_fill_kernel<false>, dim3(grid), dim3(threads), 0, s, false, out, rows,
-                    cols, rows_valid, seed, stream_id, offset, zero, zero_words);
+                    cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
 }
 
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,

@@ -462,6 +462,18 @@ int dpclip_philox_normal(void* out, int64_t n, int dtype, uint64_t seed, uint32_
   return DPCLIP_OK;
 }
 
+int dpclip_philox_rademacher(void* out, int64_t n, int dtype, uint64_t seed, uint32_t stream_id,
+                             uint64_t offset, dpclip_stream_t stream) {
+  if (!out || n < 0) return DPCLIP_ERR_INVALID_ARG;
+  if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
+  if (!aligned(out, 4)) return DPCLIP_ERR_UNSUPPORTED;
+  if (n > (int64_t)4 * 0xFFFFFFFFll) return DPCLIP_ERR_UNSUPPORTED;
+  if (n == 0) return DPCLIP_OK;
+  DPCLIP_CUDA(launch_philox_fill(out, 1, n, 1, dtype == DPCLIP_BF16, seed, stream_id, offset,
+                                 (cudaStream_t)stream, nullptr, 0, DPCLIP_PROBE_RADEMACHER));
+  return DPCLIP_OK;
+}
+
 int dpclip_clip_scales(const float* sqnorms, int B, float C, float* scales, uint8_t* clipped,
                        dpclip_stream_t stream) {
   if (!sqnorms || B <= 0) return DPCLIP_ERR_INVALID_ARG;
@@ -552,9 +564,11 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
   return DPCLIP_OK;
 }
 
-int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p, int dtype, int k,
-                       uint64_t seed, uint64_t offset, float* sqnorms, void* ws, size_t ws_bytes,
-                       dpclip_stream_t stream) {
+int dpclip_norms_hutch_ex(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                          int k, int probe, uint64_t seed, uint64_t offset, float* sqnorms,
+                          void* ws, size_t ws_bytes, dpclip_stream_t stream) {
+  if (probe != DPCLIP_PROBE_GAUSSIAN && probe != DPCLIP_PROBE_RADEMACHER)
+    return DPCLIP_ERR_INVALID_ARG;
   DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
   if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
   Plan pl;
@@ -567,7 +581,7 @@ int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p,
   if (dtype == DPCLIP_BF16) {
     const int NP = np_for(k);
     void* P = at<void>(ws, pl.off[kP]);
-    DPCLIP_CUDA(launch_philox_fill(P, NP, p, k, true, seed, 0u, offset, s, ctrl, ctrl_words));
+    DPCLIP_CUDA(launch_philox_fill(P, NP, p, k, true, seed, 0u, offset, s, ctrl, ctrl_words, probe));
     void* Yhi = at<void>(ws, pl.off[kYhi]);
     void* Ylo = at<void>(ws, pl.off[kYlo]);
     DPCLIP_TRY(run_tok(G, B, T, p, P, nullptr, NP, false, pl, ws, pl.off[kPart], Yhi, Ylo, s));
@@ -581,7 +595,7 @@ int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p,
   const float* Gf = static_cast<const float*>(G);
   float* P = at<float>(ws, pl.off[kFP]);
   float* Y = at<float>(ws, pl.off[kFY]);
-  DPCLIP_CUDA(launch_philox_fill(P, k, p, k, false, seed, 0u, offset, s, ctrl, ctrl_words));
+  DPCLIP_CUDA(launch_philox_fill(P, k, p, k, false, seed, 0u, offset, s, ctrl, ctrl_words, probe));
   SimtParams sp = simt_base();
   int nb = 0;
   sp.X = Gf; sp.xb = (long long)T * p; sp.xm = p; sp.xk = 1;        // G_i : (t, c)
@@ -599,9 +613,11 @@ int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p,
   return DPCLIP_OK;
 }
 
-int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int p, int dtype, int k,
-                         uint64_t seed, uint64_t offset, float* sqnorms, void* ws, size_t ws_bytes,
-                         dpclip_stream_t stream) {
+int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                            int k, int probe, uint64_t seed, uint64_t offset, float* sqnorms,
+                            void* ws, size_t ws_bytes, dpclip_stream_t stream) {
+  if (probe != DPCLIP_PROBE_GAUSSIAN && probe != DPCLIP_PROBE_RADEMACHER)
+    return DPCLIP_ERR_INVALID_ARG;
   DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
   if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
   Plan pl;
@@ -616,8 +632,8 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
   if (dtype == DPCLIP_BF16) {
     void* S = at<void>(ws, pl.off[kS]);
     void* Gp = at<void>(ws, pl.off[kGp]);
-    DPCLIP_CUDA(launch_philox_fill(S, 16, p, r, true, seed, 1u, offset, s, ctrl, ctrl_words));
-    DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, true, seed, 2u, offset, s));
+    DPCLIP_CUDA(launch_philox_fill(S, 16, p, r, true, seed, 1u, offset, s, ctrl, ctrl_words, probe));
+    DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, true, seed, 2u, offset, s, nullptr, 0, probe));
     void *Y1h = at<void>(ws, pl.off[kY1hi]), *Y1l = at<void>(ws, pl.off[kY1lo]);
     void *Z1h = at<void>(ws, pl.off[kZ1hi]), *Z1l = at<void>(ws, pl.off[kZ1lo]);
     void *Uh = at<void>(ws, pl.off[kUhi]), *Ul = at<void>(ws, pl.off[kUlo]);
@@ -665,8 +681,8 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
   float* V = at<float>(ws, pl.off[kFV]);
   float* QW = at<float>(ws, pl.off[kFQW]);
   float* Y3 = at<float>(ws, pl.off[kFY3]);
-  DPCLIP_CUDA(launch_philox_fill(S, r, p, r, false, seed, 1u, offset, s, ctrl, ctrl_words));
-  DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, false, seed, 2u, offset, s));
+  DPCLIP_CUDA(launch_philox_fill(S, r, p, r, false, seed, 1u, offset, s, ctrl, ctrl_words, probe));
+  DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, false, seed, 2u, offset, s, nullptr, 0, probe));
   int nb = 0;
   SimtParams sp = simt_base();
   // Y1 = G S
@@ -727,6 +743,20 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
   DPCLIP_CUDA(launch_simt(sp, kSimtSqNorm, s, &nb));
   DPCLIP_CUDA(launch_finalize_norms(sp.part, B, nb, 1, nb, 1, 1.f, sqnorms, s));
   return DPCLIP_OK;
+}
+
+int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p, int dtype, int k,
+                       uint64_t seed, uint64_t offset, float* sqnorms, void* ws, size_t ws_bytes,
+                       dpclip_stream_t stream) {
+  return dpclip_norms_hutch_ex(A, G, B, T, d, p, dtype, k, DPCLIP_PROBE_GAUSSIAN, seed, offset,
+                               sqnorms, ws, ws_bytes, stream);
+}
+
+int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int p, int dtype, int k,
+                         uint64_t seed, uint64_t offset, float* sqnorms, void* ws, size_t ws_bytes,
+                         dpclip_stream_t stream) {
+  return dpclip_norms_hutchpp_ex(A, G, B, T, d, p, dtype, k, DPCLIP_PROBE_GAUSSIAN, seed, offset,
+                                 sqnorms, ws, ws_bytes, stream);
 }
 
 int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d, int p, int dtype,

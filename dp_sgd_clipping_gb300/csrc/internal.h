@@ -181,11 +181,13 @@ size_t hpp_qr_part_floats(int B, int p);
 cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblocks_out);
 int simt_nblocks(int M, int N);
 
-// Also clears `zero_words` 32-bit words at `zero` (the control block of a
-// multi-kernel call) when zero != nullptr.
+// kind: DPCLIP_PROBE_GAUSSIAN or DPCLIP_PROBE_RADEMACHER.  Also clears
+// `zero_words` 32-bit words at `zero` (the control block of a multi-kernel
+// call) when zero != nullptr.
 cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
                                bool bf16, uint64_t seed, uint32_t stream_id, uint64_t offset,
-                               cudaStream_t s, uint32_t* zero = nullptr, int zero_words = 0);
+                               cudaStream_t s, uint32_t* zero = nullptr, int zero_words = 0,
+                               int kind = 0);
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
                                cudaStream_t s);
 // sq[i] = scale * sum_{u < nunits, w < nw} part[(u * su + i * si) * nw + w]

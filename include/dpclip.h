@@ -75,6 +75,13 @@ enum dpclip_exact_method {
   DPCLIP_EXACT_DIRECT = 2   /* ||A_i^T G_i||_F^2, tile by tile, never stored */
 };
 
+/* Probe law of the randomized estimators.  Gaussian: i.i.d. N(0,1) ("Core
+ * mechanism", item 1).  Rademacher: i.i.d. {+1, -1}, the alternative sketch
+ * the summary names as future work; exact in bfloat16.  Element e of a
+ * Rademacher stream is -1 when the top bit of word e % 4 of its Philox block
+ * (the same counter as for the normals) is set, +1 otherwise. */
+enum dpclip_probe { DPCLIP_PROBE_GAUSSIAN = 0, DPCLIP_PROBE_RADEMACHER = 1 };
+
 enum dpclip_op {
   DPCLIP_OP_NORMS_EXACT = 0,
   DPCLIP_OP_NORMS_HUTCH = 1,
@@ -115,6 +122,16 @@ int dpclip_norms_hutch(const void* A, const void* G, int B, int T, int d, int p,
 int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int p, int dtype,
                          int k, uint64_t seed, uint64_t offset, float* sqnorms, void* ws,
                          size_t ws_bytes, dpclip_stream_t stream);
+
+/* dpclip_norms_hutch / dpclip_norms_hutchpp with a choice of probe law
+ * (dpclip_probe); the plain entry points use DPCLIP_PROBE_GAUSSIAN.  Same
+ * workspace sizes.  An unknown probe value returns DPCLIP_ERR_INVALID_ARG. */
+int dpclip_norms_hutch_ex(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                          int k, int probe, uint64_t seed, uint64_t offset, float* sqnorms,
+                          void* ws, size_t ws_bytes, dpclip_stream_t stream);
+int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                            int k, int probe, uint64_t seed, uint64_t offset, float* sqnorms,
+                            void* ws, size_t ws_bytes, dpclip_stream_t stream);
 
 /* Clipped noisy gradient ("DP-SGD algorithm" steps 3-4; "Algorithmic flow"
  * steps 4-5):
@@ -166,6 +183,11 @@ int dpclip_philox_normal(void* out, int64_t n, int dtype, uint64_t seed, uint32_
 int dpclip_norms_hutch_noalloc(const void* A, const void* G, int B, int T, int d, int p,
                                int dtype, int k, uint64_t seed, uint64_t offset, float* sqnorms,
                                dpclip_stream_t stream);
+
+/* The n Rademacher values of one Philox stream (see dpclip_probe), written as
+ * float or bfloat16 into `out` (device, 4-byte aligned). */
+int dpclip_philox_rademacher(void* out, int64_t n, int dtype, uint64_t seed, uint32_t stream_id,
+                             uint64_t offset, dpclip_stream_t stream);
 
 /* Synchronises `stream`, then returns DPCLIP_OK or the error the device
  * recorded in the workspace of the last call that used it

@@ -25,7 +25,7 @@ def declared_symbols():
 
 def test_every_declared_symbol_is_exported(L):
     names = declared_symbols()
-    assert len(names) >= 11
+    assert len(names) >= 15
     for n in names:
         assert hasattr(L.lib, n), n
         assert n in L.SIGNATURES, n
@@ -117,6 +117,12 @@ def test_entry_points_reject_before_any_launch(L):
     assert lib.dpclip_clip_scales(FAKE, 4, -1.0, FAKE, FAKE, None) == L.ERR_INVALID_ARG
     assert lib.dpclip_selftest_wait_timeout(FAKE, 256, 0, None) == L.ERR_INVALID_ARG
     assert lib.dpclip_workspace_status(None, None) == L.ERR_INVALID_ARG
+    # unknown probe law
+    assert lib.dpclip_norms_hutch_ex(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 8, 7, 1, 0, FAKE, FAKE, big,
+                                     None) == L.ERR_INVALID_ARG
+    assert lib.dpclip_norms_hutchpp_ex(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 9, -1, 1, 0, FAKE, FAKE,
+                                       big, None) == L.ERR_INVALID_ARG
+    assert lib.dpclip_philox_rademacher(None, 10, L.F32, 1, 0, 0, None) == L.ERR_INVALID_ARG
 
 
 def test_product_path_does_not_import_oracle():

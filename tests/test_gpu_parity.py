@@ -273,3 +273,31 @@ def test_grad_tail_split_over_k(api):
     Ms = list(O.per_sample_grads(inp.A, inp.G))
     q = np.array([np.sum(M * M) for M in Ms])
     check_grad(api, inp, A, G, q, float(np.sqrt(q).min()), 0.0, Ms)
+
+
+# ----------------------------------------------------------------------------- Rademacher probes
+
+def test_rademacher_fill_is_exact(api):
+    n = (1 << 18) + 5
+    for dt in (torch.float32, torch.bfloat16):
+        r = api.philox_rademacher(n, seed=4242, stream_id=0, offset=(1 << 35) + 9, dtype=dt)
+        ref = O.philox_rademacher(n, 4242, 0, (1 << 35) + 9)
+        assert np.array_equal(host(r), ref)
+
+
+@pytest.mark.parametrize("case", ["bf16", "f32"])
+def test_rademacher_estimators(api, case):
+    if case == "bf16":
+        wl = W.Workload(180, "rad_bf16", 3, 300, 200, 328, "bf16", 1e-2, 1.0, 1.0, 24, ())
+    else:
+        wl = W.get(1)
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    Ms = list(O.per_sample_grads(inp.A, inp.G))
+    P = O.hutch_probe(wl.p, wl.k, wl.seed, 2, wl.dtype, kind="rademacher")
+    S, Gp = O.hutchpp_probes(wl.p, wl.k, wl.seed, 2, wl.dtype, kind="rademacher")
+    tol = TOL[wl.dtype]
+    assert_rel(host(api.norms_hutch(A, G, wl.k, wl.seed, 2, probe="rademacher")),
+               O.sqnorms_hutch(None, None, P, Ms=Ms), tol, "hutch rademacher")
+    assert_rel(host(api.norms_hutchpp(A, G, wl.k, wl.seed, 2, probe="rademacher")),
+               O.sqnorms_hutchpp(None, None, S, Gp, Ms=Ms), tol, "hutch++ rademacher")
