@@ -131,9 +131,9 @@ cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t ro
   const int grid = (int)std::max<int64_t>(
       1, std::min<int64_t>((nblk + threads - 1) / threads, 152 * 16));
   if (bf16)
-    return launch_pdl(philox_fill_kernel<true>, dim3(grid), dim3(threads), 0, s, false, out, rows,
+    return launch_pdl(philox_fill_kernel<true>, dim3(grid), dim3(threads), 0, s, 0, out, rows,
                       cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
-  return launch_pdl(philox_fill_kernel<false>, dim3(grid), dim3(threads), 0, s, false, out, rows,
+  return launch_pdl(philox_fill_kernel<false>, dim3(grid), dim3(threads), 0, s, 0, out, rows,
                     cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
 }
 
@@ -141,13 +141,13 @@ cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, u
                                cudaStream_t s) {
   const int threads = 256;
   const int grid = std::min((B + threads - 1) / threads, 1024);
-  return launch_pdl(clip_scales_kernel, dim3(grid), dim3(threads), 0, s, false, sq, B, C, scales,
+  return launch_pdl(clip_scales_kernel, dim3(grid), dim3(threads), 0, s, 0, sq, B, C, scales,
                     clipped);
 }
 
 cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long long su, long long si,
                                   int nw, float scale, float* sq, cudaStream_t s) {
-  return launch_pdl(finalize_norms_kernel, dim3(B), dim3(256), 0, s, false, part, nunits, su, si,
+  return launch_pdl(finalize_norms_kernel, dim3(B), dim3(256), 0, s, 0, part, nunits, su, si,
                     nw, scale, sq);
 }
 
@@ -157,7 +157,7 @@ cudaError_t launch_noise_add(float* grad, long long n, float scale, uint64_t see
   const int threads = 256;
   const int grid = (int)std::min<long long>((nblk + threads - 1) / threads, 152 * 16);
   if (grid <= 0) return cudaSuccess;
-  return launch_pdl(noise_add_kernel, dim3(grid), dim3(threads), 0, s, false, grad, n, scale, seed,
+  return launch_pdl(noise_add_kernel, dim3(grid), dim3(threads), 0, s, 0, grad, n, scale, seed,
                     offset);
 }
 

@@ -128,7 +128,7 @@ struct Plan {
 enum {
   kP = 0, kYhi, kYlo, kPart, kPart2, kQpart,                 // hutch
   kS = 0, kGp, kY1hi, kY1lo, kZ1hi, kZ1lo, kUhi, kUlo,       // hutch++ ...
-  kV, kQWhi, kQWlo, kY3hi, kY3lo, kQ1, kHPart, kHQpart,
+  kV, kQWhi, kQWlo, kY3hi, kY3lo, kHPart, kHQpart,
 };
 
 int np_for(int n) { return n <= 16 ? 16 : 32; }
@@ -194,7 +194,6 @@ Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
   pl.off[kQWlo] = c.take((size_t)B * 32 * p * 2);
   pl.off[kY3hi] = c.take((size_t)B * 32 * pl.Tp * 2);
   pl.off[kY3lo] = c.take((size_t)B * 32 * pl.Tp * 2);
-  pl.off[kQ1] = c.take(hpp_qr_part_floats(B, p) * 4);
   pl.off[kHPart] = c.take(part);
   pl.off[kHQpart] = c.take((size_t)B * std::max(fd, fp) * 4);
   pl.total = c.total();
@@ -228,7 +227,7 @@ Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
 }
 
 // fp32 plans
-enum { kFP = 0, kFY, kFPart, kFS, kFGp, kFY1, kFZ1, kFU, kFV, kFQW, kFQ1, kFY3, kFW };
+enum { kFP = 0, kFY, kFPart, kFS, kFGp, kFY1, kFZ1, kFU, kFV, kFQW, kFY3, kFW };
 
 Plan plan_hutch_f32(int B, int T, int d, int p, int k) {
   Plan pl;
@@ -255,7 +254,6 @@ Plan plan_hutchpp_f32(int B, int T, int d, int p, int k) {
   pl.off[kFU] = c.take((size_t)B * T * r * 4);
   pl.off[kFV] = c.take((size_t)B * 16 * p * 4);
   pl.off[kFQW] = c.take((size_t)B * 32 * p * 4);
-  pl.off[kFQ1] = c.take(hpp_qr_part_floats(B, p) * 4);
   pl.off[kFY3] = c.take((size_t)B * T * (r + m) * 4);
   pl.off[kFPart] = c.take((size_t)B * simt_nblocks(d, r + m) * 4);
   pl.total = c.total();
@@ -660,7 +658,6 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
     hq.p = p;
     hq.r = r;
     hq.m = m;
-    hq.part = at<float>(ws, pl.off[kQ1]);
     hq.out_hi = static_cast<__nv_bfloat16*>(QWh);
     hq.out_lo = static_cast<__nv_bfloat16*>(QWl);
     hq.err = at<uint32_t>(ws, pl.ctrl);
@@ -722,7 +719,6 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
   hq.p = p;
   hq.r = r;
   hq.m = m;
-  hq.part = at<float>(ws, pl.off[kFQ1]);
   hq.out_f32 = QW;
   hq.err = at<uint32_t>(ws, pl.ctrl);
   DPCLIP_CUDA(launch_hpp_qr(hq, s));

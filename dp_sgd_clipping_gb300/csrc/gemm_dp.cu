@@ -493,12 +493,12 @@ cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cuda
     if ((e = cudaFuncSetAttribute(gemm_dp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes)) != cudaSuccess)
       return e;
-    return launch_pdl(gemm_dp_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, false, p);
+    return launch_pdl(gemm_dp_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, 0, p);
   }
   if ((e = cudaFuncSetAttribute(gemm_dp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kSmemBytes)) != cudaSuccess)
     return e;
-  return launch_pdl(gemm_dp_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, false, p);
+  return launch_pdl(gemm_dp_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, 0, p);
 }
 
 }  // namespace dpclip

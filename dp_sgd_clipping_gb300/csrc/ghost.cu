@@ -310,7 +310,7 @@ cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(ghost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(ghost_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, false, p);
+  return launch_pdl(ghost_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, 0, p);
 }
 
 }  // namespace dpclip

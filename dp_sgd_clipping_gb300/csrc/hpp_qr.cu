@@ -3,8 +3,8 @@
 //   V = O_i S (p x r, fp32, from the first two sweeps)
 //   Q = orthonormal basis of range(V)        -- CholeskyQR2 with column drop
 //   W = G' - Q (Q^T G')                      -- tail probes projected off Q
-//   out = [Q | 0 | W | 0] padded to 32 columns ([B][32][p], hi/lo bf16 for
-//         the tensor-core sweep, or fp32)
+//   out = [Q | W | 0] padded to 32 columns ([B][32][p], hi/lo bf16 for the
+//         tensor-core sweep, or fp32)
 // The estimate depends on Q only through span(Q) (the head is trace(Q^T O Q)
 // and the tail uses I - Q Q^T), so any orthonormal basis of the same span
 // gives the same result as a Householder QR.
@@ -19,14 +19,27 @@
 // Gram has condition number below ~1e5, within fp32 Cholesky's reach, and the
 // second pass restores orthogonality to fp32 level.
 //
-// Parallel layout: a cooperative grid of B x ceil(p / 512) CTAs; each CTA
-// keeps its 512 rows of V (then Q) and G' in shared memory for the whole
-// kernel.  Two p-long reductions: V^T V, then Q1^T Q1 together with
-// Q1^T G' (Q^T G' = R2^-T Q1^T G' needs no third pass).  Each writes one
-// partial per CTA; after a grid-wide barrier every CTA of the sample adds the
-// partials of its sample in the same fixed order, so all of them hold the
-// same bits and factorise identically (one thread, the r x r factor fully in
-// registers; rows apply R^-1 by forward substitution).
+// Parallel layout: one thread-block cluster per sample (up to 16 CTAs where
+// the device allows clusters that large, else 8; fewer for short p).  CTA j
+// of the cluster owns a contiguous range of rows of V and G', staged in its
+// shared memory column by column ([x (r) | g (m)] columns, rows contiguous)
+// by 16-byte asynchronous copies (one round trip to L2).  The two p-long
+// reductions, V^T V and then Q1^T [Q1 | G'] (which also gives
+// Q^T G' = R2^-T Q1^T G' without a third pass), run as register-blocked
+// 4 x 4 outer products per thread; each CTA publishes its partial in its own
+// shared memory and, after a cluster barrier, every CTA reads the partials
+// of all ranks through distributed shared memory and adds them in rank
+// order.  All CTAs of the sample thus hold the same bits and factorise
+// identically.  R^-1 is then formed once as a small matrix M (the forward
+// substitution applied to unit rows), and rows are transformed as x M.  No
+// global scratch, no grid-wide barrier.
+//
+// Latency, not arithmetic, sets this kernel's time: every phase runs once
+// per CTA, so the first fetch of each phase's instructions is on the
+// critical path.  The factorisation is a short rolled loop; the unrolled
+// inverse is one (non-inlined) function that a spare warp runs once on
+// scratch while the first tile's copies are in flight; every function has a
+// single call site.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -39,305 +52,438 @@ namespace {
 namespace cg = cooperative_groups;
 
 constexpr int kThreads = 256;
-constexpr int kRows = 512;           // rows of p per CTA
+constexpr int kTileRows = 512;       // rows resident per CTA (more: tiles re-staged)
+constexpr int kRowsTarget = 512;     // rows per CTA the cluster size aims at
+constexpr int kLdc = kTileRows + 4;  // floats per staged column (16-byte aligned)
+constexpr int kCols = 32;            // staged columns: [x (r) | g (m)], r + m <= 32
 constexpr int kMaxR = 16;            // r = floor(k/3) <= 16 for k <= 48
 constexpr int kMaxM = 18;            // m = k - 2r <= 18 for k <= 48
-constexpr int kSym = kMaxR * (kMaxR + 1) / 2;     // 136 upper-triangle entries
-constexpr int kPartStride = 512;     // floats per CTA partial
-static_assert(kSym + kMaxR * kMaxM <= kPartStride, "partials of pass 2 must fit");
+constexpr int kPub = kMaxR * kMaxNP; // one CTA's partial: r x (r + m) <= 16 x 32
 constexpr float kDropTol = 1e-5f;
 
 struct Smem {
-  float x[kMaxR][kRows + 1];       // rows of V, then Q1, then Q
-  float g[kMaxM][kRows + 1];       // rows of G'
-  float S[kPartStride];            // summed partials of the current pass
-  float H[kMaxR][kMaxR + 1];       // Gram matrix of the current pass
+  float xs[kCols][kLdc];           // staged columns: V (then Q1, then Q) | G'
+  __nv_bfloat16 gtmp[kMaxM][kTileRows];   // bf16 G' as copied, before widening
+  float red[kThreads * 16];        // per-thread 4 x 4 partial blocks
+  float pub[2][kPub];              // this CTA's partials of pass 1 and 2 (read by the cluster)
+  float sum[kPub];                 // cluster sum of the current pass
   float K[kMaxR][kMaxM];           // Q1^T G'
-  float Cm[kMaxR][kMaxM];          // Q^T G' = R2^-T K (zero rows for dropped columns)
-  float R[kMaxR][kMaxR + 1];       // Cholesky factor (zero rows for dropped columns)
-  float rdiag[kMaxR];              // 1 / R[k][k], or 0 for a dropped column
+  float CmT[kMaxM][kMaxR];         // (Q^T G')^T = (R2^-T K)^T, zero for columns >= r
+  float R1[kMaxR][kMaxR + 1];      // Gram, then its Cholesky factor (upper triangle)
+  float R2[kMaxR][kMaxR + 1];
+  float rd1[kMaxR];                // 1 / R[k][k], or 0 for a dropped column
+  float rd2[kMaxR];
+  float M1[kMaxR][kMaxR];          // R^-1 as the forward substitution applies it
+  float M2[kMaxR][kMaxR];          // (zero outside the leading r x r block)
 };
 
-__device__ __forceinline__ void sym_entry(int e, int n, int& a, int& b) {
-  int rem = e, row = 0, len = n;
-  while (rem >= len) {
-    rem -= len;
-    ++row;
-    --len;
-  }
-  a = row;
-  b = row + rem;
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
 }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// This CTA's part of X^T Y over its rows, for a < na, b < nb (upper triangle
-// when sym), written to part[e].
-__device__ void partial_cross(const float (*X)[kRows + 1], int na, const float (*Y)[kRows + 1],
-                              int nb, bool sym, float* part) {
-  const int ne = sym ? na * (na + 1) / 2 : na * nb;
-  for (int e = threadIdx.x; e < ne; e += kThreads) {
-    int a, b;
-    if (sym) {
-      sym_entry(e, na, a, b);
-    } else {
-      a = e / nb;
-      b = e % nb;
-    }
-    const float* xa = X[a];
-    const float* yb = Y[b];
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    for (int c = 0; c < kRows; c += 4) {
-      s0 = fmaf(xa[c], yb[c], s0);
-      s1 = fmaf(xa[c + 1], yb[c + 1], s1);
-      s2 = fmaf(xa[c + 2], yb[c + 2], s2);
-      s3 = fmaf(xa[c + 3], yb[c + 3], s3);
-    }
-    part[e] = (s0 + s1) + (s2 + s3);
+// Copies n consecutive fp32 values to shared memory: 16-byte copies when both
+// ends allow it (vec), else 4-byte ones.
+__device__ __forceinline__ void copy_f32(float* dst, const float* src, int n, bool vec) {
+  if (vec) {
+    for (int q = threadIdx.x; q < n / 4; q += kThreads) cp_async16(dst + 4 * q, src + 4 * q);
+  } else {
+    for (int c = threadIdx.x; c < n; c += kThreads) cp_async4(dst + c, src + c);
   }
 }
 
-// sm.S[e] = sum of the per-CTA partials of this sample (chunk order), e < ne.
-__device__ void sum_partials(Smem& sm, const float* parts, int cps, int ne) {
-  for (int e = threadIdx.x; e < ne; e += kThreads) {
+// Warp 0, lane a < 16: row a of M = R^-1 as the forward substitution
+// q[b] = (x[b] - sum_{a<b} q[a] R[a][b]) rdiag[b] applies it to a unit row:
+// x M is that substitution for any row x (it is linear in x), and a dropped
+// column b (rdiag[b] = 0) is a zero column of M.  Entries outside the
+// leading r x r block are zero.  Not inlined: the two factorisations and
+// the instruction-cache warm-up below run the same code.
+__device__ __noinline__ void invert_factor(const float (*R)[kMaxR + 1], const float* rdiag,
+                                              int r, float (*M)[kMaxR]) {
+  const int a = threadIdx.x & 31;
+  if (a >= kMaxR) return;
+  float q[kMaxR];
+#pragma unroll
+  for (int b = 0; b < kMaxR; ++b) {
+    float s = (a == b && b < r) ? 1.f : 0.f;
+#pragma unroll
+    for (int c = 0; c < b; ++c) s = fmaf(-q[c], R[c][b], s);
+    q[b] = b < r ? s * rdiag[b] : 0.f;
+  }
+#pragma unroll
+  for (int b = 0; b < kMaxR; ++b) M[a][b] = a < r ? q[b] : 0.f;
+}
+
+// Stages rows [base, base + nvalid) of V (columns < r) and G' (m columns) as
+// xs[col][c], col < r + m; rows nvalid .. (nvalid rounded up to 4) are zero,
+// nothing else past nvalid is read later.  Asynchronous copies throughout
+// (bf16 G' as 8-element chunks, widened after they land), so the tile costs
+// one round trip.  Ends with a CTA barrier.
+__device__ __forceinline__ void stage_tile(Smem& sm, const HppQrParams& p, int i, int base, int nvalid,
+                                           bool warm) {
+  const int r = p.r, m = p.m;
+  const bool vec = (p.p % 4) == 0;   // then base, nvalid and every column start are 16-byte aligned
+  for (int col = 0; col < r; ++col)
+    copy_f32(sm.xs[col], p.V + ((size_t)i * p.ldv + col) * p.p + base, nvalid, vec);
+  if (warm && threadIdx.x >= 32 && threadIdx.x < 64) {
+    // While the copies are in flight, warp 1 runs the (unrolled, once-per-
+    // pass) inverse on the second factor's scratch, which pass 1 overwrites:
+    // that fetches its code into the instruction cache before the first real
+    // use, where the fetch would otherwise sit on the critical path.
+    invert_factor(sm.R2, sm.rd2, r, sm.M2);
+  }
+  if (p.gp_bf16) {
+    // p % 8 == 0 on this path: base and nvalid are multiples of 8
+    for (int l = 0; l < m; ++l) {
+      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.Gp) + (size_t)l * p.p + base;
+      for (int q = threadIdx.x; q < nvalid / 8; q += kThreads)
+        cp_async16(&sm.gtmp[l][8 * q], src + 8 * q);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    for (int l = 0; l < m; ++l)
+      for (int c = threadIdx.x; c < nvalid; c += kThreads)
+        sm.xs[r + l][c] = __bfloat162float(sm.gtmp[l][c]);
+  } else {
+    for (int l = 0; l < m; ++l)
+      copy_f32(sm.xs[r + l], static_cast<const float*>(p.Gp) + (size_t)l * p.p + base, nvalid, vec);
+    cp_async_wait_all();
+  }
+  const int pad = ((nvalid + 3) & ~3) - nvalid;
+  for (int e = threadIdx.x; e < pad * (r + m); e += kThreads) sm.xs[e / pad][nvalid + e % pad] = 0.f;
+  __syncthreads();
+}
+
+// Geometry of the register-blocked product C = X^T Y, X = columns [0, na),
+// Y = columns [0, nb) of the staged tile: 4 x 4 output blocks, and the
+// threads left over split the rows, in groups of 4, into `slices`
+// interleaved slices.
+struct Blocking {
+  int nbb, nblk, slices;
+  __device__ Blocking(int na, int nb) {
+    nbb = (nb + 3) / 4;
+    nblk = ((na + 3) / 4) * nbb;
+    slices = kThreads / nblk;
+  }
+};
+
+// acc += this thread's share of X^T Y over staged rows [0, nrows): block
+// (a0.., b0..) over the row groups 4 (s + k slices) .. + 3.
+__device__ __forceinline__ void accumulate(const Smem& sm, const Blocking& bk, int nrows,
+                                           float (&acc)[4][4]) {
+  const int blk = (int)threadIdx.x % bk.nblk, s = (int)threadIdx.x / bk.nblk;
+  if (s >= bk.slices) return;
+  const int a0 = (blk / bk.nbb) * 4, b0 = (blk % bk.nbb) * 4;
+  const int ngroups = (nrows + 3) / 4;
+#pragma unroll 2
+  for (int g = s; g < ngroups; g += bk.slices) {
+    float4 x[4], y[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = *reinterpret_cast<const float4*>(&sm.xs[a0 + u][4 * g]);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) y[w] = *reinterpret_cast<const float4*>(&sm.xs[b0 + w][4 * g]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        float a = acc[u][w];
+        a = fmaf(x[u].x, y[w].x, a);
+        a = fmaf(x[u].y, y[w].y, a);
+        a = fmaf(x[u].z, y[w].z, a);
+        a = fmaf(x[u].w, y[w].w, a);
+        acc[u][w] = a;
+      }
+  }
+}
+
+// sm.pub[pass][a * nb + b] = this CTA's sum of X^T Y, the slices added in
+// slice order (deterministic).
+__device__ __forceinline__ void stash_acc(Smem& sm, const float (&acc)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) sm.red[threadIdx.x * 16 + u * 4 + w] = acc[u][w];
+  __syncthreads();
+}
+__device__ __forceinline__ void publish(Smem& sm, int nbb, int nblk, int slices, int pass, int na,
+                                     int nb) {
+  for (int e = threadIdx.x; e < na * nb; e += kThreads) {
+    const int a = e / nb, b = e % nb;
+    const int blk = (a / 4) * nbb + b / 4, q = (a % 4) * 4 + b % 4;
     float s = 0.f;
-    for (int q0 = 0; q0 < cps; q0 += 8) {   // 8 loads in flight, added in chunk order
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = q0 + u < cps ? __ldcg(parts + (size_t)(q0 + u) * kPartStride + e) : 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) s += v[u];
-    }
-    sm.S[e] = s;
+    for (int sl = 0; sl < slices; ++sl) s += sm.red[(sl * nblk + blk) * 16 + q];
+    sm.pub[pass][e] = s;
   }
 }
 
-// sm.H (n x n) from the upper-triangle sums in sm.S[0 .. n(n+1)/2).
-__device__ void expand_sym(Smem& sm, int n) {
-  for (int e = threadIdx.x; e < n * (n + 1) / 2; e += kThreads) {
-    int a, b;
-    sym_entry(e, n, a, b);
-    sm.H[a][b] = sm.S[e];
-    sm.H[b][a] = sm.S[e];
+// sm.sum[e] = sum over the cluster's ranks, in rank order, of pub[pass][e].
+__device__ __forceinline__ void cluster_sum(Smem& sm, cg::cluster_group& cluster, int pass, int ne, int cs) {
+  cluster.sync();   // every rank has published
+  for (int e = threadIdx.x; e < ne; e += kThreads) {
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      v[q] = q < cs ? cluster.map_shared_rank(&sm.pub[pass][0], q)[e] : 0.f;
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) s += v[q];
+    sm.sum[e] = s;
   }
+  __syncthreads();
 }
 
-// One thread: Cholesky H = R^T R of the n x n Gram in sm.H, fully unrolled in
-// registers.  A pivot below kDropTol times the largest diagonal entry marks
-// its column as dependent on the earlier ones: its row of R and its entry of
-// rdiag (= 1 / R[k][k]) are zero, so the matching column of Q comes out zero
-// and drops out of both the head and the tail projection.
-__device__ void serial_cholesky(Smem& sm, int n) {
-  float a[kMaxR][kMaxR];
-#pragma unroll
-  for (int i = 0; i < kMaxR; ++i)
-#pragma unroll
-    for (int j = i; j < kMaxR; ++j) a[i][j] = (i < n && j < n) ? sm.H[i][j] : 0.f;
+// Warp 0: Cholesky A = R^T R in place on the n x n Gram in A (upper
+// triangle read, R written over it), lane j owning column j.  A pivot below
+// kDropTol times the largest diagonal entry marks its column as dependent on
+// the earlier ones: its row of R and its entry of rdiag (= 1 / R[k][k]) are
+// zero, so the matching column of Q comes out zero and drops out of both the
+// head and the tail projection.  1 / R[k][k] is the hardware reciprocal
+// square root (within 2 ulp); the second CholeskyQR pass absorbs that.
+// Short rolled loops: this runs once per CTA, where the fetch of unrolled
+// straight-line code would cost more than the arithmetic.
+__device__ __forceinline__ void cholesky(float (*A)[kMaxR + 1], int n, float* rdiag) {
+  const int j = threadIdx.x & 31;
   float dmax = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxR; ++i) dmax = fmaxf(dmax, a[i][i]);
+  for (int a = 0; a < n; ++a) dmax = fmaxf(dmax, A[a][a]);
   const float tol = kDropTol * dmax;
-#pragma unroll
-  for (int k = 0; k < kMaxR; ++k) {
-    const bool keep = k < n && a[k][k] > tol && dmax > 0.f;
-    const float rkk = keep ? sqrtf(a[k][k]) : 0.f;
-    const float inv = keep ? 1.f / rkk : 0.f;
-    sm.rdiag[k] = inv;
-    a[k][k] = rkk;
-#pragma unroll
-    for (int j = k + 1; j < kMaxR; ++j) a[k][j] *= inv;
-#pragma unroll
-    for (int i = k + 1; i < kMaxR; ++i)
-#pragma unroll
-      for (int j = i; j < kMaxR; ++j) a[i][j] = fmaf(-a[k][i], a[k][j], a[i][j]);
+  for (int k = 0; k < n; ++k) {
+    const float piv = A[k][k];
+    const bool keep = piv > tol && dmax > 0.f;
+    const float inv = keep ? rsqrtf(piv) : 0.f;
+    __syncwarp();
+    if (j == k) {
+      A[k][k] = piv * inv;
+      rdiag[k] = inv;
+    } else if (j > k && j < n) {
+      A[k][j] *= inv;
+    }
+    __syncwarp();
+    if (j > k && j < n) {
+      const float rkj = A[k][j];
+      for (int i2 = k + 1; i2 <= j; ++i2) A[i2][j] = fmaf(-A[k][i2], rkj, A[i2][j]);
+    }
+    __syncwarp();
   }
-#pragma unroll
-  for (int i = 0; i < kMaxR; ++i)
-#pragma unroll
-    for (int j = 0; j < kMaxR; ++j) sm.R[i][j] = j >= i ? a[i][j] : 0.f;
 }
 
-// In place on the shared rows: x[c, :] <- x[c, :] R^-1 by forward
-// substitution, q[b] = (x[b] - sum_{a<b} q[a] R[a][b]) / R[b][b] (zero for a
-// dropped column).  Thread t owns rows t, t + 256.
-__device__ void apply_rinv(Smem& sm, int n) {
-  for (int c = threadIdx.x; c < kRows; c += kThreads) {
+// In place on the staged rows [0, nrows): x[c, :] <- x[c, :] M over the first
+// r columns.  One thread per row.
+__device__ __forceinline__ void apply_matrix(Smem& sm, const float (*M)[kMaxR], int r, int nrows) {
+  for (int c = threadIdx.x; c < nrows; c += kThreads) {
     float q[kMaxR];
 #pragma unroll
-    for (int b = 0; b < kMaxR; ++b) {
-      float s = b < n ? sm.x[b][c] : 0.f;
+    for (int b = 0; b < kMaxR; ++b) q[b] = 0.f;
+    for (int a = 0; a < r; ++a) {
+      const float xa = sm.xs[a][c];
 #pragma unroll
-      for (int a = 0; a < b; ++a) s = fmaf(-q[a], sm.R[a][b], s);
-      q[b] = s * sm.rdiag[b];
+      for (int b4 = 0; b4 < kMaxR; b4 += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(&M[a][b4]);
+        q[b4] = fmaf(xa, m4.x, q[b4]);
+        q[b4 + 1] = fmaf(xa, m4.y, q[b4 + 1]);
+        q[b4 + 2] = fmaf(xa, m4.z, q[b4 + 2]);
+        q[b4 + 3] = fmaf(xa, m4.w, q[b4 + 3]);
+      }
     }
 #pragma unroll
-    for (int b = 0; b < kMaxR; ++b) sm.x[b][c] = q[b];
+    for (int b = 0; b < kMaxR; ++b)
+      if (b < r) sm.xs[b][c] = q[b];
   }
 }
 
-__global__ void __launch_bounds__(kThreads) hpp_qr_kernel(const __grid_constant__ HppQrParams p) {
+// In place on the staged rows [0, nrows), after Q: g columns <- W = G' - Q
+// (Q^T G').  One thread per row, its Q row in registers.
+__device__ __forceinline__ void tail_rows(Smem& sm, int r, int m, int nrows) {
+  for (int c = threadIdx.x; c < nrows; c += kThreads) {
+    float q[kMaxR];
+#pragma unroll
+    for (int a = 0; a < kMaxR; ++a) q[a] = a < r ? sm.xs[a][c] : 0.f;
+    for (int l = 0; l < m; ++l) {
+      const float* cm = sm.CmT[l];
+      float s0 = sm.xs[r + l][c], s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int a = 0; a < kMaxR; a += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(cm + a);
+        s0 = fmaf(-q[a], v.x, s0);
+        s1 = fmaf(-q[a + 1], v.y, s1);
+        s2 = fmaf(-q[a + 2], v.z, s2);
+        s3 = fmaf(-q[a + 3], v.w, s3);
+      }
+      sm.xs[r + l][c] = (s0 + s1) + (s2 + s3);
+    }
+  }
+}
+
+// Output rows [0, nrows) of the tile at global row `base`: [Q | W | 0] from
+// the staged columns.  Items of 8 consecutive rows x one column; 16-byte
+// stores when the row range allows them.
+__device__ __forceinline__ void write_rows(const Smem& sm, const HppQrParams& p, int i, int base,
+                                           int nrows) {
+  const int nc = p.r + p.m;
+  const int groups = (nrows + 7) / 8;
+  const bool vec = (p.p % 8) == 0;   // then base and every column start are 16-byte aligned (bf16)
+  for (int e = threadIdx.x; e < kMaxNP * groups; e += kThreads) {
+    const int j = e / groups, c0 = (e % groups) * 8;
+    float v[8];
+    if (j < nc) {
+      const float4 x0 = *reinterpret_cast<const float4*>(&sm.xs[j][c0]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&sm.xs[j][c0 + 4]);
+      v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+      v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = 0.f;
+    }
+    const size_t o = ((size_t)i * kMaxNP + j) * p.p + base + c0;
+    if (p.out_f32) {
+      for (int u = 0; u < 8 && c0 + u < nrows; ++u) p.out_f32[o + u] = v[u];
+    } else if (vec && c0 + 8 <= nrows) {
+      __align__(16) __nv_bfloat16 hi[8], lo[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) split_hilo(v[u], hi[u], lo[u]);
+      *reinterpret_cast<uint4*>(p.out_hi + o) = *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(p.out_lo + o) = *reinterpret_cast<const uint4*>(lo);
+    } else {
+      for (int u = 0; u < 8 && c0 + u < nrows; ++u) {
+        __nv_bfloat16 hi, lo;
+        split_hilo(v[u], hi, lo);
+        p.out_hi[o + u] = hi;
+        p.out_lo[o + u] = lo;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void zero_acc(float (&acc)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) acc[u][w] = 0.f;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_constant__ HppQrParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  cg::grid_group grid = cg::this_grid();
+  cg::cluster_group cluster = cg::this_cluster();
   pdl_trigger();
   pdl_wait();
-  const int cps = p.cps;
-  const int i = p.sample0 + (int)blockIdx.x / cps;
-  const int chunk = (int)blockIdx.x % cps;
-  const int c0 = chunk * kRows;
+  const int cs = p.cs;
+  const int i = (int)blockIdx.x / cs;               // one cluster per sample
+  const int rank = (int)cluster.block_rank();
   const int r = p.r, m = p.m;
-  const bool active = i < p.B;   // grids are whole samples; guard anyway
-  const int ia = active ? i : 0;
-  float* part1 = p.part + ((size_t)0 * p.B + ia) * cps * kPartStride;
-  float* part2 = p.part + ((size_t)1 * p.B + ia) * cps * kPartStride;
+  const int per = (((p.p + cs - 1) / cs) + 7) / 8 * 8;
+  const int row0 = min(p.p, rank * per);
+  const int row_end = min(p.p, row0 + per);
+  const int nt = max(1, (row_end - row0 + kTileRows - 1) / kTileRows);
+  const bool resident = nt == 1;
 
-  // ---- stage this CTA's rows of V (r columns) and G' (m columns); the loads
-  // of 16 consecutive elements per thread are issued before any is stored
-  constexpr int kBatch = 16;
-  for (int it0 = 0; it0 < kMaxR * kRows; it0 += kBatch * kThreads) {
-    float v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int idx = it0 + u * kThreads + threadIdx.x;
-      const int a = idx / kRows, c = idx % kRows;
-      v[u] = (active && a < r && c0 + c < p.p) ? p.V[((size_t)i * p.ldv + a) * p.p + c0 + c] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int idx = it0 + u * kThreads + threadIdx.x;
-      sm.x[idx / kRows][idx % kRows] = v[u];
-    }
-  }
-  for (int it0 = 0; it0 < kMaxM * kRows; it0 += kBatch * kThreads) {
-    float v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int idx = it0 + u * kThreads + threadIdx.x;
-      const int l = idx / kRows, c = idx % kRows;
-      float x = 0.f;
-      if (idx < kMaxM * kRows && active && l < m && c0 + c < p.p) {
-        const size_t o = (size_t)l * p.p + c0 + c;
-        x = p.gp_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.Gp)[o])
-                      : static_cast<const float*>(p.Gp)[o];
+  // pass 0: Gram V^T V -> R1.  pass 1: Q1 = V R1^-1, one reduction for both
+  // Q1^T Q1 (close to the identity) -> R2 and K = Q1^T G'; then Q = Q1 R2^-1
+  // and Q^T G' = R2^-T K.  pass 2: outputs [Q | W | 0].  A resident tile is
+  // staged once and transformed in place; otherwise every pass re-stages
+  // each tile and re-applies the factors it needs.
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int nb = pass == 0 ? r : r + m;
+    const Blocking bk(r, nb);
+    float acc[4][4];
+    zero_acc(acc);
+#pragma unroll 1
+    for (int t = 0; t < nt; ++t) {
+      const int base = row0 + t * kTileRows;
+      const int nv = max(0, min(kTileRows, row_end - base));
+      if (pass == 0 || !resident) stage_tile(sm, p, i, base, nv, pass == 0 && t == 0);
+      const int first = (pass == 0 || (resident && pass == 2)) ? 2 : 1;
+      const int last = pass == 2 ? 2 : pass;   // factors applied: M1 (1), M2 (2)
+#pragma unroll 1
+      for (int f = first; f <= last; ++f) {
+        apply_matrix(sm, f == 1 ? sm.M1 : sm.M2, r, nv);
+        __syncthreads();
       }
-      v[u] = x;
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int idx = it0 + u * kThreads + threadIdx.x;
-      if (idx < kMaxM * kRows) sm.g[idx / kRows][idx % kRows] = v[u];
-    }
-  }
-  __syncthreads();
-
-  // ---- pass 1: Cholesky of V^T V; Q1 = V R1^-1
-  const int ne = r * (r + 1) / 2;
-  if (active) partial_cross(sm.x, r, sm.x, r, true, part1 + (size_t)chunk * kPartStride);
-  __threadfence();
-  grid.sync();
-  if (active) sum_partials(sm, part1, cps, ne);
-  __syncthreads();
-  expand_sym(sm, r);
-  __syncthreads();
-  if (threadIdx.x == 0) serial_cholesky(sm, r);
-  __syncthreads();
-  apply_rinv(sm, r);
-  __syncthreads();
-
-  // ---- pass 2, one reduction for both: Q1^T Q1 (close to the identity) and
-  // K = Q1^T G'.  Then Q = Q1 R2^-1 and Q^T G' = R2^-T K.
-  if (active) {
-    float* mine = part2 + (size_t)chunk * kPartStride;
-    partial_cross(sm.x, r, sm.x, r, true, mine);
-    partial_cross(sm.x, r, sm.g, m, false, mine + ne);
-  }
-  __threadfence();
-  grid.sync();
-  if (active) sum_partials(sm, part2, cps, ne + r * m);
-  __syncthreads();
-  expand_sym(sm, r);
-  for (int e = threadIdx.x; e < r * m; e += kThreads) sm.K[e / m][e % m] = sm.S[ne + e];
-  __syncthreads();
-  if (threadIdx.x == 0) serial_cholesky(sm, r);
-  __syncthreads();
-  // C = R2^-T K by forward substitution, one tail column per thread
-  if (threadIdx.x < m) {
-    const int l = threadIdx.x;
-    float cc[kMaxR];
-#pragma unroll
-    for (int b = 0; b < kMaxR; ++b) {
-      float s = b < r ? sm.K[b][l] : 0.f;
-#pragma unroll
-      for (int a = 0; a < b; ++a) s = fmaf(-sm.R[a][b], cc[a], s);
-      cc[b] = s * sm.rdiag[b];
-      sm.Cm[b][l] = cc[b];
-    }
-  }
-  apply_rinv(sm, r);
-  __syncthreads();
-  if (!active) return;
-
-  // ---- outputs [Q | W | 0], W = G' - Q (Q^T G'); each thread owns rows
-  for (int c = threadIdx.x; c < kRows; c += kThreads) {
-    if (c0 + c >= p.p) break;
-    float qrow[kMaxR];
-#pragma unroll
-    for (int a = 0; a < kMaxR; ++a) qrow[a] = sm.x[a][c];
-#pragma unroll
-    for (int j = 0; j < kMaxNP; ++j) {
-      float val = 0.f;
-      if (j < kMaxR && j < r) {
-        val = qrow[j < kMaxR ? j : 0];
-      } else if (j >= r && j < r + m) {
-        const int l = j - r;
-        float s = sm.g[l][c];
-#pragma unroll
-        for (int a = 0; a < kMaxR; ++a) s = fmaf(-qrow[a], sm.Cm[a][l], s);
-        val = s;
-      }
-      const size_t o = ((size_t)i * kMaxNP + j) * p.p + c0 + c;
-      if (p.out_f32) {
-        p.out_f32[o] = val;
+      if (pass < 2) {
+        accumulate(sm, bk, nv, acc);
       } else {
-        __nv_bfloat16 hi, lo;
-        split_hilo(val, hi, lo);
-        p.out_hi[o] = hi;
-        p.out_lo[o] = lo;
+        tail_rows(sm, r, m, nv);
+        __syncthreads();
+        write_rows(sm, p, i, base, nv);
       }
+      if (!resident) __syncthreads();
+    }
+    if (pass == 2) break;
+    stash_acc(sm, acc);
+    publish(sm, bk.nbb, bk.nblk, bk.slices, pass, r, nb);
+    cluster_sum(sm, cluster, pass, r * nb, cs);
+    float (*R)[kMaxR + 1] = pass == 0 ? sm.R1 : sm.R2;
+    for (int e = threadIdx.x; e < r * nb; e += kThreads) {
+      const int a = e / nb, b = e % nb;
+      if (b < r) R[a][b] = sm.sum[e];
+      else sm.K[a][b - r] = sm.sum[e];
+    }
+    __syncthreads();
+    float* rd = pass == 0 ? sm.rd1 : sm.rd2;
+    if (threadIdx.x < 32) cholesky(R, r, rd);
+    __syncthreads();
+    if (threadIdx.x < 32) invert_factor(R, rd, r, pass == 0 ? sm.M1 : sm.M2);
+    __syncthreads();
+    if (pass == 1) {
+      // Cm = R2^-T K = M2^T K, stored transposed; one entry per thread
+      for (int e = threadIdx.x; e < kMaxM * kMaxR; e += kThreads) {
+        const int l = e / kMaxR, b = e % kMaxR;
+        float s2 = 0.f;
+        if (l < m)
+          for (int a = 0; a <= b && a < r; ++a) s2 = fmaf(sm.M2[a][b], sm.K[a][l], s2);
+        sm.CmT[l][b] = s2;
+      }
+      __syncthreads();
     }
   }
+  // the other ranks may still be reading this CTA's partials
+  cluster.sync();
+}
+
+// Largest cluster this kernel can be launched with on the current device:
+// 16 CTAs (a non-portable size) where the device has room for one, else 8.
+int cluster_cap(size_t smem) {
+  static int cap = 0;
+  if (cap) return cap;
+  int c = 8;
+  if (cudaFuncSetAttribute(hpp_qr_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 16;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, hpp_qr_kernel, &cfg) == cudaSuccess && n > 0) c = 16;
+  }
+  (void)cudaGetLastError();
+  cap = c;
+  return cap;
 }
 
 }  // namespace
 
-size_t hpp_qr_part_floats(int B, int p) {
-  return (size_t)2 * B * ((p + kRows - 1) / kRows) * kPartStride;
-}
-
 cudaError_t launch_hpp_qr(const HppQrParams& p_in, cudaStream_t s) {
-  if (p_in.r > kMaxR || p_in.m > kMaxM || p_in.r + p_in.m > kMaxNP) return cudaErrorInvalidValue;
+  if (p_in.r < 1 || p_in.r > kMaxR || p_in.m > kMaxM || p_in.r + p_in.m > kMaxNP)
+    return cudaErrorInvalidValue;
   const size_t smem = sizeof(Smem);
   cudaError_t e =
       cudaFuncSetAttribute(hpp_qr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, nsm = 0, per_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hpp_qr_kernel, kThreads, smem)) !=
-      cudaSuccess)
-    return e;
   HppQrParams p = p_in;
-  p.cps = (p.p + kRows - 1) / kRows;
-  const int resident = std::max(1, per_sm * nsm);
-  if (p.cps > resident) return cudaErrorCooperativeLaunchTooLarge;
-  // whole samples per cooperative launch, as many as stay co-resident
-  const int per_launch = std::max(1, resident / p.cps);
-  for (int s0 = 0; s0 < p.B; s0 += per_launch) {
-    p.sample0 = s0;
-    const int nb = std::min(per_launch, p.B - s0);
-    e = launch_pdl(hpp_qr_kernel, dim3(nb * p.cps), dim3(kThreads), smem, s, true, p);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  p.cs = std::min(cluster_cap(smem), std::max(1, (p.p + kRowsTarget - 1) / kRowsTarget));
+  return launch_pdl(hpp_qr_kernel, dim3(p.B * p.cs), dim3(kThreads), smem, s, p.cs, p);
 }
 
 }  // namespace dpclip

@@ -16,10 +16,11 @@ namespace dpclip {
 
 // Launches `kernel` with programmatic stream serialisation, so that its
 // prologue overlaps the tail of the previous kernel in the stream (the kernel
-// itself waits for that kernel before touching global memory).
+// itself waits for that kernel before touching global memory).  cluster_x > 0
+// groups consecutive CTAs along x into thread-block clusters of that size.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t s, bool cooperative, Args&&... args) {
+                       cudaStream_t s, int cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -28,10 +29,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)(cluster_x > 0 ? cluster_x : 1);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = cooperative ? 2 : 1;
+  cfg.numAttrs = cluster_x > 0 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -137,8 +140,7 @@ struct HppQrParams {
   const void* Gp;        // [m][p], bf16 or fp32 (gp_bf16)
   int gp_bf16;
   int B, p, r, m;
-  float* part;           // hpp_qr_part_floats(B, p) fp32 scratch
-  int cps, sample0;      // set by the launcher: CTAs per sample, first sample
+  int cs;                // set by the launcher: CTAs (one cluster) per sample
   __nv_bfloat16* out_hi; // bf16 output (when out_f32 == nullptr)
   __nv_bfloat16* out_lo;
   float* out_f32;        // fp32 output [B][32][p]
@@ -177,7 +179,6 @@ cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s);
 cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cudaStream_t s);
 cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s);
 cudaError_t launch_hpp_qr(const HppQrParams& p, cudaStream_t s);
-size_t hpp_qr_part_floats(int B, int p);
 cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblocks_out);
 int simt_nblocks(int M, int N);
 

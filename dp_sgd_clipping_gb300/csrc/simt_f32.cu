@@ -120,7 +120,7 @@ cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblo
   const dim3 grid((p.N + kTile - 1) / kTile, (p.M + kTile - 1) / kTile,
                   mode == kSimtGrad ? 1 : p.batch);
   if (nblocks_out) *nblocks_out = (int)(grid.x * grid.y);
-  return launch_pdl(simt_gemm_kernel, grid, dim3(256), 0, s, false, p, mode);
+  return launch_pdl(simt_gemm_kernel, grid, dim3(256), 0, s, 0, p, mode);
 }
 
 }  // namespace dpclip

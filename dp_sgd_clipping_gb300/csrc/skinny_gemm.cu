@@ -424,11 +424,11 @@ cudaError_t launch_tok_gemm(const TokGemmParams& p, cudaStream_t s) {
   if (p.NP == 16) {
     const size_t sm = skinny_smem_bytes<16>();
     if ((e = set_smem(tok_gemm_kernel<16>, sm)) != cudaSuccess) return e;
-    return launch_pdl(tok_gemm_kernel<16>, grid, dim3(128), sm, s, false, p);
+    return launch_pdl(tok_gemm_kernel<16>, grid, dim3(128), sm, s, 0, p);
   } else if (p.NP == 32) {
     const size_t sm = skinny_smem_bytes<32>();
     if ((e = set_smem(tok_gemm_kernel<32>, sm)) != cudaSuccess) return e;
-    return launch_pdl(tok_gemm_kernel<32>, grid, dim3(128), sm, s, false, p);
+    return launch_pdl(tok_gemm_kernel<32>, grid, dim3(128), sm, s, 0, p);
   }
   return cudaErrorInvalidValue;
 }
@@ -439,7 +439,7 @@ static cudaError_t launch_feat_t(const FeatGemmParams& p, cudaStream_t s) {
   const size_t sm = skinny_smem_bytes<NP>();
   cudaError_t e = set_smem(feat_gemm_kernel<NP, MODE>, sm);
   if (e != cudaSuccess) return e;
-  return launch_pdl(feat_gemm_kernel<NP, MODE>, grid, dim3(128), sm, s, false, p);
+  return launch_pdl(feat_gemm_kernel<NP, MODE>, grid, dim3(128), sm, s, 0, p);
 }
 
 cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s) {

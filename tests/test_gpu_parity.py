@@ -249,6 +249,18 @@ def test_hutchpp_budgets(api, k):
     _run_all(api, wl, paths=("hutchpp",))
 
 
+@pytest.mark.parametrize("case", ["bf16", "f32_rankdef"])
+def test_hutchpp_wide_layer(api, case):
+    # p = 20000 (17001) rows: each CTA of the sample's cluster owns more rows
+    # than it keeps resident, so V and G' are staged tile by tile in every pass;
+    # with T = 7 < r = 10 the head also drops dependent columns on that path.
+    if case == "bf16":
+        wl = W.Workload(174, "hpp_wide", 2, 40, 24, 20000, "bf16", 1e-2, 1.0, 1.0, 32, ())
+    else:
+        wl = W.Workload(175, "hpp_wide_f32", 2, 7, 24, 17001, "f32", 1.0, 1.0, 1.0, 32, ())
+    _run_all(api, wl, paths=("hutchpp",))
+
+
 def test_f32_odd_shapes(api):
     wl = W.Workload(170, "f32_odd", 3, 37, 29, 50, "f32", 1.0, 1.0, 1.0, 7, ())
     _run_all(api, wl)
