@@ -37,7 +37,8 @@ WORKLOAD_ID = 4
 METRIC = "clip+noise tokens/s per linear layer (Hutch/Hutch++/exact); % bf16 tensor peak"
 ROWS = ("hutch", "hutchpp", "exact_direct", "exact_ghost", "clipped_noisy_grad")
 # measured after the step, not part of it: the Rademacher-probe variants
-EXTRA_ROWS = ("hutch_rademacher", "hutchpp_rademacher")
+EXTRA_ROWS = ("hutch_rademacher", "hutchpp_rademacher", "exact_direct_stored",
+              "stored_clipped_noisy_grad")
 # kernels each ABI call launches for bf16 inputs (memsets of the control block excluded)
 LAUNCHES = {"hutch": 3, "hutchpp": 9, "exact_direct": 1, "exact_ghost": 1, "clipped_noisy_grad": 1}
 
@@ -53,6 +54,10 @@ def algorithmic_work(wl):
         "hutchpp": (3.0 * ag, "bytes", "hbm"),
         "hutch_rademacher": (ag + 2.0 * k * p, "bytes", "hbm"),
         "hutchpp_rademacher": (3.0 * ag, "bytes", "hbm"),
+        # exact direct norms that keep every A_i^T G_i, then the clipped sum
+        # as one elementwise pass over them (read B d p fp32, write d p fp32)
+        "exact_direct_stored": (2.0 * B * T * d * p, "flops", "tensor"),
+        "stored_clipped_noisy_grad": (4.0 * (B + 1) * d * p, "bytes", "hbm"),
         "exact_direct": (2.0 * B * T * d * p, "flops", "tensor"),
         "exact_ghost": (1.0 * B * T * (T + 1) * (d + p), "flops", "tensor"),
         "clipped_noisy_grad": (2.0 * B * T * d * p, "flops", "tensor"),
@@ -253,6 +258,12 @@ def main():
           "exact_direct": ws_for(L.OP_NORMS_EXACT, L.EXACT_DIRECT),
           "exact_ghost": ws_for(L.OP_NORMS_EXACT, L.EXACT_GHOST),
           "clipped_noisy_grad": ws_for(L.OP_CLIPPED_NOISY_GRAD, 0)}
+    stored = {}   # StoredGradients of the stored-direct extra rows
+
+    def ensure_stored_ws():
+        if "ws" not in stored:
+            stored["ws"] = ws_for(L.OP_STORED_DIRECT, 0)
+        return stored["ws"]
     stream = torch.cuda.current_stream(dev)
 
     def row_fn(name, step, bufs=None):
@@ -272,6 +283,17 @@ def main():
                                              ws=ws["hutchpp"], probe="rademacher")
         if name == "exact_direct":
             return lambda: api.norms_exact(b["A"], b["G"], L.EXACT_DIRECT, out=b["q_d"], ws=ws[name])
+        if name == "exact_direct_stored":
+            def call():
+                _, stored["h"] = api.norms_direct_store(b["A"], b["G"], sqnorms=b["q_d"],
+                                                        ws=ensure_stored_ws())
+            return call
+        if name == "stored_clipped_noisy_grad":
+            if "h" not in stored:
+                row_fn("exact_direct_stored", step, bufs)()
+            return lambda: api.stored_clipped_noisy_grad(stored["h"], b["q_d"], wl.C, wl.sigma,
+                                                         wl.seed, step, grad=b["grad"],
+                                                         scales=b["scales"], clipped=b["clipped"])
         if name == "exact_ghost":
             return lambda: api.norms_exact(b["A"], b["G"], L.EXACT_GHOST, out=b["q_g"], ws=ws[name])
         return lambda: api.clipped_noisy_grad(b["A"], b["G"], b["q_h"], wl.C, wl.sigma, wl.seed, step,
@@ -311,6 +333,8 @@ def main():
     clk = clocks.stop(wall0, wall1) if rank == 0 else None
     elapsed_ms = start.elapsed_time(end)
     for name in rows:
+        if name not in ws:
+            continue
         st = api.workspace_status(ws[name])
         if st != 0:
             raise SystemExit(f"{name}: device reported status {st}")
@@ -439,9 +463,18 @@ def main():
     extra = {}
     for r, ms in extra_ms.items():
         amount, unit, bound = work[r]
-        ach, pk, u = amount / (ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        if unit == "bytes":
+            ach, pk, u = amount / (ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            ach, pk, u = amount / (ms * 1e-3) / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
         extra[r] = {"ms": round(ms, 4), "tokens_per_s": B * T / (ms * 1e-3), "bound": bound,
                     "achieved": round(ach, 2), "peak": pk, "unit": u, "frac": round(ach / pk, 4)}
+    if "exact_direct_stored" in extra_ms and "stored_clipped_noisy_grad" in extra_ms:
+        # exact norms + clipped noisy gradient of the layer, against the same
+        # two results from exact_direct + clipped_noisy_grad (two GEMMs)
+        ms = extra_ms["exact_direct_stored"] + extra_ms["stored_clipped_noisy_grad"]
+        extra["layer_exact_stored_total"] = {"ms": round(ms, 4),
+                                             "tokens_per_s": B * T / (ms * 1e-3)}
     dom = max(rows, key=lambda r: row_ms[r])
     traffic = _traffic_from_profiles(dom)
     roof = dict(breakdown[dom])

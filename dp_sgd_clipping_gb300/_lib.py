@@ -24,6 +24,7 @@ EXACT_AUTO, EXACT_GHOST, EXACT_DIRECT = 0, 1, 2
 PROBE_GAUSSIAN, PROBE_RADEMACHER = 0, 1
 PROBES = {"gaussian": PROBE_GAUSSIAN, "rademacher": PROBE_RADEMACHER}
 OP_NORMS_EXACT, OP_NORMS_HUTCH, OP_NORMS_HUTCHPP, OP_CLIPPED_NOISY_GRAD = 0, 1, 2, 3
+OP_STORED_DIRECT = 4
 HUTCH_MAX_K = 32
 HUTCHPP_MAX_K = 48
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -46,6 +47,9 @@ SIGNATURES = {
     "dpclip_clipped_noisy_grad": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _f, _u64, _u64,
                                        _vp, _vp, _vp, _vp, _sz, _vp]),
     "dpclip_clip_scales": (_i, [_vp, _i, _f, _vp, _vp, _vp]),
+    "dpclip_norms_direct_store": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "dpclip_stored_clipped_noisy_grad": (_i, [_i, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _vp, _vp,
+                                              _vp, _sz, _vp]),
     "dpclip_norms_hutch_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp]),
     "dpclip_philox_normal": (_i, [_vp, _i64, _i, _u64, _u32, _u64, _vp]),
     "dpclip_workspace_status": (_i, [_vp, _vp]),

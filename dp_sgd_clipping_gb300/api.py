@@ -12,6 +12,7 @@ import torch
 from . import _lib as L
 
 __all__ = ["norms_exact", "norms_hutch", "norms_hutchpp", "clipped_noisy_grad", "clip_scales",
+           "norms_direct_store", "stored_clipped_noisy_grad", "StoredGradients",
            "philox_normal", "philox_rademacher", "workspace_bytes", "workspace_status",
            "selftest_wait_timeout"]
 
@@ -99,6 +100,54 @@ def clipped_noisy_grad(A, G, sqnorms, C: float, sigma: float, seed: int, offset:
     L.check("dpclip_clipped_noisy_grad", L.lib.dpclip_clipped_noisy_grad(
         A.data_ptr(), G.data_ptr(), B, T, d, p, dt, sqnorms.data_ptr(), float(C), float(sigma),
         seed, offset, grad.data_ptr(), scales.data_ptr() if scales is not None else None,
+        clipped.data_ptr() if clipped is not None else None, ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream(stream)))
+    return grad, scales, clipped
+
+
+class StoredGradients:
+    """The workspace of a norms_direct_store call: it holds the per-sample
+    gradients that stored_clipped_noisy_grad reads.  Keep it alive (and
+    unchanged) until that call has been enqueued."""
+
+    def __init__(self, ws, B: int, d: int, p: int):
+        self.ws, self.B, self.d, self.p = ws, B, d, p
+
+
+def norms_direct_store(A, G, sqnorms=None, accumulate: bool = False, ws=None, stream=None):
+    """Exact per-sample squared norms (direct method), keeping every A_i^T G_i.
+
+    Returns (sqnorms, StoredGradients).  With accumulate=True the norms are
+    added to `sqnorms` (summing the layers of a model)."""
+    B, T, d, p, dt = _check_pair(A, G)
+    nb = workspace_bytes(L.OP_STORED_DIRECT, B, T, d, p, dt, 0)
+    ws = _workspace(nb, A.device, ws)
+    if sqnorms is None:
+        if accumulate:
+            raise ValueError("accumulate needs the sqnorms tensor to add to")
+        sqnorms = torch.empty(B, dtype=torch.float32, device=A.device)
+    L.check("dpclip_norms_direct_store", L.lib.dpclip_norms_direct_store(
+        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, int(bool(accumulate)), sqnorms.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)))
+    return sqnorms, StoredGradients(ws, B, d, p)
+
+
+def stored_clipped_noisy_grad(stored: StoredGradients, sqnorms, C: float, sigma: float, seed: int,
+                              offset: int = 0, grad=None, scales=None, clipped=None, stream=None,
+                              want_scales: bool = True):
+    """clipped_noisy_grad from the per-sample gradients kept by norms_direct_store.
+
+    Returns (grad [d, p] fp32, scales [B] fp32, clipped [B] uint8)."""
+    B, d, p, ws = stored.B, stored.d, stored.p, stored.ws
+    if sqnorms.dtype != torch.float32 or sqnorms.numel() != B or not sqnorms.is_cuda:
+        raise ValueError("sqnorms must be a CUDA float32 tensor of B entries")
+    grad = torch.empty(d, p, dtype=torch.float32, device=ws.device) if grad is None else grad
+    if want_scales:
+        scales = torch.empty(B, dtype=torch.float32, device=ws.device) if scales is None else scales
+        clipped = torch.empty(B, dtype=torch.uint8, device=ws.device) if clipped is None else clipped
+    L.check("dpclip_stored_clipped_noisy_grad", L.lib.dpclip_stored_clipped_noisy_grad(
+        B, d, p, sqnorms.data_ptr(), float(C), float(sigma), seed, offset, grad.data_ptr(),
+        scales.data_ptr() if scales is not None else None,
         clipped.data_ptr() if clipped is not None else None, ws.data_ptr(),
         ws.numel() * ws.element_size(), _stream(stream)))
     return grad, scales, clipped

@@ -66,7 +66,7 @@ __global__ void clip_scales_kernel(const float* sq, int B, float C, float* scale
 // sq[i] = scale * sum over units u and slots w of part[(u*su + i*si)*nw + w];
 // one block per sample, fixed summation tree.
 __global__ void finalize_norms_kernel(const float* part, int nunits, long long su, long long si,
-                                      int nw, float scale, float* sq) {
+                                      int nw, float scale, float* sq, int accumulate) {
   __shared__ float red[32];
   pdl_trigger();
   pdl_wait();
@@ -83,7 +83,94 @@ __global__ void finalize_norms_kernel(const float* part, int nunits, long long s
   if (threadIdx.x == 0) {
     float s = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-    sq[i] = scale * s;
+    sq[i] = accumulate ? sq[i] + scale * s : scale * s;
+  }
+}
+
+// Stored per-sample gradients -> clipped noisy sum ("DP-SGD algorithm" steps
+// 3-4 of the DP-SGD glossary): one thread per Philox block of four elements,
+// the samples added in index order.
+__global__ void stored_grad_kernel(const float* __restrict__ M, int B, long long n,
+                                   long long stride, const float* sq, float C, float nscale,
+                                   uint64_t seed, uint64_t offset, float* grad, float* scales,
+                                   uint8_t* clipped) {
+  extern __shared__ float s_sh[];
+  pdl_trigger();
+  pdl_wait();
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    const float q = sq[i];
+    const float si = q > 0.f ? fminf(1.f, C / sqrtf(q)) : 1.f;
+    s_sh[i] = si;
+    if (blockIdx.x == 0) {
+      if (scales) scales[i] = si;
+      if (clipped) clipped[i] = (uint8_t)(sqrtf(fmaxf(q, 0.f)) > C);
+    }
+  }
+  __syncthreads();
+  const long long nb = (n + 3) / 4, s4 = stride / 4;
+  const float4* M4 = reinterpret_cast<const float4*>(M);
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nb;
+       b += (long long)gridDim.x * blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int i = 0;
+    for (; i + 4 <= B; i += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldcs(M4 + (size_t)(i + u) * s4 + b);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float si = s_sh[i + u];
+        acc.x = fmaf(si, v[u].x, acc.x);
+        acc.y = fmaf(si, v[u].y, acc.y);
+        acc.z = fmaf(si, v[u].z, acc.z);
+        acc.w = fmaf(si, v[u].w, acc.w);
+      }
+    }
+    for (; i < B; ++i) {
+      const float4 v = __ldcs(M4 + (size_t)i * s4 + b);
+      const float si = s_sh[i];
+      acc.x = fmaf(si, v.x, acc.x);
+      acc.y = fmaf(si, v.y, acc.y);
+      acc.z = fmaf(si, v.z, acc.z);
+      acc.w = fmaf(si, v.w, acc.w);
+    }
+    if (nscale != 0.f) {
+      float z[4];
+      philox_normal4(seed, 3u, offset, (uint32_t)b, z);
+      acc.x = fmaf(nscale, z[0], acc.x);
+      acc.y = fmaf(nscale, z[1], acc.y);
+      acc.z = fmaf(nscale, z[2], acc.z);
+      acc.w = fmaf(nscale, z[3], acc.w);
+    }
+    if (4 * b + 3 < n) {
+      reinterpret_cast<float4*>(grad)[b] = acc;
+    } else {   // ragged end: lanes past n hold padding and are not stored
+      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+      for (int l = 0; 4 * b + l < n; ++l) grad[4 * b + l] = a4[l];
+    }
+  }
+}
+
+// part[i * nblk + b] = sum of squares of elements [b c, (b + 1) c) of sample i
+// (at M + i * stride), c = ceil(n / nblk); fixed summation tree.
+__global__ void stored_sqnorm_kernel(const float* __restrict__ M, long long n, long long stride,
+                                     float* part) {
+  __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
+  const int i = blockIdx.y, nblk = gridDim.x;
+  const long long chunk = (n + nblk - 1) / nblk;
+  const long long e0 = blockIdx.x * chunk, e1 = min(n, e0 + chunk);
+  const float* m = M + (size_t)i * stride;
+  float acc = 0.f;
+  for (long long e = e0 + threadIdx.x; e < e1; e += blockDim.x) acc = fmaf(m[e], m[e], acc);
+  acc = warp_sum(acc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+    part[(size_t)i * nblk + blockIdx.x] = s;
   }
 }
 
@@ -146,9 +233,26 @@ cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, u
 }
 
 cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long long su, long long si,
-                                  int nw, float scale, float* sq, cudaStream_t s) {
+                                  int nw, float scale, float* sq, cudaStream_t s, int accumulate) {
   return launch_pdl(finalize_norms_kernel, dim3(B), dim3(256), 0, s, 0, part, nunits, su, si,
-                    nw, scale, sq);
+                    nw, scale, sq, accumulate);
+}
+
+cudaError_t launch_stored_grad(const float* M, int B, long long n, long long stride,
+                               const float* sq, float C, float nscale, uint64_t seed,
+                               uint64_t offset, float* grad, float* scales, uint8_t* clipped,
+                               cudaStream_t s) {
+  const long long nb = (n + 3) / 4;
+  const int threads = 256;
+  const int grid = (int)std::max<long long>(1, std::min<long long>((nb + threads - 1) / threads,
+                                                                   152 * 8));
+  return launch_pdl(stored_grad_kernel, dim3(grid), dim3(threads), (size_t)B * sizeof(float), s,
+                    0, M, B, n, stride, sq, C, nscale, seed, offset, grad, scales, clipped);
+}
+
+cudaError_t launch_stored_sqnorm(const float* M, int B, long long n, long long stride, int nblk,
+                                 float* part, cudaStream_t s) {
+  return launch_pdl(stored_sqnorm_kernel, dim3(nblk, B), dim3(256), 0, s, 0, M, n, stride, part);
 }
 
 cudaError_t launch_noise_add(float* grad, long long n, float scale, uint64_t seed, uint64_t offset,

@@ -306,12 +306,13 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 // Every thread of every CTA calls it once at the end of the kernel.  The
 // summation order is fixed (thread partition, 8-wide batches, shuffle tree,
 // warps in order), so results do not depend on CTA timing.  `ticket` must be
-// zero at launch; the last CTA resets it.
+// zero at launch; the last CTA resets it.  With `accumulate`, sq[i] += the
+// result instead.
 __device__ __forceinline__ void reduce_partials_last_cta(const float* part, int B, int nunits,
                                                          long long su, long long si, int nw,
                                                          float scale, float* sq,
                                                          uint32_t* ticket, float* red_smem,
-                                                         int* flag_smem) {
+                                                         int* flag_smem, bool accumulate = false) {
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) *flag_smem = (atomicAdd(ticket, 1u) == gridDim.x - 1u) ? 1 : 0;
@@ -339,7 +340,7 @@ __device__ __forceinline__ void reduce_partials_last_cta(const float* part, int 
     if (threadIdx.x == 0) {
       float s = 0.f;
       for (int w = 0; w < nwarps; ++w) s += red_smem[w];
-      sq[i] = scale * s;
+      sq[i] = accumulate ? sq[i] + scale * s : scale * s;
     }
     __syncthreads();
   }

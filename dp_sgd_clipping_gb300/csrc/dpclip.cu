@@ -292,6 +292,24 @@ Plan plan_grad(int d, int p, int dtype) {
   return pl;
 }
 
+// Stored direct norms: the control block, then the per-sample gradients M
+// (at offset kAlign, so that the gradient call finds them from B, d and p
+// alone; sample i at i * stored_stride floats), then the norm partials.
+constexpr int kStoredSqBlocks = 64;   // fp32 path: chunks per sample of ||M_i||^2
+size_t stored_stride(int d, int p) { return ((size_t)d * p + 3) / 4 * 4; }
+
+Plan plan_stored(int B, int d, int p, int dtype) {
+  Plan pl;
+  Carve c;
+  pl.ctrl_bytes = kAlign;
+  pl.ctrl = c.take(pl.ctrl_bytes);
+  pl.off[0] = c.take((size_t)B * stored_stride(d, p) * 4);
+  pl.off[1] = c.take(dtype == DPCLIP_BF16 ? (size_t)dp_ntiles(d, p) * B * kEpiWarps * 4
+                                          : (size_t)B * kStoredSqBlocks * 4);
+  pl.total = c.total();
+  return pl;
+}
+
 int hutch_k_ok(int k) { return k >= 1 && k <= DPCLIP_HUTCH_MAX_K; }
 int hutchpp_k_ok(int k) { return k >= 3 && k <= DPCLIP_HUTCHPP_MAX_K && (k - k / 3) <= kMaxNP; }
 
@@ -314,6 +332,9 @@ int plan_for(int op, int B, int T, int d, int p, int dtype, int param, Plan& pl)
       return DPCLIP_OK;
     case DPCLIP_OP_CLIPPED_NOISY_GRAD:
       pl = plan_grad(d, p, dtype);
+      return DPCLIP_OK;
+    case DPCLIP_OP_STORED_DIRECT:
+      pl = plan_stored(B, d, p, dtype);
       return DPCLIP_OK;
     default:
       return DPCLIP_ERR_INVALID_ARG;
@@ -810,6 +831,69 @@ int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d,
   if (sigma > 0.f)
     DPCLIP_CUDA(launch_noise_add(grad, (long long)d * p, sigma * C, seed, offset, s));
   if (scales || clipped) DPCLIP_CUDA(launch_clip_scales(sqnorms, B, C, scales, clipped, s));
+  return DPCLIP_OK;
+}
+
+int dpclip_norms_direct_store(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                              int accumulate, float* sqnorms, void* ws, size_t ws_bytes,
+                              dpclip_stream_t stream) {
+  DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
+  if (!sqnorms || (accumulate != 0 && accumulate != 1)) return DPCLIP_ERR_INVALID_ARG;
+  const Plan pl = plan_stored(B, d, p, dtype);
+  DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
+  cudaStream_t s = (cudaStream_t)stream;
+  float* M = at<float>(ws, pl.off[0]);
+  const long long stride = (long long)stored_stride(d, p);
+  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  if (dtype == DPCLIP_BF16) {
+    GemmDpParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!make_map(&gp.map_a, A, d, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
+    if (!make_map(&gp.map_g, G, p, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
+    gp.B = B;
+    gp.T = T;
+    gp.d = d;
+    gp.p = p;
+    gp.mtiles = cdiv(d, kDpTileM);
+    gp.ntiles = cdiv(p, kDpTileN);
+    gp.tblocks = cdiv(T, kBlockK);
+    gp.part = at<float>(ws, pl.off[1]);
+    gp.sq = sqnorms;
+    gp.ticket = at<uint32_t>(ws, pl.ctrl + 4);
+    gp.err = at<uint32_t>(ws, pl.ctrl);
+    gp.pstore = M;
+    gp.accumulate = accumulate;
+    const int ntiles = gp.mtiles * gp.ntiles;
+    DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min({ntiles * B, num_sms(), kMaxPersistentGrid}), s));
+    return DPCLIP_OK;
+  }
+  SimtParams sp = simt_base();
+  sp.X = static_cast<const float*>(A); sp.xb = (long long)T * d; sp.xm = 1; sp.xk = d;   // A_i^T
+  sp.Y = static_cast<const float*>(G); sp.yb = (long long)T * p; sp.yk = p; sp.yn = 1;   // G_i
+  sp.batch = B; sp.M = d; sp.N = p; sp.K = T;
+  sp.out = M; sp.ob = stride; sp.om = p; sp.on = 1;
+  int nb = 0;
+  DPCLIP_CUDA(launch_simt(sp, kSimtStore, s, &nb));
+  float* part = at<float>(ws, pl.off[1]);
+  DPCLIP_CUDA(launch_stored_sqnorm(M, B, (long long)d * p, stride, kStoredSqBlocks, part, s));
+  DPCLIP_CUDA(launch_finalize_norms(part, B, kStoredSqBlocks, 1, kStoredSqBlocks, 1, 1.f, sqnorms,
+                                    s, accumulate));
+  return DPCLIP_OK;
+}
+
+int dpclip_stored_clipped_noisy_grad(int B, int d, int p, const float* sqnorms, float C,
+                                     float sigma, uint64_t seed, uint64_t offset, float* grad,
+                                     float* scales, uint8_t* clipped, const void* ws,
+                                     size_t ws_bytes, dpclip_stream_t stream) {
+  if (B <= 0 || d <= 0 || p <= 0 || !sqnorms || !grad) return DPCLIP_ERR_INVALID_ARG;
+  if (!(C > 0.f) || !std::isfinite(C)) return DPCLIP_ERR_INVALID_ARG;
+  if (!(sigma >= 0.f) || !std::isfinite(sigma)) return DPCLIP_ERR_INVALID_ARG;
+  if (!aligned(grad, 16) || B > kMaxStoredB) return DPCLIP_ERR_UNSUPPORTED;
+  const long long stride = (long long)stored_stride(d, p);
+  DPCLIP_TRY(check_ws(ws, ws_bytes, kAlign + (size_t)B * stride * 4));
+  const float* M = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + kAlign);
+  DPCLIP_CUDA(launch_stored_grad(M, B, (long long)d * p, stride, sqnorms, C, sigma * C, seed,
+                                 offset, grad, scales, clipped, (cudaStream_t)stream));
   return DPCLIP_OK;
 }
 

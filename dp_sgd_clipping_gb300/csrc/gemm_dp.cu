@@ -8,7 +8,9 @@
 //               rescaled by s_i is, for one linear layer, this scaled sum.
 //   norm mode  (direct exact norm, the per-sample gradient materialisation of
 //               "Problem definition", reduced on chip): partial sums of
-//               (A_i^T G_i)^2, never storing the d x p tile.
+//               (A_i^T G_i)^2.  The stored variant also writes every tile
+//               to M_i = A_i^T G_i ([B][d][p] fp32): the clipped sum is then
+//               an elementwise pass over M instead of a second GEMM.
 //
 // Output tiles are 128 d-rows x 256 p-columns; both operands are MN-major
 // (tokens are the slow axis of A and G), loaded by TMA with 128-byte swizzle.
@@ -72,6 +74,11 @@ struct Ctl {
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kABytes + kGBytes) + sizeof(Ctl);
+// Stored norm mode: one 32 x 33 fp32 transpose tile per epilogue warp, so
+// that each store instruction writes 32 consecutive floats of one row.
+constexpr size_t kStoreTileFloats = 32 * 33;
+constexpr size_t kSmemBytesStore = kSmemBytes + kEpiWarps * kStoreTileFloats * sizeof(float);
+static_assert(kSmemBytesStore <= 232448, "stored variant exceeds the shared memory of a CTA");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -400,15 +407,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
                            (itm.tile / p.mtiles) * kDpTileN + half * 128, tot);
       } else {
         float ss = 0.f;
+        if (p.pstore) {
+          // stored variant: read the whole 32 x 128 slab, release the
+          // accumulator, then write the slab to M_i through a per-warp
+          // transpose tile, one 128-byte row segment per store instruction
+          float v[4][32];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          float v[32];
-          tmem_ld32(taddr + c4 * 32, v);
+          for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(taddr + c4 * 32, v[c4]);
+          tc_fence_before();
+          mbar_arrive(&ctl->tempty[acc]);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+          for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ss = fmaf(v[c4][j], v[c4][j], ss);
+          float* tb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctl) + sizeof(Ctl)) +
+                      (size_t)ew * kStoreTileFloats;
+          const int r0 = (itm.tile % p.mtiles) * kDpTileM + quad * 32;
+          const int cb = (itm.tile / p.mtiles) * kDpTileN + half * 128;
+          const int nrows = min(32, p.d - r0);
+          float* mbase = p.pstore + ((size_t)itm.i * p.d + r0) * p.p;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tb[lane * 33 + j] = v[c4][j];
+            __syncwarp();
+            const int c = cb + c4 * 32 + lane;
+            if (c < p.p)
+              for (int rr = 0; rr < nrows; ++rr) mbase[(size_t)rr * p.p + c] = tb[rr * 33 + lane];
+          }
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float v[32];
+            tmem_ld32(taddr + c4 * 32, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+          }
+          tc_fence_before();
+          mbar_arrive(&ctl->tempty[acc]);
         }
-        tc_fence_before();
-        mbar_arrive(&ctl->tempty[acc]);
         ss = warp_sum(ss);
         if (lane == 0) p.part[((size_t)itm.tile * p.B + itm.i) * kEpiWarps + ew] = ss;
       }
@@ -417,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 
   if (!kGrad)
     reduce_partials_last_cta(p.part, p.B, ntiles_total, p.B, 1, kEpiWarps, 1.f, p.sq, p.ticket,
-                             ctl->red, &ctl->is_last);
+                             ctl->red, &ctl->is_last, p.accumulate != 0);
 
   tc_fence_before();
   __syncthreads();
@@ -495,10 +533,11 @@ cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cuda
       return e;
     return launch_pdl(gemm_dp_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, 0, p);
   }
+  const size_t smem = p.pstore ? kSmemBytesStore : kSmemBytes;
   if ((e = cudaFuncSetAttribute(gemm_dp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSmemBytes)) != cudaSuccess)
+                                (int)smem)) != cudaSuccess)
     return e;
-  return launch_pdl(gemm_dp_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, s, 0, p);
+  return launch_pdl(gemm_dp_kernel<false>, dim3(grid), dim3(kThreads), smem, s, 0, p);
 }
 
 }  // namespace dpclip

@@ -114,6 +114,8 @@ struct GemmDpParams {
   float* sq;             // norm mode: per-sample result [B]
   uint32_t* ticket;      // norm mode: zeroed grid ticket
   uint32_t* err;
+  float* pstore;         // norm mode: if set, every tile A_i^T G_i also goes to [B][d][p]
+  int accumulate;        // norm mode: sq[i] += the estimate (else =)
 };
 
 // ghost: per sample i and token tiles a <= b, sum((A_a A_b^T) o (G_a G_b^T)),
@@ -192,8 +194,21 @@ cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t ro
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
                                cudaStream_t s);
 // sq[i] = scale * sum_{u < nunits, w < nw} part[(u * su + i * si) * nw + w]
+// grad[e] = sum_i s_i M_i[e] + nscale z_e (z: Philox stream 3, element e), e < n,
+// M_i = M + i * stride (stride a multiple of 4, M and grad 16-byte aligned),
+// s_i = min(1, C / sqrt(sq[i])) (1 for sq[i] = 0); scales and clipped (either
+// may be null) get s_i and [sqrt(sq[i]) > C].  B <= kMaxStoredB.
+constexpr int kMaxStoredB = 12288;
+cudaError_t launch_stored_grad(const float* M, int B, long long n, long long stride,
+                               const float* sq, float C, float nscale, uint64_t seed,
+                               uint64_t offset, float* grad, float* scales, uint8_t* clipped,
+                               cudaStream_t s);
+// part[i * nblk + b] = sum of squares of chunk b of M_i (n elements at M + i * stride).
+cudaError_t launch_stored_sqnorm(const float* M, int B, long long n, long long stride, int nblk,
+                                 float* part, cudaStream_t s);
 cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long long su,
-                                  long long si, int nw, float scale, float* sq, cudaStream_t s);
+                                  long long si, int nw, float scale, float* sq, cudaStream_t s,
+                                  int accumulate = 0);
 cudaError_t launch_noise_add(float* grad, long long n, float scale, uint64_t seed,
                              uint64_t offset, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t s);

@@ -86,7 +86,8 @@ enum dpclip_op {
   DPCLIP_OP_NORMS_EXACT = 0,
   DPCLIP_OP_NORMS_HUTCH = 1,
   DPCLIP_OP_NORMS_HUTCHPP = 2,
-  DPCLIP_OP_CLIPPED_NOISY_GRAD = 3
+  DPCLIP_OP_CLIPPED_NOISY_GRAD = 3,
+  DPCLIP_OP_STORED_DIRECT = 4    /* dpclip_norms_direct_store + dpclip_stored_clipped_noisy_grad */
 };
 
 /* Largest probe count k for Hutch (k <= 32) and Hutch++ (k - floor(k/3) <= 32). */
@@ -147,6 +148,32 @@ int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d,
                               uint64_t seed, uint64_t offset, float* grad, float* scales,
                               uint8_t* clipped, void* ws, size_t ws_bytes,
                               dpclip_stream_t stream);
+
+/* Exact per-sample squared norms by the direct method, keeping every
+ * per-sample gradient M_i = A_i^T G_i (fp32) in `ws` for
+ * dpclip_stored_clipped_noisy_grad.  This is the per-sample gradient
+ * materialisation of "Problem definition" taken as a deliberate trade: it
+ * costs B*d*p*4 bytes of workspace (268 MB for B = 4 at d x p = 2048 x 8192,
+ * small against this GPU's HBM), and in return the clipped sum is one
+ * elementwise pass over the stored gradients instead of a second GEMM over A
+ * and G.  accumulate = 0: sqnorms[i] = ||M_i||_F^2; accumulate = 1:
+ * sqnorms[i] += ||M_i||_F^2 (the per-sample norm of a whole model is the sum
+ * over its layers).  Workspace: dpclip_workspace_size(DPCLIP_OP_STORED_DIRECT,
+ * ...), param ignored; its contents must be kept, unchanged, until the
+ * matching dpclip_stored_clipped_noisy_grad has been enqueued. */
+int dpclip_norms_direct_store(const void* A, const void* G, int B, int T, int d, int p,
+                              int dtype, int accumulate, float* sqnorms, void* ws,
+                              size_t ws_bytes, dpclip_stream_t stream);
+
+/* The clipped noisy gradient of dpclip_clipped_noisy_grad (same formula, the
+ * same noise stream and element mapping, the same optional outputs) from the
+ * per-sample gradients a dpclip_norms_direct_store call with the same B, d
+ * and p left in `ws`, enqueued after it on the same stream.  sqnorms may
+ * hold the sum over several layers.  grad: 16-byte aligned. */
+int dpclip_stored_clipped_noisy_grad(int B, int d, int p, const float* sqnorms, float C,
+                                     float sigma, uint64_t seed, uint64_t offset, float* grad,
+                                     float* scales, uint8_t* clipped, const void* ws,
+                                     size_t ws_bytes, dpclip_stream_t stream);
 
 /* Clip scales alone: scales[i] = min(1, C / sqrt(sqnorms[i])) (1 when the norm
  * is 0) and clipped[i] = sqrt(sqnorms[i]) > C; either output may be NULL. */

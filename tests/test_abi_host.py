@@ -55,6 +55,11 @@ def test_workspace_sizes(L):
     assert direct > 0 and ghost > 0
     assert ws(L.OP_NORMS_HUTCH, 4, 64, 32, 48, L.F32, 8) > 0
     assert ws(L.OP_NORMS_EXACT, 4, 64, 32, 48, L.F32, L.EXACT_GHOST) >= 4 * 64 * 64 * 4
+    # stored direct norms: the control block, B fp32 d x p gradients (each
+    # padded to a multiple of 4 floats), then the norm partials
+    st = ws(L.OP_STORED_DIRECT, 4, 4096, 2048, 8192, L.BF16, 0)
+    assert 256 + 4 * 2048 * 8192 * 4 < st < 256 + 4 * 2048 * 8192 * 4 + (1 << 20)
+    assert ws(L.OP_STORED_DIRECT, 3, 37, 29, 50, L.F32, 0) >= 256 + 3 * 1452 * 4
 
 
 def test_workspace_size_rejects(L):
@@ -123,6 +128,18 @@ def test_entry_points_reject_before_any_launch(L):
     assert lib.dpclip_norms_hutchpp_ex(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 9, -1, 1, 0, FAKE, FAKE,
                                        big, None) == L.ERR_INVALID_ARG
     assert lib.dpclip_philox_rademacher(None, 10, L.F32, 1, 0, 0, None) == L.ERR_INVALID_ARG
+    # stored direct norms and their gradient
+    st = lib.dpclip_norms_direct_store
+    assert st(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 2, FAKE, FAKE, big, None) == L.ERR_INVALID_ARG
+    assert st(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 0, None, FAKE, big, None) == L.ERR_INVALID_ARG
+    assert st(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 0, FAKE, FAKE, 1024, None) == L.ERR_WORKSPACE
+    sg = lib.dpclip_stored_clipped_noisy_grad
+    assert sg(0, 16, 16, FAKE, 1.0, 1.0, 1, 0, FAKE, None, None, FAKE, big, None) == L.ERR_INVALID_ARG
+    assert sg(2, 16, 16, FAKE, -1.0, 1.0, 1, 0, FAKE, None, None, FAKE, big, None) == L.ERR_INVALID_ARG
+    assert sg(2, 16, 16, FAKE, 1.0, 1.0, 1, 0, FAKE + 4, None, None, FAKE, big,
+              None) == L.ERR_UNSUPPORTED
+    assert sg(2, 16, 16, FAKE, 1.0, 1.0, 1, 0, FAKE, None, None, FAKE, 256 + 2 * 256 * 4 - 1,
+              None) == L.ERR_WORKSPACE
 
 
 def test_product_path_does_not_import_oracle():

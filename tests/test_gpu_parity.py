@@ -37,11 +37,16 @@ def oracle_all(inp, k=None, want=("direct", "hutch", "hutchpp")):
     return out
 
 
-def check_grad(api, inp, A, G, q, C, sigma, Ms, offset=0):
+def check_grad(api, inp, A, G, q, C, sigma, Ms, offset=0, stored=None):
+    # stored: the StoredGradients of norms_direct_store; then the gradient comes
+    # from the stored per-sample tiles instead of a second GEMM
     wl = inp.wl
     tol = TOL[wl.dtype]
     qd = torch.tensor(q, dtype=torch.float32, device="cuda")
-    grad, scales, clipped = api.clipped_noisy_grad(A, G, qd, C, sigma, wl.seed, offset)
+    if stored is None:
+        grad, scales, clipped = api.clipped_noisy_grad(A, G, qd, C, sigma, wl.seed, offset)
+    else:
+        grad, scales, clipped = api.stored_clipped_noisy_grad(stored, qd, C, sigma, wl.seed, offset)
     torch.cuda.synchronize()
     q32 = qd.double().cpu().numpy()          # the sqnorms the GPU saw
     D, s_ref, _ = O.clipped_noisy_grad(None, None, q32, C, sigma, wl.seed, offset, Ms=Ms)
@@ -194,6 +199,10 @@ def test_full_size_workloads(api, wid):
     if "direct" in wl.runs:
         assert_rel(host(api.norms_exact(A, G, method=2)), ref["direct"], tol, "direct")
     check_grad(api, inp, A, G, host(q_h), wl.C, wl.sigma, ref["Ms"])
+    # the stored variant of the exact norms and of the gradient
+    q_s, stored = api.norms_direct_store(A, G)
+    assert_rel(host(q_s), ref["direct"], tol, "direct (stored)")
+    check_grad(api, inp, A, G, host(q_h), wl.C, wl.sigma, ref["Ms"], stored=stored)
 
 
 # ----------------------------------------------------------------------------- failure path
@@ -247,6 +256,28 @@ def test_hutchpp_budgets(api, k):
     # r = k // 3 head columns, m = k - 2r tail probes; k = 48 fills all 32 columns
     wl = W.Workload(160 + k, f"hpp_{k}", 2, 260, 96, 192, "bf16", 1e-2, 1.0, 1.0, k, ())
     _run_all(api, wl, paths=("hutchpp",))
+
+
+@pytest.mark.parametrize("wid", [1, 2, 170, 176])
+def test_stored_direct(api, wid):
+    # exact norms that keep every A_i^T G_i, then the clipped sum from them:
+    # fp32 with d*p not a multiple of 4 (padded per-sample blocks, ragged
+    # end), bf16 over several tiles with ragged tails; half the samples clip
+    shapes = {170: W.Workload(170, "f32_odd", 3, 37, 29, 50, "f32", 1.0, 1.0, 1.0, 7, ()),
+              176: W.Workload(176, "stored_ragged", 5, 300, 200, 328, "bf16", 1e-2, 1.0, 0.7, 8, ())}
+    wl = shapes[wid] if wid in shapes else W.get(wid)
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    ref = oracle_all(inp, want=())
+    tol = TOL[wl.dtype]
+    q, stored = api.norms_direct_store(A, G)
+    assert_rel(host(q), ref["direct"], tol, "direct (stored)")
+    # accumulate: a second layer with the same inputs doubles the sum
+    q2 = q.clone()
+    api.norms_direct_store(A, G, sqnorms=q2, accumulate=True, ws=stored.ws)
+    assert_rel(host(q2), 2 * ref["direct"], tol, "direct (stored, accumulated)")
+    C_med = float(np.median(np.sqrt(ref["direct"])))
+    check_grad(api, inp, A, G, ref["direct"], C_med, wl.sigma, ref["Ms"], offset=9, stored=stored)
 
 
 @pytest.mark.parametrize("case", ["bf16", "f32_rankdef"])
