@@ -56,9 +56,11 @@ __all__ = [
     "sqnorms_outer_bruteforce",
     "hutch_probe", "sqnorms_hutch", "hutchpp_split", "hutchpp_probes",
     "sqnorms_hutchpp", "clip_scales", "noise_matrix", "clipped_noisy_grad",
+    "STREAM_BIAS_NOISE", "per_sample_bias_grads", "bias_sqnorms", "clipped_noisy_bias_grad",
 ]
 
 STREAM_P, STREAM_S, STREAM_GP, STREAM_NOISE = 0, 1, 2, 3
+STREAM_BIAS_NOISE = 4   # the bias gradient's noise (a stream of its own)
 
 _MASK32 = np.uint64(0xFFFFFFFF)
 # PH: Philox-4x32 multipliers and the Weyl key increments (golden ratio and
@@ -315,3 +317,36 @@ def clipped_noisy_grad(A, G, q, C: float, sigma: float, seed: int, offset: int, 
     if sigma != 0.0:
         D = D + (sigma * C) * noise_matrix(D.shape[0], D.shape[1], seed, offset)
     return D, s, flags
+
+
+# ----------------------------------------------------------------------------
+# Bias of the linear layer (RC, Algorithmic flow steps 3-5 for the whole
+# per-sample gradient; GL step 3 clips the gradient of every parameter).
+# For y_t = x_t W + b the derivative of the output w.r.t. b is the identity at
+# every token, so the per-sample bias gradient sums the output gradients over
+# the sample's tokens.  It is the weight gradient of an extra input feature
+# that is 1 at every token.
+
+def per_sample_bias_grads(G: np.ndarray) -> np.ndarray:
+    """b_i = sum_t G_i[t, :] for every sample (B x p, fp64)."""
+    return G.astype(np.float64).sum(axis=1)
+
+
+def bias_sqnorms(G: np.ndarray) -> np.ndarray:
+    """||b_i||^2 per sample: the bias's share of the per-sample squared norm."""
+    b = per_sample_bias_grads(G)
+    return np.sum(b * b, axis=1)
+
+
+def clipped_noisy_bias_grad(G, q, C: float, sigma: float, seed: int, offset: int, bs=None):
+    """sum_i s_i b_i + N(0, sigma^2 C^2 I_p), the same s_i as the weights (q is
+    the per-sample squared norm of the whole gradient), noise from stream 4
+    with column c at element index c.  Returns (Db, s, flags), Db of length p."""
+    s, flags = clip_scales(q, C)
+    bs = per_sample_bias_grads(G) if bs is None else bs
+    Db = np.zeros(bs.shape[1])
+    for si, b in zip(s, bs):
+        Db = Db + si * b
+    if sigma != 0.0:
+        Db = Db + (sigma * C) * philox_normals(bs.shape[1], seed, STREAM_BIAS_NOISE, offset)
+    return Db, s, flags

@@ -320,3 +320,51 @@ def test_rademacher_hutchpp_exact_at_low_rank_and_unbiased():
     est = np.array([O.sqnorms_hutchpp(None, None, *O.hutchpp_probes(11, 6, 31, off, "f32", "rademacher"),
                                       Ms=[M])[0] for off in range(1500)])
     assert abs(est.mean() - np.sum(M * M)) < 4 * est.std(ddof=1) / math.sqrt(1500)
+
+
+# --------------------------------------------------------------- bias of the linear layer
+
+def test_bias_grad_is_the_weight_grad_of_a_constant_input():
+    # y = x W + b is y = [x, 1] [W; b]: the bias gradient is the last row of
+    # the augmented layer's weight gradient A_aug^T G
+    A, G = _tiny(B=3, T=9, d=4, p=7, seed=41)
+    ones = np.ones(A.shape[:2] + (1,))
+    A_aug = np.concatenate([A, ones], axis=2)
+    b = O.per_sample_bias_grads(G)
+    for i, M in enumerate(O.per_sample_grads(A_aug, G)):
+        np.testing.assert_allclose(b[i], M[-1], rtol=1e-13, atol=1e-13)
+    # and its squared norm is what the augmented layer adds to ||M_i||^2
+    q_aug = O.sqnorms_direct(A_aug, G)
+    np.testing.assert_allclose(q_aug, O.sqnorms_direct(A, G) + O.bias_sqnorms(G), rtol=1e-12)
+
+
+def test_bias_grad_single_token_and_linearity():
+    _, G = _tiny(B=2, T=1, d=1, p=5, seed=42)
+    np.testing.assert_array_equal(O.per_sample_bias_grads(G), G[:, 0, :])
+    _, G = _tiny(B=2, T=6, d=1, p=5, seed=43)
+    np.testing.assert_allclose(O.per_sample_bias_grads(-2.5 * G), -2.5 * O.per_sample_bias_grads(G),
+                               rtol=1e-14)
+
+
+def test_clipped_bias_grad_special_cases():
+    _, G = _tiny(B=4, T=5, d=1, p=8, seed=44)
+    q = O.bias_sqnorms(G)
+    # no clipping, no noise: the plain sum over samples and tokens
+    Db, s, flags = O.clipped_noisy_bias_grad(G, q, 1e12, 0.0, 1, 0)
+    np.testing.assert_allclose(Db, G.sum(axis=(0, 1)), rtol=1e-13)
+    assert np.all(s == 1.0) and not flags.any()
+    # clipping every sample to C: each clipped bias gradient has norm C
+    C = 0.5 * float(np.sqrt(q.min()))
+    _, s, flags = O.clipped_noisy_bias_grad(G, q, C, 0.0, 1, 0)
+    b = O.per_sample_bias_grads(G)
+    np.testing.assert_allclose(np.linalg.norm(s[:, None] * b, axis=1), C, rtol=1e-12)
+    assert flags.all()
+
+
+def test_bias_noise_is_its_own_stream():
+    _, G = _tiny(B=1, T=1, d=1, p=4096, seed=45)
+    z = O.clipped_noisy_bias_grad(0 * G, np.zeros(1), 1.0, 1.0, 77, 3)[0]
+    np.testing.assert_array_equal(z, O.philox_normals(4096, 77, O.STREAM_BIAS_NOISE, 3))
+    w = O.philox_normals(4096, 77, O.STREAM_NOISE, 3)
+    assert not np.allclose(z, w)
+    assert abs(z.mean()) < 4 / 64 and abs(z.var() - 1) < 4 * math.sqrt(2 / 4096)
