@@ -57,6 +57,7 @@ __all__ = [
     "hutch_probe", "sqnorms_hutch", "hutchpp_split", "hutchpp_probes",
     "sqnorms_hutchpp", "clip_scales", "noise_matrix", "clipped_noisy_grad",
     "STREAM_BIAS_NOISE", "per_sample_bias_grads", "bias_sqnorms", "clipped_noisy_bias_grad",
+    "sgd_update",
 ]
 
 STREAM_P, STREAM_S, STREAM_GP, STREAM_NOISE = 0, 1, 2, 3
@@ -314,6 +315,10 @@ def clipped_noisy_grad(A, G, q, C: float, sigma: float, seed: int, offset: int, 
     D = None
     for si, M in zip(s, Ms):
         D = si * M if D is None else D + si * M
+    if D is None:
+        # an empty lot (Poisson sampling can draw none, GL step 1): the sum of
+        # no clipped gradients is zero and only the noise remains
+        D = np.zeros((A.shape[2], G.shape[2]))
     if sigma != 0.0:
         D = D + (sigma * C) * noise_matrix(D.shape[0], D.shape[1], seed, offset)
     return D, s, flags
@@ -350,3 +355,15 @@ def clipped_noisy_bias_grad(G, q, C: float, sigma: float, seed: int, offset: int
     if sigma != 0.0:
         Db = Db + (sigma * C) * philox_normals(bs.shape[1], seed, STREAM_BIAS_NOISE, offset)
     return Db, s, flags
+
+
+# ----------------------------------------------------------------------------
+# Parameter update (GL step 5): theta <- theta - eta * g~ / L, g~ the noisy sum
+# of clipped per-sample gradients and L the lot size of the average.  With
+# Poisson sampling (each example joins the lot with probability L / N) the
+# drawn lot size varies from step to step and L is its expectation, so the
+# noise scale relative to the update does not depend on the draw.
+
+def sgd_update(theta: np.ndarray, g_noisy: np.ndarray, lr: float, denom: float) -> np.ndarray:
+    """theta - lr * g_noisy / denom, in fp64."""
+    return np.asarray(theta, np.float64) - (lr / denom) * np.asarray(g_noisy, np.float64)

@@ -368,3 +368,34 @@ def test_bias_noise_is_its_own_stream():
     w = O.philox_normals(4096, 77, O.STREAM_NOISE, 3)
     assert not np.allclose(z, w)
     assert abs(z.mean()) < 4 / 64 and abs(z.var() - 1) < 4 * math.sqrt(2 / 4096)
+
+
+# --------------------------------------------------------------- parameter update and Poisson lots
+
+def test_update_without_clipping_or_noise_is_sgd_on_the_lot():
+    # C -> inf, sigma = 0: theta - lr / L * (sum of per-sample gradients), and
+    # the sum of the per-sample gradients of a linear layer is one GEMM over
+    # the lot's tokens
+    A, G = _tiny(B=4, T=6, d=5, p=3, seed=51)
+    theta = _rng(52).standard_normal((5, 3))
+    q = O.sqnorms_direct(A, G)
+    D, _, _ = O.clipped_noisy_grad(A, G, q, 1e12, 0.0, 1, 0)
+    got = O.sgd_update(theta, D, 0.1, 7.0)
+    full = A.reshape(-1, 5).T @ G.reshape(-1, 3)
+    np.testing.assert_allclose(got, theta - 0.1 / 7.0 * full, rtol=1e-13, atol=1e-14)
+    np.testing.assert_array_equal(O.sgd_update(theta, D, 0.0, 7.0), theta)
+
+
+def test_empty_poisson_lot_updates_by_noise_only():
+    # a lot with no examples: the update is the noise alone, N(0, (lr sigma C / L)^2)
+    d, p = 64, 48
+    A = np.zeros((0, 5, d))
+    G = np.zeros((0, 5, p))
+    D, s, flags = O.clipped_noisy_grad(A, G, np.zeros(0), 2.0, 1.5, 9, 4)
+    assert D.shape == (d, p) and s.shape == (0,) and flags.shape == (0,)
+    theta = np.ones((d, p))
+    step = (theta - O.sgd_update(theta, D, 0.3, 10.0)) / (0.3 / 10.0 * 1.5 * 2.0)
+    n = d * p
+    assert abs(step.mean()) < 4 / math.sqrt(n) and abs(step.var() - 1) < 4 * math.sqrt(2 / n)
+    Db, _, _ = O.clipped_noisy_bias_grad(G, np.zeros(0), 2.0, 1.5, 9, 4, bs=np.zeros((0, p)))
+    assert Db.shape == (p,) and np.all(Db != 0)
