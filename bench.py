@@ -38,7 +38,7 @@ METRIC = "clip+noise tokens/s per linear layer (Hutch/Hutch++/exact); % bf16 ten
 ROWS = ("hutch", "hutchpp", "exact_direct", "exact_ghost", "clipped_noisy_grad")
 # measured after the step, not part of it: the Rademacher-probe variants
 EXTRA_ROWS = ("hutch_rademacher", "hutchpp_rademacher", "exact_direct_stored",
-              "stored_clipped_noisy_grad")
+              "stored_clipped_noisy_grad", "bias_grads", "clipped_noisy_grad_sgd")
 # kernels each ABI call launches for bf16 inputs (memsets of the control block excluded)
 LAUNCHES = {"hutch": 3, "hutchpp": 9, "exact_direct": 1, "exact_ghost": 1, "clipped_noisy_grad": 1}
 
@@ -58,6 +58,10 @@ def algorithmic_work(wl):
         # as one elementwise pass over them (read B d p fp32, write d p fp32)
         "exact_direct_stored": (2.0 * B * T * d * p, "flops", "tensor"),
         "stored_clipped_noisy_grad": (4.0 * (B + 1) * d * p, "bytes", "hbm"),
+        # per-sample bias gradients and their squared norms: one read of G
+        "bias_grads": (2.0 * B * T * p, "bytes", "hbm"),
+        # the clipped noisy gradient applied to fp32 weights in its epilogue
+        "clipped_noisy_grad_sgd": (2.0 * B * T * d * p, "flops", "tensor"),
         "exact_direct": (2.0 * B * T * d * p, "flops", "tensor"),
         "exact_ghost": (1.0 * B * T * (T + 1) * (d + p), "flops", "tensor"),
         "clipped_noisy_grad": (2.0 * B * T * d * p, "flops", "tensor"),
@@ -288,6 +292,21 @@ def main():
                 _, stored["h"] = api.norms_direct_store(b["A"], b["G"], sqnorms=b["q_d"],
                                                         ws=ensure_stored_ws())
             return call
+        if name == "bias_grads":
+            if "bias_ws" not in stored:
+                stored["bias_ws"] = ws_for(L.OP_BIAS, 0)
+                stored["bias"] = torch.empty(B, p, **f32)
+            return lambda: L.check("dpclip_bias_grads", L.lib.dpclip_bias_grads(
+                b["G"].data_ptr(), B, T, p, L.BF16, 1, b["q_d"].data_ptr(),
+                stored["bias"].data_ptr(), stored["bias_ws"].data_ptr(),
+                stored["bias_ws"].numel(), stream.cuda_stream))
+        if name == "clipped_noisy_grad_sgd":
+            if "theta" not in stored:
+                stored["theta"] = torch.zeros(d, p, **f32)
+            upd = api.SGDUpdate(stored["theta"], 1e-3, float(B), store_grad=False)
+            return lambda: api.clipped_noisy_grad(b["A"], b["G"], b["q_h"], wl.C, wl.sigma, wl.seed,
+                                                  step, scales=b["scales"], clipped=b["clipped"],
+                                                  ws=ws["clipped_noisy_grad"], update=upd)
         if name == "stored_clipped_noisy_grad":
             if "h" not in stored:
                 row_fn("exact_direct_stored", step, bufs)()

@@ -25,6 +25,7 @@ PROBE_GAUSSIAN, PROBE_RADEMACHER = 0, 1
 PROBES = {"gaussian": PROBE_GAUSSIAN, "rademacher": PROBE_RADEMACHER}
 OP_NORMS_EXACT, OP_NORMS_HUTCH, OP_NORMS_HUTCHPP, OP_CLIPPED_NOISY_GRAD = 0, 1, 2, 3
 OP_STORED_DIRECT = 4
+OP_BIAS = 5
 HUTCH_MAX_K = 32
 HUTCHPP_MAX_K = 48
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -32,6 +33,16 @@ NOALLOC_SCRATCH_BYTES = 16 << 20
 _c = ctypes
 _vp, _i, _u64, _u32, _i64, _f = _c.c_void_p, _c.c_int, _c.c_uint64, _c.c_uint32, _c.c_int64, _c.c_float
 _sz = _c.c_size_t
+
+
+
+class SgdUpdate(_c.Structure):
+    """struct dpclip_sgd_update: param -= (lr / denom) * g, in place."""
+    _fields_ = [("param", _c.c_void_p), ("lr", _c.c_float), ("denom", _c.c_float),
+                ("store_grad", _c.c_int)]
+
+
+_up = _c.POINTER(SgdUpdate)
 
 # symbol -> (restype, argtypes)
 SIGNATURES = {
@@ -47,6 +58,14 @@ SIGNATURES = {
     "dpclip_clipped_noisy_grad": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _f, _u64, _u64,
                                        _vp, _vp, _vp, _vp, _sz, _vp]),
     "dpclip_clip_scales": (_i, [_vp, _i, _f, _vp, _vp, _vp]),
+    "dpclip_clipped_noisy_grad_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _f, _u64, _u64,
+                                          _vp, _vp, _vp, _up, _vp, _sz, _vp]),
+    "dpclip_stored_clipped_noisy_grad_ex": (_i, [_i, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _vp,
+                                                 _vp, _up, _vp, _sz, _vp]),
+    "dpclip_clipped_noisy_bias_grad_ex": (_i, [_vp, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _up,
+                                               _vp]),
+    "dpclip_bias_grads": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "dpclip_clipped_noisy_bias_grad": (_i, [_vp, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _vp]),
     "dpclip_norms_direct_store": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "dpclip_stored_clipped_noisy_grad": (_i, [_i, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _vp, _vp,
                                               _vp, _sz, _vp]),

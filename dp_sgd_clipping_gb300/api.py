@@ -7,12 +7,15 @@ step of the computation runs in libdpclip's kernels.
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _lib as L
 
 __all__ = ["norms_exact", "norms_hutch", "norms_hutchpp", "clipped_noisy_grad", "clip_scales",
            "norms_direct_store", "stored_clipped_noisy_grad", "StoredGradients",
+           "bias_grads", "clipped_noisy_bias_grad", "SGDUpdate",
            "philox_normal", "philox_rademacher", "workspace_bytes", "workspace_status",
            "selftest_wait_timeout"]
 
@@ -84,23 +87,48 @@ def norms_hutchpp(A, G, k: int, seed: int, offset: int = 0, out=None, ws=None, s
     return out
 
 
+class SGDUpdate:
+    """A parameter update fused into a gradient call: param -= (lr / denom) g,
+    in place.  param is the layer's fp32 tensor in the gradient's layout
+    ([d, p] weights or [p] bias); denom is the lot size L of the average (its
+    expectation for Poisson-sampled lots).  store_grad=False skips writing g."""
+
+    def __init__(self, param, lr: float, denom: float, store_grad: bool = True):
+        if param.dtype != torch.float32 or not param.is_cuda or not param.is_contiguous():
+            raise ValueError("param must be a contiguous CUDA float32 tensor")
+        self.param, self.lr, self.denom, self.store_grad = param, lr, denom, store_grad
+
+    def _c(self):
+        return L.SgdUpdate(self.param.data_ptr(), float(self.lr), float(self.denom),
+                           int(bool(self.store_grad)))
+
+
+def _upd(update):
+    return None if update is None else ctypes.pointer(update._c())
+
+
 def clipped_noisy_grad(A, G, sqnorms, C: float, sigma: float, seed: int, offset: int = 0,
                        grad=None, scales=None, clipped=None, ws=None, stream=None,
-                       want_scales: bool = True):
-    """Returns (grad [d, p] fp32, scales [B] fp32, clipped [B] uint8)."""
+                       want_scales: bool = True, update: SGDUpdate = None):
+    """Returns (grad [d, p] fp32, scales [B] fp32, clipped [B] uint8); with
+    `update`, also applies it.  A lot of B = 0 samples ([0, T, d] tensors)
+    gives the noise alone."""
     B, T, d, p, dt = _check_pair(A, G)
-    if sqnorms.dtype != torch.float32 or sqnorms.numel() != B or not sqnorms.is_cuda:
+    if B > 0 and (sqnorms.dtype != torch.float32 or sqnorms.numel() != B or not sqnorms.is_cuda):
         raise ValueError("sqnorms must be a CUDA float32 tensor of B entries")
-    nb = workspace_bytes(L.OP_CLIPPED_NOISY_GRAD, B, T, d, p, dt, 0)
+    nb = workspace_bytes(L.OP_CLIPPED_NOISY_GRAD, max(B, 1), T, d, p, dt, 0)
     ws = _workspace(nb, A.device, ws)
-    grad = torch.empty(d, p, dtype=torch.float32, device=A.device) if grad is None else grad
+    if grad is None and (update is None or update.store_grad or dt == L.F32):
+        grad = torch.empty(d, p, dtype=torch.float32, device=A.device)
     if want_scales:
         scales = torch.empty(B, dtype=torch.float32, device=A.device) if scales is None else scales
         clipped = torch.empty(B, dtype=torch.uint8, device=A.device) if clipped is None else clipped
-    L.check("dpclip_clipped_noisy_grad", L.lib.dpclip_clipped_noisy_grad(
-        A.data_ptr(), G.data_ptr(), B, T, d, p, dt, sqnorms.data_ptr(), float(C), float(sigma),
-        seed, offset, grad.data_ptr(), scales.data_ptr() if scales is not None else None,
-        clipped.data_ptr() if clipped is not None else None, ws.data_ptr(),
+    L.check("dpclip_clipped_noisy_grad_ex", L.lib.dpclip_clipped_noisy_grad_ex(
+        A.data_ptr() if B else None, G.data_ptr() if B else None, B, T, d, p, dt,
+        sqnorms.data_ptr() if B else None, float(C), float(sigma), seed, offset,
+        grad.data_ptr() if grad is not None else None,
+        scales.data_ptr() if scales is not None and B else None,
+        clipped.data_ptr() if clipped is not None and B else None, _upd(update), ws.data_ptr(),
         ws.numel() * ws.element_size(), _stream(stream)))
     return grad, scales, clipped
 
@@ -134,23 +162,62 @@ def norms_direct_store(A, G, sqnorms=None, accumulate: bool = False, ws=None, st
 
 def stored_clipped_noisy_grad(stored: StoredGradients, sqnorms, C: float, sigma: float, seed: int,
                               offset: int = 0, grad=None, scales=None, clipped=None, stream=None,
-                              want_scales: bool = True):
+                              want_scales: bool = True, update: SGDUpdate = None):
     """clipped_noisy_grad from the per-sample gradients kept by norms_direct_store.
 
     Returns (grad [d, p] fp32, scales [B] fp32, clipped [B] uint8)."""
     B, d, p, ws = stored.B, stored.d, stored.p, stored.ws
     if sqnorms.dtype != torch.float32 or sqnorms.numel() != B or not sqnorms.is_cuda:
         raise ValueError("sqnorms must be a CUDA float32 tensor of B entries")
-    grad = torch.empty(d, p, dtype=torch.float32, device=ws.device) if grad is None else grad
+    if grad is None and (update is None or update.store_grad):
+        grad = torch.empty(d, p, dtype=torch.float32, device=ws.device)
     if want_scales:
         scales = torch.empty(B, dtype=torch.float32, device=ws.device) if scales is None else scales
         clipped = torch.empty(B, dtype=torch.uint8, device=ws.device) if clipped is None else clipped
-    L.check("dpclip_stored_clipped_noisy_grad", L.lib.dpclip_stored_clipped_noisy_grad(
-        B, d, p, sqnorms.data_ptr(), float(C), float(sigma), seed, offset, grad.data_ptr(),
+    L.check("dpclip_stored_clipped_noisy_grad_ex", L.lib.dpclip_stored_clipped_noisy_grad_ex(
+        B, d, p, sqnorms.data_ptr(), float(C), float(sigma), seed, offset,
+        grad.data_ptr() if grad is not None else None,
         scales.data_ptr() if scales is not None else None,
-        clipped.data_ptr() if clipped is not None else None, ws.data_ptr(),
+        clipped.data_ptr() if clipped is not None else None, _upd(update), ws.data_ptr(),
         ws.numel() * ws.element_size(), _stream(stream)))
     return grad, scales, clipped
+
+
+def bias_grads(G, sqnorms=None, accumulate: bool = False, want_grads: bool = True, ws=None,
+               stream=None):
+    """Per-sample bias gradients b_i = sum_t G_i[t, :] and their squared norms.
+
+    Returns (sqnorms [B], bias_grads [B, p] or None).  accumulate=True adds
+    ||b_i||^2 to the given sqnorms (e.g. the weights' norms of the layer)."""
+    if not G.is_cuda or G.dim() != 3 or G.dtype not in _DT or not G.is_contiguous():
+        raise ValueError("G must be a contiguous CUDA [B, T, p] float32 or bfloat16 tensor")
+    B, T, p = G.shape
+    nb = workspace_bytes(L.OP_BIAS, B, T, 0, p, _DT[G.dtype], 0)
+    ws = _workspace(nb, G.device, ws)
+    if sqnorms is None:
+        if accumulate:
+            raise ValueError("accumulate needs the sqnorms tensor to add to")
+        sqnorms = torch.empty(B, dtype=torch.float32, device=G.device)
+    bg = torch.empty(B, p, dtype=torch.float32, device=G.device) if want_grads else None
+    L.check("dpclip_bias_grads", L.lib.dpclip_bias_grads(
+        G.data_ptr(), B, T, p, _DT[G.dtype], int(bool(accumulate)), sqnorms.data_ptr(),
+        bg.data_ptr() if bg is not None else None, ws.data_ptr(), ws.numel() * ws.element_size(),
+        _stream(stream)))
+    return sqnorms, bg
+
+
+def clipped_noisy_bias_grad(bias_grads, sqnorms, C: float, sigma: float, seed: int, offset: int = 0,
+                            out=None, stream=None, update: SGDUpdate = None):
+    """sum_i s_i b_i + sigma C z (z: Philox stream 4), fp32 [p]; with
+    `update`, also applies it.  bias_grads of shape [0, p]: the noise alone."""
+    B, p = bias_grads.shape
+    if out is None and (update is None or update.store_grad):
+        out = torch.empty(p, dtype=torch.float32, device=bias_grads.device)
+    L.check("dpclip_clipped_noisy_bias_grad_ex", L.lib.dpclip_clipped_noisy_bias_grad_ex(
+        bias_grads.data_ptr() if B else None, B, p, sqnorms.data_ptr() if B else None, float(C),
+        float(sigma), seed, offset, out.data_ptr() if out is not None else None, _upd(update),
+        _stream(stream)))
+    return out
 
 
 def clip_scales(sqnorms, C: float, stream=None):

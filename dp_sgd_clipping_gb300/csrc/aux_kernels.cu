@@ -93,7 +93,7 @@ __global__ void finalize_norms_kernel(const float* part, int nunits, long long s
 __global__ void stored_grad_kernel(const float* __restrict__ M, int B, long long n,
                                    long long stride, const float* sq, float C, float nscale,
                                    uint64_t seed, uint64_t offset, float* grad, float* scales,
-                                   uint8_t* clipped) {
+                                   uint8_t* clipped, float* param, float upd_scale) {
   extern __shared__ float s_sh[];
   pdl_trigger();
   pdl_wait();
@@ -142,13 +142,57 @@ __global__ void stored_grad_kernel(const float* __restrict__ M, int B, long long
       acc.z = fmaf(nscale, z[2], acc.z);
       acc.w = fmaf(nscale, z[3], acc.w);
     }
+    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
     if (4 * b + 3 < n) {
-      reinterpret_cast<float4*>(grad)[b] = acc;
+      if (grad) reinterpret_cast<float4*>(grad)[b] = acc;
+      if (param) {   // the fused parameter update: theta -= (lr / L) g
+        float4 w = reinterpret_cast<const float4*>(param)[b];
+        w.x = fmaf(-upd_scale, acc.x, w.x);
+        w.y = fmaf(-upd_scale, acc.y, w.y);
+        w.z = fmaf(-upd_scale, acc.z, w.z);
+        w.w = fmaf(-upd_scale, acc.w, w.w);
+        reinterpret_cast<float4*>(param)[b] = w;
+      }
     } else {   // ragged end: lanes past n hold padding and are not stored
-      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-      for (int l = 0; 4 * b + l < n; ++l) grad[4 * b + l] = a4[l];
+      for (int l = 0; 4 * b + l < n; ++l) {
+        if (grad) grad[4 * b + l] = a4[l];
+        if (param) param[4 * b + l] = fmaf(-upd_scale, a4[l], param[4 * b + l]);
+      }
     }
   }
+}
+
+// An empty lot (no samples): g = nscale z from Philox stream `stream_id`
+// (element e), stored to grad and / or applied as param -= upd_scale g.
+__global__ void noise_only_kernel(float* grad, float* param, long long n, float nscale,
+                                  float upd_scale, uint64_t seed, uint32_t stream_id,
+                                  uint64_t offset) {
+  pdl_trigger();
+  pdl_wait();
+  const long long nblk = (n + 3) / 4;
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblk;
+       b += (long long)gridDim.x * blockDim.x) {
+    float z[4] = {0.f, 0.f, 0.f, 0.f};
+    if (nscale != 0.f) philox_normal4(seed, stream_id, offset, (uint32_t)b, z);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const long long e = 4 * b + l;
+      if (e < n) {
+        const float g = nscale * z[l];
+        if (grad) grad[e] = g;
+        if (param) param[e] = fmaf(-upd_scale, g, param[e]);
+      }
+    }
+  }
+}
+
+// param[e] -= scale * grad[e] (the update of the fp32 gradient path).
+__global__ void sgd_update_kernel(float* param, const float* grad, long long n, float scale) {
+  pdl_trigger();
+  pdl_wait();
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n;
+       e += (long long)gridDim.x * blockDim.x)
+    param[e] = fmaf(-scale, grad[e], param[e]);
 }
 
 // part[i * nblk + b] = sum of squares of elements [b c, (b + 1) c) of sample i
@@ -241,13 +285,33 @@ cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long lon
 cudaError_t launch_stored_grad(const float* M, int B, long long n, long long stride,
                                const float* sq, float C, float nscale, uint64_t seed,
                                uint64_t offset, float* grad, float* scales, uint8_t* clipped,
-                               cudaStream_t s) {
+                               float* param, float upd_scale, cudaStream_t s) {
   const long long nb = (n + 3) / 4;
   const int threads = 256;
   const int grid = (int)std::max<long long>(1, std::min<long long>((nb + threads - 1) / threads,
                                                                    152 * 8));
   return launch_pdl(stored_grad_kernel, dim3(grid), dim3(threads), (size_t)B * sizeof(float), s,
-                    0, M, B, n, stride, sq, C, nscale, seed, offset, grad, scales, clipped);
+                    0, M, B, n, stride, sq, C, nscale, seed, offset, grad, scales, clipped, param,
+                    upd_scale);
+}
+
+cudaError_t launch_noise_only(float* grad, float* param, long long n, float nscale,
+                              float upd_scale, uint64_t seed, uint32_t stream_id, uint64_t offset,
+                              cudaStream_t s) {
+  const long long nblk = (n + 3) / 4;
+  const int threads = 256;
+  const int grid = (int)std::max<long long>(1, std::min<long long>((nblk + threads - 1) / threads,
+                                                                   152 * 8));
+  return launch_pdl(noise_only_kernel, dim3(grid), dim3(threads), 0, s, 0, grad, param, n, nscale,
+                    upd_scale, seed, stream_id, offset);
+}
+
+cudaError_t launch_sgd_update(float* param, const float* grad, long long n, float scale,
+                              cudaStream_t s) {
+  const int threads = 256;
+  const int grid = (int)std::max<long long>(1, std::min<long long>((n + threads - 1) / threads,
+                                                                   152 * 8));
+  return launch_pdl(sgd_update_kernel, dim3(grid), dim3(threads), 0, s, 0, param, grad, n, scale);
 }
 
 cudaError_t launch_stored_sqnorm(const float* M, int B, long long n, long long stride, int nblk,

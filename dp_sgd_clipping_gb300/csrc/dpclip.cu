@@ -336,6 +336,13 @@ int plan_for(int op, int B, int T, int d, int p, int dtype, int param, Plan& pl)
     case DPCLIP_OP_STORED_DIRECT:
       pl = plan_stored(B, d, p, dtype);
       return DPCLIP_OK;
+    case DPCLIP_OP_BIAS: {
+      Carve c;
+      pl.ctrl_bytes = 0;
+      pl.off[0] = c.take(bias_part_floats(B, T, p) * 4);
+      pl.total = c.total();
+      return DPCLIP_OK;
+    }
     default:
       return DPCLIP_ERR_INVALID_ARG;
   }
@@ -461,7 +468,7 @@ const char* dpclip_status_string(int status) {
 
 int dpclip_workspace_size(int op, int B, int T, int d, int p, int dtype, int param, size_t* bytes) {
   if (!bytes) return DPCLIP_ERR_INVALID_ARG;
-  if (B <= 0 || T <= 0 || d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || p <= 0 || (d <= 0 && op != DPCLIP_OP_BIAS)) return DPCLIP_ERR_INVALID_ARG;
   if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
   Plan pl;
   DPCLIP_TRY(plan_for(op, B, T, d, p, dtype, param, pl));
@@ -776,18 +783,52 @@ int dpclip_norms_hutchpp(const void* A, const void* G, int B, int T, int d, int 
                                  sqnorms, ws, ws_bytes, stream);
 }
 
-int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d, int p, int dtype,
-                              const float* sqnorms, float C, float sigma, uint64_t seed,
-                              uint64_t offset, float* grad, float* scales, uint8_t* clipped,
-                              void* ws, size_t ws_bytes, dpclip_stream_t stream) {
-  DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
-  if (!sqnorms || !grad) return DPCLIP_ERR_INVALID_ARG;
+namespace dpclip {
+namespace {
+// Checks an optional update; *scale = lr / denom.  Returns a status.
+int check_update(const dpclip_sgd_update* u, float* scale) {
+  *scale = 0.f;
+  if (!u) return DPCLIP_OK;
+  if (!u->param || (u->store_grad != 0 && u->store_grad != 1)) return DPCLIP_ERR_INVALID_ARG;
+  if (!std::isfinite(u->lr) || !(u->denom > 0.f) || !std::isfinite(u->denom))
+    return DPCLIP_ERR_INVALID_ARG;
+  *scale = u->lr / u->denom;
+  return DPCLIP_OK;
+}
+bool writes_grad(const dpclip_sgd_update* u) { return !u || u->store_grad; }
+int check_noise_args(float C, float sigma) {
   if (!(C > 0.f) || !std::isfinite(C)) return DPCLIP_ERR_INVALID_ARG;
   if (!(sigma >= 0.f) || !std::isfinite(sigma)) return DPCLIP_ERR_INVALID_ARG;
-  if (!aligned(grad, dtype == DPCLIP_BF16 ? 16 : 4)) return DPCLIP_ERR_UNSUPPORTED;
+  return DPCLIP_OK;
+}
+}  // namespace
+}  // namespace dpclip
+
+int dpclip_clipped_noisy_grad_ex(const void* A, const void* G, int B, int T, int d, int p,
+                                 int dtype, const float* sqnorms, float C, float sigma,
+                                 uint64_t seed, uint64_t offset, float* grad, float* scales,
+                                 uint8_t* clipped, const dpclip_sgd_update* update, void* ws,
+                                 size_t ws_bytes, dpclip_stream_t stream) {
+  float upd_scale;
+  DPCLIP_TRY(check_update(update, &upd_scale));
+  DPCLIP_TRY(check_noise_args(C, sigma));
+  if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
+  const bool need_grad = writes_grad(update) || dtype == DPCLIP_F32;
+  if (need_grad && !grad) return DPCLIP_ERR_INVALID_ARG;
+  float* param = update ? update->param : nullptr;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (B == 0) {   // an empty lot: the noise alone
+    if (d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+    DPCLIP_CUDA(launch_noise_only(writes_grad(update) ? grad : nullptr, param, (long long)d * p,
+                                  sigma * C, upd_scale, seed, 3u, offset, s));
+    return DPCLIP_OK;
+  }
+  DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
+  if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
+  if (grad && !aligned(grad, dtype == DPCLIP_BF16 ? 16 : 4)) return DPCLIP_ERR_UNSUPPORTED;
+  if (param && !aligned(param, dtype == DPCLIP_BF16 ? 16 : 4)) return DPCLIP_ERR_UNSUPPORTED;
   Plan pl = plan_grad(d, p, dtype);
   DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
-  cudaStream_t s = (cudaStream_t)stream;
   DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
   if (dtype == DPCLIP_BF16) {
     GemmDpParams gp;
@@ -806,9 +847,11 @@ int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d,
     gp.sigma = sigma;
     gp.seed = seed;
     gp.offset = offset;
-    gp.grad = grad;
+    gp.grad = writes_grad(update) ? grad : nullptr;
     gp.scales = scales;
     gp.clipped = clipped;
+    gp.upd_param = param;
+    gp.upd_scale = upd_scale;
     gp.err = at<uint32_t>(ws, pl.ctrl);
     gp.tickets = at<uint32_t>(ws, pl.ctrl + 4);
     gp.slots = at<float>(ws, pl.off[0]);
@@ -831,7 +874,16 @@ int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d,
   if (sigma > 0.f)
     DPCLIP_CUDA(launch_noise_add(grad, (long long)d * p, sigma * C, seed, offset, s));
   if (scales || clipped) DPCLIP_CUDA(launch_clip_scales(sqnorms, B, C, scales, clipped, s));
+  if (param) DPCLIP_CUDA(launch_sgd_update(param, grad, (long long)d * p, upd_scale, s));
   return DPCLIP_OK;
+}
+
+int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+                              const float* sqnorms, float C, float sigma, uint64_t seed,
+                              uint64_t offset, float* grad, float* scales, uint8_t* clipped,
+                              void* ws, size_t ws_bytes, dpclip_stream_t stream) {
+  return dpclip_clipped_noisy_grad_ex(A, G, B, T, d, p, dtype, sqnorms, C, sigma, seed, offset,
+                                      grad, scales, clipped, nullptr, ws, ws_bytes, stream);
 }
 
 int dpclip_norms_direct_store(const void* A, const void* G, int B, int T, int d, int p, int dtype,
@@ -881,20 +933,90 @@ int dpclip_norms_direct_store(const void* A, const void* G, int B, int T, int d,
   return DPCLIP_OK;
 }
 
-int dpclip_stored_clipped_noisy_grad(int B, int d, int p, const float* sqnorms, float C,
-                                     float sigma, uint64_t seed, uint64_t offset, float* grad,
-                                     float* scales, uint8_t* clipped, const void* ws,
-                                     size_t ws_bytes, dpclip_stream_t stream) {
-  if (B <= 0 || d <= 0 || p <= 0 || !sqnorms || !grad) return DPCLIP_ERR_INVALID_ARG;
-  if (!(C > 0.f) || !std::isfinite(C)) return DPCLIP_ERR_INVALID_ARG;
-  if (!(sigma >= 0.f) || !std::isfinite(sigma)) return DPCLIP_ERR_INVALID_ARG;
-  if (!aligned(grad, 16) || B > kMaxStoredB) return DPCLIP_ERR_UNSUPPORTED;
+int dpclip_stored_clipped_noisy_grad_ex(int B, int d, int p, const float* sqnorms, float C,
+                                        float sigma, uint64_t seed, uint64_t offset, float* grad,
+                                        float* scales, uint8_t* clipped,
+                                        const dpclip_sgd_update* update, const void* ws,
+                                        size_t ws_bytes, dpclip_stream_t stream) {
+  float upd_scale;
+  DPCLIP_TRY(check_update(update, &upd_scale));
+  DPCLIP_TRY(check_noise_args(C, sigma));
+  if (B < 0 || d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  float* g = writes_grad(update) ? grad : nullptr;
+  float* param = update ? update->param : nullptr;
+  if (writes_grad(update) && !grad) return DPCLIP_ERR_INVALID_ARG;
+  if ((g && !aligned(g, 16)) || (param && !aligned(param, 16)) || B > kMaxStoredB)
+    return DPCLIP_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (B == 0) {
+    DPCLIP_CUDA(launch_noise_only(g, param, (long long)d * p, sigma * C, upd_scale, seed, 3u,
+                                  offset, s));
+    return DPCLIP_OK;
+  }
+  if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
   const long long stride = (long long)stored_stride(d, p);
   DPCLIP_TRY(check_ws(ws, ws_bytes, kAlign + (size_t)B * stride * 4));
   const float* M = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + kAlign);
   DPCLIP_CUDA(launch_stored_grad(M, B, (long long)d * p, stride, sqnorms, C, sigma * C, seed,
-                                 offset, grad, scales, clipped, (cudaStream_t)stream));
+                                 offset, g, scales, clipped, param, upd_scale, s));
   return DPCLIP_OK;
+}
+
+int dpclip_stored_clipped_noisy_grad(int B, int d, int p, const float* sqnorms, float C,
+                                     float sigma, uint64_t seed, uint64_t offset, float* grad,
+                                     float* scales, uint8_t* clipped, const void* ws,
+                                     size_t ws_bytes, dpclip_stream_t stream) {
+  if (B <= 0) return DPCLIP_ERR_INVALID_ARG;
+  return dpclip_stored_clipped_noisy_grad_ex(B, d, p, sqnorms, C, sigma, seed, offset, grad,
+                                             scales, clipped, nullptr, ws, ws_bytes, stream);
+}
+
+int dpclip_bias_grads(const void* G, int B, int T, int p, int dtype, int accumulate,
+                      float* sqnorms, float* bias_grads, void* ws, size_t ws_bytes,
+                      dpclip_stream_t stream) {
+  if (!G || B <= 0 || T <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return DPCLIP_ERR_INVALID_ARG;
+  if (!sqnorms && !bias_grads) return DPCLIP_ERR_INVALID_ARG;
+  if (dtype == DPCLIP_BF16 && (p % 8 != 0 || !aligned(G, 16))) return DPCLIP_ERR_UNSUPPORTED;
+  if (dtype == DPCLIP_F32 && !aligned(G, 4)) return DPCLIP_ERR_UNSUPPORTED;
+  Plan pl;
+  DPCLIP_TRY(plan_for(DPCLIP_OP_BIAS, B, T, 1, p, dtype, 0, pl));
+  DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
+  DPCLIP_CUDA(launch_bias_grads(G, dtype == DPCLIP_BF16, B, T, p, at<float>(ws, pl.off[0]),
+                                bias_grads, sqnorms, accumulate, (cudaStream_t)stream));
+  return DPCLIP_OK;
+}
+
+int dpclip_clipped_noisy_bias_grad_ex(const float* bias_grads, int B, int p, const float* sqnorms,
+                                      float C, float sigma, uint64_t seed, uint64_t offset,
+                                      float* grad_b, const dpclip_sgd_update* update,
+                                      dpclip_stream_t stream) {
+  float upd_scale;
+  DPCLIP_TRY(check_update(update, &upd_scale));
+  DPCLIP_TRY(check_noise_args(C, sigma));
+  if (B < 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  float* g = writes_grad(update) ? grad_b : nullptr;
+  float* param = update ? update->param : nullptr;
+  if (writes_grad(update) && !grad_b) return DPCLIP_ERR_INVALID_ARG;
+  if (B > kMaxStoredB) return DPCLIP_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (B == 0) {
+    DPCLIP_CUDA(launch_noise_only(g, param, p, sigma * C, upd_scale, seed, 4u, offset, s));
+    return DPCLIP_OK;
+  }
+  if (!bias_grads || !sqnorms) return DPCLIP_ERR_INVALID_ARG;
+  DPCLIP_CUDA(launch_bias_clip(bias_grads, B, p, sqnorms, C, sigma * C, seed, offset, g, param,
+                               upd_scale, s));
+  return DPCLIP_OK;
+}
+
+int dpclip_clipped_noisy_bias_grad(const float* bias_grads, int B, int p, const float* sqnorms,
+                                   float C, float sigma, uint64_t seed, uint64_t offset,
+                                   float* grad_b, dpclip_stream_t stream) {
+  if (B <= 0) return DPCLIP_ERR_INVALID_ARG;
+  return dpclip_clipped_noisy_bias_grad_ex(bias_grads, B, p, sqnorms, C, sigma, seed, offset,
+                                           grad_b, nullptr, stream);
 }
 
 int dpclip_workspace_status(const void* ws, dpclip_stream_t stream) {

@@ -187,7 +187,8 @@ __device__ __forceinline__ void store_with_noise(const GemmDpParams& p, int r, i
                                                  const float (&tot)[128]) {
   if (r >= p.d) return;
   const float nscale = p.sigma * p.C;
-  float* rowp = p.grad + (size_t)r * p.p;
+  float* rowp = p.grad ? p.grad + (size_t)r * p.p : nullptr;
+  float* wrow = p.upd_param ? p.upd_param + (size_t)r * p.p : nullptr;
 #pragma unroll
   for (int jb = 0; jb < 32; ++jb) {
     const int c = cb + 4 * jb;
@@ -201,7 +202,16 @@ __device__ __forceinline__ void store_with_noise(const GemmDpParams& p, int r, i
         o.z = fmaf(nscale, z.z, o.z);
         o.w = fmaf(nscale, z.w, o.w);
       }
-      *reinterpret_cast<float4*>(rowp + c) = o;
+      if (rowp) *reinterpret_cast<float4*>(rowp + c) = o;
+      if (wrow) {
+        // the fused parameter update: theta -= (lr / L) g
+        float4 w = *reinterpret_cast<const float4*>(wrow + c);
+        w.x = fmaf(-p.upd_scale, o.x, w.x);
+        w.y = fmaf(-p.upd_scale, o.y, w.y);
+        w.z = fmaf(-p.upd_scale, o.z, w.z);
+        w.w = fmaf(-p.upd_scale, o.w, w.w);
+        *reinterpret_cast<float4*>(wrow + c) = w;
+      }
     }
   }
 }

@@ -116,6 +116,8 @@ struct GemmDpParams {
   uint32_t* err;
   float* pstore;         // norm mode: if set, every tile A_i^T G_i also goes to [B][d][p]
   int accumulate;        // norm mode: sq[i] += the estimate (else =)
+  float* upd_param;      // grad mode: if set, upd_param -= upd_scale * grad (grad may be null)
+  float upd_scale;
 };
 
 // ghost: per sample i and token tiles a <= b, sum((A_a A_b^T) o (G_a G_b^T)),
@@ -202,7 +204,24 @@ constexpr int kMaxStoredB = 12288;
 cudaError_t launch_stored_grad(const float* M, int B, long long n, long long stride,
                                const float* sq, float C, float nscale, uint64_t seed,
                                uint64_t offset, float* grad, float* scales, uint8_t* clipped,
-                               cudaStream_t s);
+                               float* param, float upd_scale, cudaStream_t s);
+// grad (may be null) = nscale z (stream_id, element e), param (may be null)
+// -= upd_scale * that, e < n: the gradient of an empty lot.
+cudaError_t launch_noise_only(float* grad, float* param, long long n, float nscale,
+                              float upd_scale, uint64_t seed, uint32_t stream_id, uint64_t offset,
+                              cudaStream_t s);
+// param[e] -= scale * grad[e], e < n.
+cudaError_t launch_sgd_update(float* param, const float* grad, long long n, float scale,
+                              cudaStream_t s);
+// Bias of the linear layer: bias[i][c] = sum_t G_i[t][c] (bias may be null),
+// sq[i] (+)= ||bias_i||^2 (sq may be null); part holds bias_part_floats
+// floats.  bias_clip: grad_b = sum_i s_i bias_i + nscale z (Philox stream 4).
+size_t bias_part_floats(int B, int T, int p);
+cudaError_t launch_bias_grads(const void* G, bool bf16, int B, int T, int p, float* part,
+                              float* bias, float* sq, int accumulate, cudaStream_t s);
+cudaError_t launch_bias_clip(const float* bias, int B, int p, const float* sq, float C, float nscale,
+                             uint64_t seed, uint64_t offset, float* grad_b, float* param,
+                             float upd_scale, cudaStream_t s);
 // part[i * nblk + b] = sum of squares of chunk b of M_i (n elements at M + i * stride).
 cudaError_t launch_stored_sqnorm(const float* M, int B, long long n, long long stride, int nblk,
                                  float* part, cudaStream_t s);

@@ -87,7 +87,8 @@ enum dpclip_op {
   DPCLIP_OP_NORMS_HUTCH = 1,
   DPCLIP_OP_NORMS_HUTCHPP = 2,
   DPCLIP_OP_CLIPPED_NOISY_GRAD = 3,
-  DPCLIP_OP_STORED_DIRECT = 4    /* dpclip_norms_direct_store + dpclip_stored_clipped_noisy_grad */
+  DPCLIP_OP_STORED_DIRECT = 4,   /* dpclip_norms_direct_store + dpclip_stored_clipped_noisy_grad */
+  DPCLIP_OP_BIAS = 5             /* dpclip_bias_grads (d and param ignored) */
 };
 
 /* Largest probe count k for Hutch (k <= 32) and Hutch++ (k - floor(k/3) <= 32). */
@@ -174,6 +175,63 @@ int dpclip_stored_clipped_noisy_grad(int B, int d, int p, const float* sqnorms, 
                                      float sigma, uint64_t seed, uint64_t offset, float* grad,
                                      float* scales, uint8_t* clipped, const void* ws,
                                      size_t ws_bytes, dpclip_stream_t stream);
+
+/* Per-sample gradients of the bias of a linear layer y_t = x_t W + b: the
+ * derivative of y_t with respect to b is the identity, so
+ * bias_grads[i][c] = sum_t G_i[t][c] (fp32 [B][p], device, may be NULL), and
+ * the bias's share of the per-sample squared norm ("DP-SGD algorithm" step 3
+ * clips the gradient of every parameter): sqnorms[i] = ||b_i||^2
+ * (accumulate = 0) or sqnorms[i] += ||b_i||^2 (accumulate = 1; sqnorms may be
+ * NULL).  G as for the norms ([B][T][p], bf16 or fp32).  Reads G once.
+ * Workspace: dpclip_workspace_size(DPCLIP_OP_BIAS, B, T, 0, p, dtype, 0). */
+int dpclip_bias_grads(const void* G, int B, int T, int p, int dtype, int accumulate,
+                      float* sqnorms, float* bias_grads, void* ws, size_t ws_bytes,
+                      dpclip_stream_t stream);
+
+/* Clipped noisy bias gradient: s_i = min(1, C / sqrt(sqnorms[i])) (1 when 0),
+ * grad_b[c] = sum_i s_i bias_grads[i][c] + sigma * C * z_c with z from Philox
+ * stream 4 at element c (its own stream: the weight noise is stream 3).
+ * sqnorms should be the whole per-sample squared norm (weights and bias).
+ * bias_grads as written by dpclip_bias_grads; grad_b fp32 [p].  B <= 12288. */
+int dpclip_clipped_noisy_bias_grad(const float* bias_grads, int B, int p, const float* sqnorms,
+                                   float C, float sigma, uint64_t seed, uint64_t offset,
+                                   float* grad_b, dpclip_stream_t stream);
+
+/* Parameter update fused into the gradient calls ("DP-SGD algorithm" step 5:
+ * theta <- theta - eta * g / L, g the noisy clipped sum).  `param` is the
+ * layer's fp32 parameter tensor in the gradient's layout ([d][p] weights or
+ * [p] bias, device, 16-byte aligned for the weights); it is updated in place
+ * as param -= (lr / denom) * g.  denom is the lot size L of the average: the
+ * drawn lot size, or its expectation when the lot is Poisson sampled (then
+ * the drawn B varies per step, may be 0, and the update's noise scale stays
+ * sigma C lr / L).  store_grad = 0 skips writing g itself (grad may then be
+ * NULL on the bf16 paths). */
+typedef struct dpclip_sgd_update {
+  float* param;
+  float lr;
+  float denom;
+  int store_grad;
+} dpclip_sgd_update;
+
+/* dpclip_clipped_noisy_grad, dpclip_stored_clipped_noisy_grad and
+ * dpclip_clipped_noisy_bias_grad with an optional fused update (NULL: none)
+ * and with B = 0 accepted (an empty lot: A, G, sqnorms and the stored
+ * gradients are not read, g = sigma C z).  fp32 inputs need `grad` even with
+ * store_grad = 0 (it is the scratch of the update). */
+int dpclip_clipped_noisy_grad_ex(const void* A, const void* G, int B, int T, int d, int p,
+                                 int dtype, const float* sqnorms, float C, float sigma,
+                                 uint64_t seed, uint64_t offset, float* grad, float* scales,
+                                 uint8_t* clipped, const dpclip_sgd_update* update, void* ws,
+                                 size_t ws_bytes, dpclip_stream_t stream);
+int dpclip_stored_clipped_noisy_grad_ex(int B, int d, int p, const float* sqnorms, float C,
+                                        float sigma, uint64_t seed, uint64_t offset, float* grad,
+                                        float* scales, uint8_t* clipped,
+                                        const dpclip_sgd_update* update, const void* ws,
+                                        size_t ws_bytes, dpclip_stream_t stream);
+int dpclip_clipped_noisy_bias_grad_ex(const float* bias_grads, int B, int p, const float* sqnorms,
+                                      float C, float sigma, uint64_t seed, uint64_t offset,
+                                      float* grad_b, const dpclip_sgd_update* update,
+                                      dpclip_stream_t stream);
 
 /* Clip scales alone: scales[i] = min(1, C / sqrt(sqnorms[i])) (1 when the norm
  * is 0) and clipped[i] = sqrt(sqnorms[i]) > C; either output may be NULL. */

@@ -60,6 +60,8 @@ def test_workspace_sizes(L):
     st = ws(L.OP_STORED_DIRECT, 4, 4096, 2048, 8192, L.BF16, 0)
     assert 256 + 4 * 2048 * 8192 * 4 < st < 256 + 4 * 2048 * 8192 * 4 + (1 << 20)
     assert ws(L.OP_STORED_DIRECT, 3, 37, 29, 50, L.F32, 0) >= 256 + 3 * 1452 * 4
+    # bias: per (sample, 512-token chunk) column sums
+    assert ws(L.OP_BIAS, 4, 4096, 0, 8192, L.BF16, 0) == (4 * 8 * 8192 + 4 * 32) * 4
 
 
 def test_workspace_size_rejects(L):
@@ -128,6 +130,16 @@ def test_entry_points_reject_before_any_launch(L):
     assert lib.dpclip_norms_hutchpp_ex(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 9, -1, 1, 0, FAKE, FAKE,
                                        big, None) == L.ERR_INVALID_ARG
     assert lib.dpclip_philox_rademacher(None, 10, L.F32, 1, 0, 0, None) == L.ERR_INVALID_ARG
+    # bias of the linear layer
+    bg = lib.dpclip_bias_grads
+    assert bg(FAKE, 2, 8, 16, L.BF16, 0, None, None, FAKE, big, None) == L.ERR_INVALID_ARG
+    assert bg(FAKE, 2, 8, 12, L.BF16, 0, FAKE, FAKE, FAKE, big, None) == L.ERR_UNSUPPORTED
+    assert bg(FAKE, 2, 8, 16, L.BF16, 3, FAKE, FAKE, FAKE, big, None) == L.ERR_INVALID_ARG
+    assert bg(FAKE, 2, 8, 16, L.BF16, 0, FAKE, FAKE, FAKE, 0, None) == L.ERR_WORKSPACE
+    cb = lib.dpclip_clipped_noisy_bias_grad
+    assert cb(FAKE, 2, 16, FAKE, 0.0, 1.0, 1, 0, FAKE, None) == L.ERR_INVALID_ARG
+    assert cb(None, 2, 16, FAKE, 1.0, 1.0, 1, 0, FAKE, None) == L.ERR_INVALID_ARG
+    assert cb(FAKE, 20000, 16, FAKE, 1.0, 1.0, 1, 0, FAKE, None) == L.ERR_UNSUPPORTED
     # stored direct norms and their gradient
     st = lib.dpclip_norms_direct_store
     assert st(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 2, FAKE, FAKE, big, None) == L.ERR_INVALID_ARG

@@ -280,6 +280,109 @@ def test_stored_direct(api, wid):
     check_grad(api, inp, A, G, ref["direct"], C_med, wl.sigma, ref["Ms"], offset=9, stored=stored)
 
 
+@pytest.mark.parametrize("wid", [170, 177, 4])
+def test_bias_grads(api, wid):
+    # per-sample bias gradients sum_t G_i[t, :], their share of the norm and
+    # the clipped noisy bias gradient; 1100 tokens = two full 512-token chunks
+    # and a ragged one, p = 328 a full and a partial 256-column block
+    shapes = {170: W.Workload(170, "f32_odd", 3, 37, 29, 50, "f32", 1.0, 1.0, 1.0, 7, ()),
+              177: W.Workload(177, "bias_ragged", 3, 1100, 8, 328, "bf16", 1e-2, 1.0, 0.9, 8, ())}
+    wl = shapes[wid] if wid in shapes else W.get(wid)
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    tol = TOL[wl.dtype]
+    b_ref = O.per_sample_bias_grads(inp.G)
+    q_b, bg = api.bias_grads(G)
+    b = host(bg)
+    assert np.max(np.abs(b - b_ref)) <= tol * np.max(np.abs(b_ref))
+    assert_rel(host(q_b), O.bias_sqnorms(inp.G), tol, "bias sqnorms")
+    # the whole per-sample norm: weights (exact) + bias, accumulated on device
+    q_w = api.norms_exact(A, G, method=2 if wl.dtype == "bf16" else 0)
+    q_tot = q_w.clone()
+    api.bias_grads(G, sqnorms=q_tot, accumulate=True, want_grads=False)
+    q_ref = O.sqnorms_direct(inp.A, inp.G) + O.bias_sqnorms(inp.G)
+    assert_rel(host(q_tot), q_ref, tol, "weights + bias sqnorms")
+    C = float(np.median(np.sqrt(q_ref)))
+    q32 = host(q_tot).astype(np.float64)
+    Db = host(api.clipped_noisy_bias_grad(bg, q_tot, C, wl.sigma, wl.seed, 11))
+    Db_ref, s_ref, _ = O.clipped_noisy_bias_grad(None, q32, C, wl.sigma, wl.seed, 11, bs=b_ref)
+    mag = np.abs(Db_ref) + wl.sigma * C + np.sum(s_ref[:, None] * np.abs(b_ref), axis=0)
+    assert np.all(np.abs(Db - Db_ref) <= tol * mag)
+
+
+def _check_update(theta0, theta1, D_ref, scale, tol, mag):
+    # theta1 = theta0 - scale * g, g within tolerance of the oracle's D
+    want = theta0.astype(np.float64) - scale * D_ref
+    slack = tol * scale * (np.abs(D_ref) + mag) + 4 * np.spacing(np.abs(theta0).astype(np.float32))
+    assert np.all(np.abs(theta1 - want) <= slack)
+
+
+@pytest.mark.parametrize("path", ["gemm_bf16", "gemm_f32", "stored_bf16"])
+def test_fused_sgd_update(api, path):
+    # weights and bias updated in place by the gradient calls, with and
+    # without the gradient itself being stored
+    if path == "gemm_f32":
+        wl = W.Workload(170, "f32_odd", 3, 37, 29, 50, "f32", 1.0, 1.0, 1.0, 7, ())
+    else:
+        wl = W.Workload(176, "stored_ragged", 5, 300, 200, 328, "bf16", 1e-2, 1.0, 0.7, 8, ())
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    tol = TOL[wl.dtype]
+    Ms = list(O.per_sample_grads(inp.A, inp.G))
+    q_ref = O.sqnorms_direct(inp.A, inp.G) + O.bias_sqnorms(inp.G)
+    C = float(np.median(np.sqrt(q_ref)))
+    qd = torch.tensor(q_ref, dtype=torch.float32, device="cuda")
+    q32 = host(qd).astype(np.float64)
+    D_ref, s_ref, _ = O.clipped_noisy_grad(None, None, q32, C, wl.sigma, wl.seed, 5, Ms=Ms)
+    mag = grad_magnitude(inp.A, inp.G, s_ref) + wl.sigma * C
+    lr, L = 0.3, 7.0
+    rng = np.random.default_rng(3)
+    for store in (True, False):
+        theta0 = rng.standard_normal((wl.d, wl.p)).astype(np.float32)
+        theta = torch.tensor(theta0, device="cuda")
+        upd = api.SGDUpdate(theta, lr, L, store_grad=store)
+        if path == "stored_bf16":
+            _, stored = api.norms_direct_store(A, G)
+            g, _, _ = api.stored_clipped_noisy_grad(stored, qd, C, wl.sigma, wl.seed, 5, update=upd)
+        else:
+            g, _, _ = api.clipped_noisy_grad(A, G, qd, C, wl.sigma, wl.seed, 5, update=upd)
+        _check_update(theta0, host(theta), D_ref, lr / L, tol, mag)
+        if store:
+            assert_grad(host(g), D_ref, tol, wl.sigma * C, mag=grad_magnitude(inp.A, inp.G, s_ref))
+        elif path != "gemm_f32":
+            assert g is None
+    # the bias
+    q_b, bg = api.bias_grads(G)
+    b_ref = O.per_sample_bias_grads(inp.G)
+    Db_ref, _, _ = O.clipped_noisy_bias_grad(None, q32, C, wl.sigma, wl.seed, 5, bs=b_ref)
+    beta0 = rng.standard_normal(wl.p).astype(np.float32)
+    beta = torch.tensor(beta0, device="cuda")
+    api.clipped_noisy_bias_grad(bg, qd, C, wl.sigma, wl.seed, 5,
+                                update=api.SGDUpdate(beta, lr, L, store_grad=False))
+    bmag = np.abs(Db_ref) + wl.sigma * C + np.sum(s_ref[:, None] * np.abs(b_ref), axis=0)
+    _check_update(beta0, host(beta), Db_ref, lr / L, tol, bmag)
+
+
+def test_empty_poisson_lot(api):
+    # B = 0: the gradient is the noise alone (streams 3 and 4), the update too
+    d, p, C, sigma, lr, L = 40, 24, 2.0, 1.5, 0.3, 10.0
+    A = torch.zeros(0, 5, d, dtype=torch.bfloat16, device="cuda")
+    G = torch.zeros(0, 5, p, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(0, device="cuda")
+    theta = torch.ones(d, p, device="cuda")
+    g, _, _ = api.clipped_noisy_grad(A, G, q, C, sigma, 9, 4, update=api.SGDUpdate(theta, lr, L))
+    D_ref, _, _ = O.clipped_noisy_grad(np.zeros((0, 5, d)), np.zeros((0, 5, p)), np.zeros(0), C,
+                                       sigma, 9, 4)
+    assert np.max(np.abs(host(g) - D_ref)) < 1e-4
+    np.testing.assert_allclose(host(theta), O.sgd_update(np.ones((d, p)), D_ref, lr, L), atol=1e-5)
+    beta = torch.zeros(p, device="cuda")
+    gb = api.clipped_noisy_bias_grad(torch.zeros(0, p, device="cuda"), q, C, sigma, 9, 4,
+                                     update=api.SGDUpdate(beta, lr, L))
+    Db_ref, _, _ = O.clipped_noisy_bias_grad(None, np.zeros(0), C, sigma, 9, 4, bs=np.zeros((0, p)))
+    assert np.max(np.abs(host(gb) - Db_ref)) < 1e-4
+    np.testing.assert_allclose(host(beta), -lr / L * Db_ref, atol=1e-5)
+
+
 @pytest.mark.parametrize("case", ["bf16", "f32_rankdef"])
 def test_hutchpp_wide_layer(api, case):
     # p = 20000 (17001) rows: each CTA of the sample's cluster owns more rows
