@@ -216,6 +216,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the extra (non-step) rows")
+    ap.add_argument("--extra-rows", default=",".join(EXTRA_ROWS),
+                    help="comma-separated subset of the extra rows (default: all)")
     ap.add_argument("--rows", default=",".join(ROWS),
                     help="comma-separated subset of rows (default: all, the full step)")
     args = ap.parse_args()
@@ -446,7 +448,9 @@ def main():
     # ---------------------------------------------------------------- extra rows (not in the step)
     extra_ms = {}
     if not args.no_extra:
-        for r in EXTRA_ROWS:
+        for r in (x for x in args.extra_rows.split(",") if x):
+            if r not in EXTRA_ROWS:
+                raise SystemExit(f"unknown extra row {r}")
             for s_ in range(args.warmup):
                 row_fn(r, s_)()
             barrier()
