@@ -16,6 +16,10 @@ Sources (cited by title and section throughout):
       1: complexity reduction".
   PH  J. Salmon, M. Moraes, R. Dror, D. Shaw, "Parallel random numbers: as easy
       as 1, 2, 3", SC'11 -- the Philox-4x32 bijection with 10 rounds.
+  FB  "Technical summary: FIBER -- a differentially private optimizer with
+      filter-aware innovation bias correction" (gist.science summary of arXiv
+      2605.03425) -- section "Method: FIBER", A (innovation-space filtering)
+      and C (filter-aware second-moment calibration).
 
 Notation (RC, Core mechanism): for sample i, A_i is the T x d matrix of layer
 inputs (activations), G_i the T x p matrix of output gradients, the per-sample
@@ -57,7 +61,7 @@ __all__ = [
     "hutch_probe", "sqnorms_hutch", "hutchpp_split", "hutchpp_probes",
     "sqnorms_hutchpp", "clip_scales", "noise_matrix", "clipped_noisy_grad",
     "STREAM_BIAS_NOISE", "per_sample_bias_grads", "bias_sqnorms", "clipped_noisy_bias_grad",
-    "sgd_update",
+    "sgd_update", "fiber_attenuation", "fiber_filter_step", "fiber_adamw_step",
 ]
 
 STREAM_P, STREAM_S, STREAM_GP, STREAM_NOISE = 0, 1, 2, 3
@@ -367,3 +371,48 @@ def clipped_noisy_bias_grad(G, q, C: float, sigma: float, seed: int, offset: int
 def sgd_update(theta: np.ndarray, g_noisy: np.ndarray, lr: float, denom: float) -> np.ndarray:
     """theta - lr * g_noisy / denom, in fp64."""
     return np.asarray(theta, np.float64) - (lr / denom) * np.asarray(g_noisy, np.float64)
+
+
+# ----------------------------------------------------------------------------
+# FIBER (FB, Method A and C): the privatized gradient g_t is filtered in
+# innovation space and fed to AdamW, whose second moment is calibrated by the
+# filtered noise variance.
+#   innovation   nu_t = g_t - gf_{t-1}
+#   residual     r_t  = (1 - omega) r_{t-1} + omega nu_t
+#   integration  gf_t = gf_{t-1} + r_t
+# A stable linear filter; for white noise of variance s2 at its input the
+# output variance in steady state is A(omega) s2, A = (2 - omega)/(4 - 3 omega).
+# AdamW on gf_t (decoupled weight decay), with the bias-corrected second
+# moment reduced by the attenuated noise variance:
+#   vbar_t = max(vhat_t - A(omega) s2, eps_v).
+# Readings (FB is silent): the filter and moment states start at zero; the
+# update is theta -= lr (mhat / (sqrt(vbar) + eps) + wd theta), the AdamW form;
+# g_t is the privatized gradient the optimizer sees (the noisy clipped sum
+# divided by the lot size), its noise variance per coordinate s2 = (sigma C / L)^2.
+
+def fiber_attenuation(omega: float) -> float:
+    """A(omega) = (2 - omega) / (4 - 3 omega), in [0.5, 1] for 0 < omega <= 1."""
+    return (2.0 - omega) / (4.0 - 3.0 * omega)
+
+
+def fiber_filter_step(g, gf, r, omega: float):
+    """One step of the innovation filter: returns (gf_t, r_t)."""
+    nu = np.asarray(g, np.float64) - gf
+    r = (1.0 - omega) * r + omega * nu
+    return gf + r, r
+
+
+def fiber_adamw_step(theta, g, state, t: int, lr: float, beta1: float, beta2: float, eps: float,
+                     eps_v: float, wd: float, omega: float, noise_var: float):
+    """One FIBER step at step number t >= 1.  state = (gf, r, m, v), every
+    array shaped like theta; returns (theta_t, state_t), all fp64."""
+    gf, r, m, v = state
+    gf, r = fiber_filter_step(g, gf, r, omega)
+    m = beta1 * m + (1.0 - beta1) * gf
+    v = beta2 * v + (1.0 - beta2) * gf * gf
+    mhat = m / (1.0 - beta1 ** t)
+    vhat = v / (1.0 - beta2 ** t)
+    vbar = np.maximum(vhat - fiber_attenuation(omega) * noise_var, eps_v)
+    theta = np.asarray(theta, np.float64)
+    theta = theta - lr * (mhat / (np.sqrt(vbar) + eps) + wd * theta)
+    return theta, (gf, r, m, v)

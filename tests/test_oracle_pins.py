@@ -399,3 +399,68 @@ def test_empty_poisson_lot_updates_by_noise_only():
     assert abs(step.mean()) < 4 / math.sqrt(n) and abs(step.var() - 1) < 4 * math.sqrt(2 / n)
     Db, _, _ = O.clipped_noisy_bias_grad(G, np.zeros(0), 2.0, 1.5, 9, 4, bs=np.zeros((0, p)))
     assert Db.shape == (p,) and np.all(Db != 0)
+
+
+# --------------------------------------------------------------- FIBER filter and calibrated AdamW
+
+@pytest.mark.parametrize("omega", [0.15, 0.5, 0.85, 1.0])
+def test_fiber_filter_attenuates_white_noise_by_A(omega):
+    # the closed form of the summary against a long simulation of the filter
+    # on unit white noise (many independent coordinates, steady state)
+    r = _rng(61)
+    n, steps = 20000, 400
+    gf = np.zeros(n)
+    res = np.zeros(n)
+    for _ in range(steps):
+        gf, res = O.fiber_filter_step(r.standard_normal(n), gf, res, omega)
+    var = gf.var()
+    A = O.fiber_attenuation(omega)
+    assert 0.5 <= A <= 1.0
+    # chi-square spread of a sample variance over n coordinates
+    assert abs(var - A) < 5 * A * math.sqrt(2.0 / n)
+
+
+def test_fiber_filter_tracks_a_drifting_gradient():
+    # the second-order (constant-velocity) recursion follows a linear drift with
+    # no steady-state error, where an EMA of the state lags by a constant
+    gf, res = np.zeros(1), np.zeros(1)
+    ema = np.zeros(1)
+    for t in range(1, 400):
+        g = np.array([1.0 + 0.01 * t])
+        gf, res = O.fiber_filter_step(g, gf, res, 0.2)
+        ema = 0.8 * ema + 0.2 * g
+    assert abs(gf[0] - g[0]) < 1e-6
+    assert abs(ema[0] - g[0]) > 0.03
+
+
+def test_fiber_with_unit_gain_and_no_noise_is_adamw():
+    # omega = 1 passes the gradient through; noise_var = 0 and eps_v = 0 leave
+    # AdamW: compare with torch.optim.AdamW in fp64 over a few steps
+    r = _rng(62)
+    theta0 = r.standard_normal(50)
+    grads = [r.standard_normal(50) for _ in range(6)]
+    p = torch.tensor(theta0, dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.AdamW([p], lr=0.01, betas=(0.9, 0.99), eps=1e-8, weight_decay=0.05)
+    theta = theta0.copy()
+    state = tuple(np.zeros(50) for _ in range(4))
+    for t, g in enumerate(grads, start=1):
+        p.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        theta, state = O.fiber_adamw_step(theta, g, state, t, 0.01, 0.9, 0.99, 1e-8, 0.0, 0.05,
+                                          1.0, 0.0)
+    np.testing.assert_allclose(theta, p.detach().numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_fiber_calibration_removes_the_filtered_noise():
+    # pure DP noise of variance s2: the filtered second moment settles at
+    # A(omega) s2, which the calibration removes (down to the floor eps_v)
+    r = _rng(63)
+    n, s2, omega = 20000, 0.04, 0.3
+    theta = np.zeros(n)
+    state = tuple(np.zeros(n) for _ in range(4))
+    for t in range(1, 1201):
+        g = math.sqrt(s2) * r.standard_normal(n)
+        theta, state = O.fiber_adamw_step(theta, g, state, t, 0.0, 0.9, 0.999, 1e-8, 1e-12, 0.0,
+                                          omega, s2)
+    v = state[3] / (1 - 0.999 ** 1200)
+    assert abs(v.mean() - O.fiber_attenuation(omega) * s2) < 0.05 * s2
