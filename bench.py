@@ -38,7 +38,8 @@ METRIC = "clip+noise tokens/s per linear layer (Hutch/Hutch++/exact); % bf16 ten
 ROWS = ("hutch", "hutchpp", "exact_direct", "exact_ghost", "clipped_noisy_grad")
 # measured after the step, not part of it: the Rademacher-probe variants
 EXTRA_ROWS = ("hutch_rademacher", "hutchpp_rademacher", "exact_direct_stored",
-              "stored_clipped_noisy_grad", "bias_grads", "clipped_noisy_grad_sgd")
+              "stored_clipped_noisy_grad", "bias_grads", "clipped_noisy_grad_sgd",
+              "fiber_step", "clipped_noisy_grad_fiber")
 # kernels each ABI call launches for bf16 inputs (memsets of the control block excluded)
 LAUNCHES = {"hutch": 3, "hutchpp": 9, "exact_direct": 1, "exact_ghost": 1, "clipped_noisy_grad": 1}
 
@@ -62,6 +63,10 @@ def algorithmic_work(wl):
         "bias_grads": (2.0 * B * T * p, "bytes", "hbm"),
         # the clipped noisy gradient applied to fp32 weights in its epilogue
         "clipped_noisy_grad_sgd": (2.0 * B * T * d * p, "flops", "tensor"),
+        # FIBER step on d x p parameters: read g, read and write the parameter
+        # and its four states (fp32)
+        "fiber_step": (44.0 * d * p, "bytes", "hbm"),
+        "clipped_noisy_grad_fiber": (2.0 * B * T * d * p, "flops", "tensor"),
         "exact_direct": (2.0 * B * T * d * p, "flops", "tensor"),
         "exact_ghost": (1.0 * B * T * (T + 1) * (d + p), "flops", "tensor"),
         "clipped_noisy_grad": (2.0 * B * T * d * p, "flops", "tensor"),
@@ -309,6 +314,17 @@ def main():
             return lambda: api.clipped_noisy_grad(b["A"], b["G"], b["q_h"], wl.C, wl.sigma, wl.seed,
                                                   step, scales=b["scales"], clipped=b["clipped"],
                                                   ws=ws["clipped_noisy_grad"], update=upd)
+        if name in ("fiber_step", "clipped_noisy_grad_fiber"):
+            if "fiber" not in stored:
+                nv = (wl.sigma * wl.C / B) ** 2
+                stored["fiber"] = api.FiberAdamW(torch.zeros(d, p, **f32), lr=1e-4, denom=float(B),
+                                                 noise_var=nv)
+            if name == "fiber_step":
+                return lambda: api.fiber_step(b["grad"], stored["fiber"])
+            return lambda: api.clipped_noisy_grad(b["A"], b["G"], b["q_h"], wl.C, wl.sigma, wl.seed,
+                                                  step, scales=b["scales"], clipped=b["clipped"],
+                                                  ws=ws["clipped_noisy_grad"], fiber=stored["fiber"],
+                                                  store_grad=False)
         if name == "stored_clipped_noisy_grad":
             if "h" not in stored:
                 row_fn("exact_direct_stored", step, bufs)()

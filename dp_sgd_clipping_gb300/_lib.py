@@ -44,6 +44,18 @@ class SgdUpdate(_c.Structure):
 
 _up = _c.POINTER(SgdUpdate)
 
+
+class FiberAdamW(_c.Structure):
+    """struct dpclip_fiber_adamw: the FIBER step's tensors and hyper-parameters."""
+    _fields_ = [("param", _c.c_void_p), ("filt", _c.c_void_p), ("resid", _c.c_void_p),
+                ("m", _c.c_void_p), ("v", _c.c_void_p), ("lr", _c.c_float),
+                ("beta1", _c.c_float), ("beta2", _c.c_float), ("eps", _c.c_float),
+                ("eps_v", _c.c_float), ("weight_decay", _c.c_float), ("omega", _c.c_float),
+                ("noise_var", _c.c_float), ("denom", _c.c_float), ("step", _c.c_int)]
+
+
+_fp = _c.POINTER(FiberAdamW)
+
 # symbol -> (restype, argtypes)
 SIGNATURES = {
     "dpclip_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, _i, _c.POINTER(_sz)]),
@@ -64,6 +76,13 @@ SIGNATURES = {
                                                  _vp, _up, _vp, _sz, _vp]),
     "dpclip_clipped_noisy_bias_grad_ex": (_i, [_vp, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _up,
                                                _vp]),
+    "dpclip_fiber_adamw_step": (_i, [_vp, _i64, _fp, _vp]),
+    "dpclip_clipped_noisy_grad_fiber": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _f, _f, _u64,
+                                             _u64, _vp, _vp, _vp, _fp, _vp, _sz, _vp]),
+    "dpclip_stored_clipped_noisy_grad_fiber": (_i, [_i, _i, _i, _vp, _f, _f, _u64, _u64, _vp,
+                                                    _vp, _vp, _fp, _vp, _sz, _vp]),
+    "dpclip_clipped_noisy_bias_grad_fiber": (_i, [_vp, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _fp,
+                                                  _vp]),
     "dpclip_bias_grads": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "dpclip_clipped_noisy_bias_grad": (_i, [_vp, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _vp]),
     "dpclip_norms_direct_store": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp]),

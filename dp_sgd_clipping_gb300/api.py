@@ -15,7 +15,7 @@ from . import _lib as L
 
 __all__ = ["norms_exact", "norms_hutch", "norms_hutchpp", "clipped_noisy_grad", "clip_scales",
            "norms_direct_store", "stored_clipped_noisy_grad", "StoredGradients",
-           "bias_grads", "clipped_noisy_bias_grad", "SGDUpdate",
+           "bias_grads", "clipped_noisy_bias_grad", "SGDUpdate", "FiberAdamW", "fiber_step",
            "philox_normal", "philox_rademacher", "workspace_bytes", "workspace_status",
            "selftest_wait_timeout"]
 
@@ -103,26 +103,72 @@ class SGDUpdate:
                            int(bool(self.store_grad)))
 
 
+class FiberAdamW:
+    """FIBER optimizer state of one parameter tensor and its hyper-parameters
+    (dpclip_fiber_adamw): the innovation filter (filt, resid) and AdamW moments
+    (m, v) start at zero; `step` advances by one on every call that applies
+    the step.  noise_var is the DP noise variance per coordinate of g = D / L,
+    (sigma C / L)^2 for this library's noisy sum."""
+
+    def __init__(self, param, lr: float, denom: float, noise_var: float, omega: float = 0.5,
+                 beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8, eps_v: float = 1e-12,
+                 weight_decay: float = 0.0):
+        if param.dtype != torch.float32 or not param.is_cuda or not param.is_contiguous():
+            raise ValueError("param must be a contiguous CUDA float32 tensor")
+        self.param = param
+        self.filt, self.resid, self.m, self.v = (torch.zeros_like(param) for _ in range(4))
+        self.lr, self.denom, self.noise_var, self.omega = lr, denom, noise_var, omega
+        self.beta1, self.beta2, self.eps, self.eps_v, self.weight_decay = (beta1, beta2, eps, eps_v,
+                                                                          weight_decay)
+        self.step = 0
+
+    def _c(self):
+        self.step += 1
+        return L.FiberAdamW(self.param.data_ptr(), self.filt.data_ptr(), self.resid.data_ptr(),
+                            self.m.data_ptr(), self.v.data_ptr(), float(self.lr), float(self.beta1),
+                            float(self.beta2), float(self.eps), float(self.eps_v),
+                            float(self.weight_decay), float(self.omega), float(self.noise_var),
+                            float(self.denom), int(self.step))
+
+
+def fiber_step(grad, opt: FiberAdamW, stream=None):
+    """One FIBER step of `opt` from a gradient already formed (fp32, param's shape)."""
+    L.check("dpclip_fiber_adamw_step", L.lib.dpclip_fiber_adamw_step(
+        grad.data_ptr(), grad.numel(), ctypes.pointer(opt._c()), _stream(stream)))
+
+
 def _upd(update):
     return None if update is None else ctypes.pointer(update._c())
 
 
 def clipped_noisy_grad(A, G, sqnorms, C: float, sigma: float, seed: int, offset: int = 0,
                        grad=None, scales=None, clipped=None, ws=None, stream=None,
-                       want_scales: bool = True, update: SGDUpdate = None):
+                       want_scales: bool = True, update: SGDUpdate = None,
+                       fiber: FiberAdamW = None, store_grad: bool = True):
     """Returns (grad [d, p] fp32, scales [B] fp32, clipped [B] uint8); with
-    `update`, also applies it.  A lot of B = 0 samples ([0, T, d] tensors)
-    gives the noise alone."""
+    `update` (an SGD step) or `fiber` (a FIBER step), also applies it.  A lot
+    of B = 0 samples ([0, T, d] tensors) gives the noise alone."""
     B, T, d, p, dt = _check_pair(A, G)
     if B > 0 and (sqnorms.dtype != torch.float32 or sqnorms.numel() != B or not sqnorms.is_cuda):
         raise ValueError("sqnorms must be a CUDA float32 tensor of B entries")
     nb = workspace_bytes(L.OP_CLIPPED_NOISY_GRAD, max(B, 1), T, d, p, dt, 0)
     ws = _workspace(nb, A.device, ws)
-    if grad is None and (update is None or update.store_grad or dt == L.F32):
+    wants = update.store_grad if update is not None else (store_grad if fiber is not None else True)
+    if grad is None and (wants or dt == L.F32):
         grad = torch.empty(d, p, dtype=torch.float32, device=A.device)
     if want_scales:
         scales = torch.empty(B, dtype=torch.float32, device=A.device) if scales is None else scales
         clipped = torch.empty(B, dtype=torch.uint8, device=A.device) if clipped is None else clipped
+    if fiber is not None:
+        L.check("dpclip_clipped_noisy_grad_fiber", L.lib.dpclip_clipped_noisy_grad_fiber(
+            A.data_ptr() if B else None, G.data_ptr() if B else None, B, T, d, p, dt,
+            sqnorms.data_ptr() if B else None, float(C), float(sigma), seed, offset,
+            grad.data_ptr() if grad is not None else None,
+            scales.data_ptr() if scales is not None and B else None,
+            clipped.data_ptr() if clipped is not None and B else None,
+            ctypes.pointer(fiber._c()), ws.data_ptr(), ws.numel() * ws.element_size(),
+            _stream(stream)))
+        return grad, scales, clipped
     L.check("dpclip_clipped_noisy_grad_ex", L.lib.dpclip_clipped_noisy_grad_ex(
         A.data_ptr() if B else None, G.data_ptr() if B else None, B, T, d, p, dt,
         sqnorms.data_ptr() if B else None, float(C), float(sigma), seed, offset,
@@ -162,18 +208,30 @@ def norms_direct_store(A, G, sqnorms=None, accumulate: bool = False, ws=None, st
 
 def stored_clipped_noisy_grad(stored: StoredGradients, sqnorms, C: float, sigma: float, seed: int,
                               offset: int = 0, grad=None, scales=None, clipped=None, stream=None,
-                              want_scales: bool = True, update: SGDUpdate = None):
+                              want_scales: bool = True, update: SGDUpdate = None,
+                              fiber: FiberAdamW = None, store_grad: bool = True):
     """clipped_noisy_grad from the per-sample gradients kept by norms_direct_store.
 
     Returns (grad [d, p] fp32, scales [B] fp32, clipped [B] uint8)."""
     B, d, p, ws = stored.B, stored.d, stored.p, stored.ws
     if sqnorms.dtype != torch.float32 or sqnorms.numel() != B or not sqnorms.is_cuda:
         raise ValueError("sqnorms must be a CUDA float32 tensor of B entries")
-    if grad is None and (update is None or update.store_grad):
+    wants = update.store_grad if update is not None else (store_grad if fiber is not None else True)
+    if grad is None and wants:
         grad = torch.empty(d, p, dtype=torch.float32, device=ws.device)
     if want_scales:
         scales = torch.empty(B, dtype=torch.float32, device=ws.device) if scales is None else scales
         clipped = torch.empty(B, dtype=torch.uint8, device=ws.device) if clipped is None else clipped
+    if fiber is not None:
+        L.check("dpclip_stored_clipped_noisy_grad_fiber",
+                L.lib.dpclip_stored_clipped_noisy_grad_fiber(
+                    B, d, p, sqnorms.data_ptr(), float(C), float(sigma), seed, offset,
+                    grad.data_ptr() if grad is not None else None,
+                    scales.data_ptr() if scales is not None else None,
+                    clipped.data_ptr() if clipped is not None else None,
+                    ctypes.pointer(fiber._c()), ws.data_ptr(), ws.numel() * ws.element_size(),
+                    _stream(stream)))
+        return grad, scales, clipped
     L.check("dpclip_stored_clipped_noisy_grad_ex", L.lib.dpclip_stored_clipped_noisy_grad_ex(
         B, d, p, sqnorms.data_ptr(), float(C), float(sigma), seed, offset,
         grad.data_ptr() if grad is not None else None,
@@ -207,12 +265,21 @@ def bias_grads(G, sqnorms=None, accumulate: bool = False, want_grads: bool = Tru
 
 
 def clipped_noisy_bias_grad(bias_grads, sqnorms, C: float, sigma: float, seed: int, offset: int = 0,
-                            out=None, stream=None, update: SGDUpdate = None):
+                            out=None, stream=None, update: SGDUpdate = None,
+                            fiber: FiberAdamW = None, store_grad: bool = True):
     """sum_i s_i b_i + sigma C z (z: Philox stream 4), fp32 [p]; with
-    `update`, also applies it.  bias_grads of shape [0, p]: the noise alone."""
+    `update` or `fiber`, also applies it.  bias_grads of shape [0, p]: the
+    noise alone."""
     B, p = bias_grads.shape
-    if out is None and (update is None or update.store_grad):
+    wants = update.store_grad if update is not None else (store_grad if fiber is not None else True)
+    if out is None and wants:
         out = torch.empty(p, dtype=torch.float32, device=bias_grads.device)
+    if fiber is not None:
+        L.check("dpclip_clipped_noisy_bias_grad_fiber", L.lib.dpclip_clipped_noisy_bias_grad_fiber(
+            bias_grads.data_ptr() if B else None, B, p, sqnorms.data_ptr() if B else None,
+            float(C), float(sigma), seed, offset, out.data_ptr() if out is not None else None,
+            ctypes.pointer(fiber._c()), _stream(stream)))
+        return out
     L.check("dpclip_clipped_noisy_bias_grad_ex", L.lib.dpclip_clipped_noisy_bias_grad_ex(
         bias_grads.data_ptr() if B else None, B, p, sqnorms.data_ptr() if B else None, float(C),
         float(sigma), seed, offset, out.data_ptr() if out is not None else None, _upd(update),

@@ -93,7 +93,8 @@ __global__ void finalize_norms_kernel(const float* part, int nunits, long long s
 __global__ void stored_grad_kernel(const float* __restrict__ M, int B, long long n,
                                    long long stride, const float* sq, float C, float nscale,
                                    uint64_t seed, uint64_t offset, float* grad, float* scales,
-                                   uint8_t* clipped, float* param, float upd_scale) {
+                                   uint8_t* clipped, float* param, float upd_scale,
+                                   const FiberDev fiber, int use_fiber) {
   extern __shared__ float s_sh[];
   pdl_trigger();
   pdl_wait();
@@ -153,10 +154,12 @@ __global__ void stored_grad_kernel(const float* __restrict__ M, int B, long long
         w.w = fmaf(-upd_scale, acc.w, w.w);
         reinterpret_cast<float4*>(param)[b] = w;
       }
+      if (use_fiber) fiber_update4(fiber, 4 * (size_t)b, acc);
     } else {   // ragged end: lanes past n hold padding and are not stored
       for (int l = 0; 4 * b + l < n; ++l) {
         if (grad) grad[4 * b + l] = a4[l];
         if (param) param[4 * b + l] = fmaf(-upd_scale, a4[l], param[4 * b + l]);
+        if (use_fiber) fiber_update1(fiber, 4 * (size_t)b + l, a4[l]);
       }
     }
   }
@@ -166,7 +169,7 @@ __global__ void stored_grad_kernel(const float* __restrict__ M, int B, long long
 // (element e), stored to grad and / or applied as param -= upd_scale g.
 __global__ void noise_only_kernel(float* grad, float* param, long long n, float nscale,
                                   float upd_scale, uint64_t seed, uint32_t stream_id,
-                                  uint64_t offset) {
+                                  uint64_t offset, const FiberDev fiber, int use_fiber) {
   pdl_trigger();
   pdl_wait();
   const long long nblk = (n + 3) / 4;
@@ -181,7 +184,26 @@ __global__ void noise_only_kernel(float* grad, float* param, long long n, float 
         const float g = nscale * z[l];
         if (grad) grad[e] = g;
         if (param) param[e] = fmaf(-upd_scale, g, param[e]);
+        if (use_fiber) fiber_update1(fiber, (size_t)e, g);
       }
+    }
+  }
+}
+
+// The FIBER step over a gradient already formed.
+__global__ void fiber_kernel(const float* grad, long long n, const FiberDev f) {
+  pdl_trigger();
+  pdl_wait();
+  const long long nb = (n + 3) / 4;
+  const bool vec = (reinterpret_cast<uintptr_t>(grad) | reinterpret_cast<uintptr_t>(f.param) |
+                    reinterpret_cast<uintptr_t>(f.filt) | reinterpret_cast<uintptr_t>(f.resid) |
+                    reinterpret_cast<uintptr_t>(f.m) | reinterpret_cast<uintptr_t>(f.v)) % 16 == 0;
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nb;
+       b += (long long)gridDim.x * blockDim.x) {
+    if (vec && 4 * b + 3 < n) {
+      fiber_update4(f, 4 * (size_t)b, reinterpret_cast<const float4*>(grad)[b]);
+    } else {
+      for (long long e = 4 * b; e < n && e < 4 * b + 4; ++e) fiber_update1(f, (size_t)e, grad[e]);
     }
   }
 }
@@ -285,25 +307,36 @@ cudaError_t launch_finalize_norms(const float* part, int B, int nunits, long lon
 cudaError_t launch_stored_grad(const float* M, int B, long long n, long long stride,
                                const float* sq, float C, float nscale, uint64_t seed,
                                uint64_t offset, float* grad, float* scales, uint8_t* clipped,
-                               float* param, float upd_scale, cudaStream_t s) {
+                               float* param, float upd_scale, const FiberDev* fiber,
+                               cudaStream_t s) {
+  const FiberDev fz = fiber ? *fiber : FiberDev{};
   const long long nb = (n + 3) / 4;
   const int threads = 256;
   const int grid = (int)std::max<long long>(1, std::min<long long>((nb + threads - 1) / threads,
                                                                    152 * 8));
   return launch_pdl(stored_grad_kernel, dim3(grid), dim3(threads), (size_t)B * sizeof(float), s,
                     0, M, B, n, stride, sq, C, nscale, seed, offset, grad, scales, clipped, param,
-                    upd_scale);
+                    upd_scale, fz, fiber ? 1 : 0);
 }
 
 cudaError_t launch_noise_only(float* grad, float* param, long long n, float nscale,
                               float upd_scale, uint64_t seed, uint32_t stream_id, uint64_t offset,
-                              cudaStream_t s) {
+                              const FiberDev* fiber, cudaStream_t s) {
+  const FiberDev fz = fiber ? *fiber : FiberDev{};
   const long long nblk = (n + 3) / 4;
   const int threads = 256;
   const int grid = (int)std::max<long long>(1, std::min<long long>((nblk + threads - 1) / threads,
                                                                    152 * 8));
   return launch_pdl(noise_only_kernel, dim3(grid), dim3(threads), 0, s, 0, grad, param, n, nscale,
-                    upd_scale, seed, stream_id, offset);
+                    upd_scale, seed, stream_id, offset, fz, fiber ? 1 : 0);
+}
+
+cudaError_t launch_fiber(const float* grad, long long n, const FiberDev& f, cudaStream_t s) {
+  const long long nb = (n + 3) / 4;
+  const int threads = 256;
+  const int grid = (int)std::max<long long>(1, std::min<long long>((nb + threads - 1) / threads,
+                                                                   152 * 8));
+  return launch_pdl(fiber_kernel, dim3(grid), dim3(threads), 0, s, 0, grad, n, f);
 }
 
 cudaError_t launch_sgd_update(float* param, const float* grad, long long n, float scale,

@@ -120,7 +120,8 @@ __global__ void bias_sq_kernel(const float* part2, int ncb, int B, float* sq, in
 
 __global__ void bias_clip_kernel(const float* bias, int B, int p, const float* sq, float C,
                                  float nscale, uint64_t seed, uint64_t offset, float* grad_b,
-                                 float* param, float upd_scale) {
+                                 float* param, float upd_scale, const FiberDev fiber,
+                                 int use_fiber) {
   extern __shared__ float s_sh[];
   pdl_trigger();
   pdl_wait();
@@ -149,6 +150,7 @@ __global__ void bias_clip_kernel(const float* bias, int B, int p, const float* s
       if (4 * b + l < p) {
         if (grad_b) grad_b[4 * b + l] = acc[l];
         if (param) param[4 * b + l] = fmaf(-upd_scale, acc[l], param[4 * b + l]);
+        if (use_fiber) fiber_update1(fiber, 4 * (size_t)b + l, acc[l]);
       }
     }
   }
@@ -183,12 +185,14 @@ cudaError_t launch_bias_grads(const void* G, bool bf16, int B, int T, int p, flo
 
 cudaError_t launch_bias_clip(const float* bias, int B, int p, const float* sq, float C, float nscale,
                              uint64_t seed, uint64_t offset, float* grad_b, float* param,
-                             float upd_scale, cudaStream_t s) {
+                             float upd_scale, const FiberDev* fiber, cudaStream_t s) {
+  const FiberDev fz = fiber ? *fiber : FiberDev{};
   const int nb = (p + 3) / 4;
   const int threads = 256;
   const int grid = std::max(1, std::min((nb + threads - 1) / threads, 152 * 4));
   return launch_pdl(bias_clip_kernel, dim3(grid), dim3(threads), (size_t)B * sizeof(float), s, 0,
-                    bias, B, p, sq, C, nscale, seed, offset, grad_b, param, upd_scale);
+                    bias, B, p, sq, C, nscale, seed, offset, grad_b, param, upd_scale, fz,
+                    fiber ? 1 : 0);
 }
 
 }  // namespace dpclip

@@ -347,4 +347,40 @@ __device__ __forceinline__ void reduce_partials_last_cta(const float* part, int 
   if (threadIdx.x == 0) *ticket = 0u;
 }
 
+// FIBER step of one parameter element ("Technical summary: FIBER", Method A
+// and C): the innovation filter on g = grad * inv_denom, then AdamW on the
+// filtered gradient with the second moment reduced by A(omega) s2.
+__device__ __forceinline__ void fiber_elem(const FiberDev& f, float grad, float& theta, float& gf,
+                                           float& r, float& m, float& v) {
+  const float g = grad * f.inv_denom;
+  r = fmaf(f.omega, g - gf, (1.f - f.omega) * r);
+  gf += r;
+  m = fmaf(f.beta1, m, (1.f - f.beta1) * gf);
+  v = fmaf(f.beta2, v, (1.f - f.beta2) * gf * gf);
+  const float vbar = fmaxf(v * f.bc2 - f.calib, f.eps_v);
+  theta -= f.lr * ((m * f.bc1) / (sqrtf(vbar) + f.eps) + f.wd * theta);
+}
+
+// The same on four consecutive elements e .. e + 3 (16-byte aligned).
+__device__ __forceinline__ void fiber_update4(const FiberDev& f, size_t e, float4 g) {
+  float4 th = *reinterpret_cast<const float4*>(f.param + e);
+  float4 gf = *reinterpret_cast<const float4*>(f.filt + e);
+  float4 r = *reinterpret_cast<const float4*>(f.resid + e);
+  float4 m = *reinterpret_cast<const float4*>(f.m + e);
+  float4 v = *reinterpret_cast<const float4*>(f.v + e);
+  fiber_elem(f, g.x, th.x, gf.x, r.x, m.x, v.x);
+  fiber_elem(f, g.y, th.y, gf.y, r.y, m.y, v.y);
+  fiber_elem(f, g.z, th.z, gf.z, r.z, m.z, v.z);
+  fiber_elem(f, g.w, th.w, gf.w, r.w, m.w, v.w);
+  *reinterpret_cast<float4*>(f.param + e) = th;
+  *reinterpret_cast<float4*>(f.filt + e) = gf;
+  *reinterpret_cast<float4*>(f.resid + e) = r;
+  *reinterpret_cast<float4*>(f.m + e) = m;
+  *reinterpret_cast<float4*>(f.v + e) = v;
+}
+
+__device__ __forceinline__ void fiber_update1(const FiberDev& f, size_t e, float g) {
+  fiber_elem(f, g, f.param[e], f.filt[e], f.resid[e], f.m[e], f.v[e]);
+}
+
 }  // namespace dpclip

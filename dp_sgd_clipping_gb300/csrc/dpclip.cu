@@ -795,32 +795,68 @@ int check_update(const dpclip_sgd_update* u, float* scale) {
   *scale = u->lr / u->denom;
   return DPCLIP_OK;
 }
-bool writes_grad(const dpclip_sgd_update* u) { return !u || u->store_grad; }
+
+// Checks an optional FIBER step and converts it for the device.
+int make_fiber(const dpclip_fiber_adamw* o, FiberDev* f, bool vec16) {
+  if (!o) return DPCLIP_OK;
+  if (!o->param || !o->filt || !o->resid || !o->m || !o->v) return DPCLIP_ERR_INVALID_ARG;
+  const float hp[] = {o->lr, o->beta1, o->beta2, o->eps, o->eps_v, o->weight_decay, o->omega,
+                      o->noise_var, o->denom};
+  for (float x : hp)
+    if (!std::isfinite(x)) return DPCLIP_ERR_INVALID_ARG;
+  if (!(o->omega > 0.f && o->omega <= 1.f) || o->step < 1 || !(o->denom > 0.f) ||
+      !(o->beta1 >= 0.f && o->beta1 < 1.f) || !(o->beta2 >= 0.f && o->beta2 < 1.f) ||
+      o->eps < 0.f || o->eps_v < 0.f || o->noise_var < 0.f)
+    return DPCLIP_ERR_INVALID_ARG;
+  const size_t al = vec16 ? 16 : 4;
+  if (!aligned(o->param, al) || !aligned(o->filt, al) || !aligned(o->resid, al) ||
+      !aligned(o->m, al) || !aligned(o->v, al))
+    return DPCLIP_ERR_UNSUPPORTED;
+  f->param = o->param;
+  f->filt = o->filt;
+  f->resid = o->resid;
+  f->m = o->m;
+  f->v = o->v;
+  f->lr = o->lr;
+  f->beta1 = o->beta1;
+  f->beta2 = o->beta2;
+  f->eps = o->eps;
+  f->eps_v = o->eps_v;
+  f->wd = o->weight_decay;
+  f->omega = o->omega;
+  f->calib = (float)((2.0 - o->omega) / (4.0 - 3.0 * o->omega) * o->noise_var);
+  f->inv_denom = 1.f / o->denom;
+  f->bc1 = (float)(1.0 / (1.0 - std::pow((double)o->beta1, o->step)));
+  f->bc2 = (float)(1.0 / (1.0 - std::pow((double)o->beta2, o->step)));
+  return DPCLIP_OK;
+}
+
 int check_noise_args(float C, float sigma) {
   if (!(C > 0.f) || !std::isfinite(C)) return DPCLIP_ERR_INVALID_ARG;
   if (!(sigma >= 0.f) || !std::isfinite(sigma)) return DPCLIP_ERR_INVALID_ARG;
   return DPCLIP_OK;
 }
-}  // namespace
-}  // namespace dpclip
 
-int dpclip_clipped_noisy_grad_ex(const void* A, const void* G, int B, int T, int d, int p,
-                                 int dtype, const float* sqnorms, float C, float sigma,
-                                 uint64_t seed, uint64_t offset, float* grad, float* scales,
-                                 uint8_t* clipped, const dpclip_sgd_update* update, void* ws,
-                                 size_t ws_bytes, dpclip_stream_t stream) {
+// The clipped noisy gradient from A and G, with at most one of an SGD update
+// and a FIBER step fused; grad may be null when neither stores it.
+int grad_impl(const void* A, const void* G, int B, int T, int d, int p, int dtype,
+              const float* sqnorms, float C, float sigma, uint64_t seed, uint64_t offset,
+              float* grad, float* scales, uint8_t* clipped, const dpclip_sgd_update* update,
+              const dpclip_fiber_adamw* fopt, void* ws, size_t ws_bytes, cudaStream_t s) {
   float upd_scale;
   DPCLIP_TRY(check_update(update, &upd_scale));
+  FiberDev fd{};
+  DPCLIP_TRY(make_fiber(fopt, &fd, dtype == DPCLIP_BF16));
   DPCLIP_TRY(check_noise_args(C, sigma));
   if (dtype != DPCLIP_F32 && dtype != DPCLIP_BF16) return DPCLIP_ERR_INVALID_ARG;
-  const bool need_grad = writes_grad(update) || dtype == DPCLIP_F32;
-  if (need_grad && !grad) return DPCLIP_ERR_INVALID_ARG;
+  const bool store = update ? update->store_grad != 0 : (fopt ? grad != nullptr : true);
+  if ((store || dtype == DPCLIP_F32) && !grad) return DPCLIP_ERR_INVALID_ARG;
   float* param = update ? update->param : nullptr;
-  cudaStream_t s = (cudaStream_t)stream;
+  const FiberDev* fp = fopt ? &fd : nullptr;
   if (B == 0) {   // an empty lot: the noise alone
     if (d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
-    DPCLIP_CUDA(launch_noise_only(writes_grad(update) ? grad : nullptr, param, (long long)d * p,
-                                  sigma * C, upd_scale, seed, 3u, offset, s));
+    DPCLIP_CUDA(launch_noise_only(store ? grad : nullptr, param, (long long)d * p, sigma * C,
+                                  upd_scale, seed, 3u, offset, fp, s));
     return DPCLIP_OK;
   }
   DPCLIP_TRY(check_shapes(A, G, B, T, d, p, dtype));
@@ -847,11 +883,13 @@ int dpclip_clipped_noisy_grad_ex(const void* A, const void* G, int B, int T, int
     gp.sigma = sigma;
     gp.seed = seed;
     gp.offset = offset;
-    gp.grad = writes_grad(update) ? grad : nullptr;
+    gp.grad = store ? grad : nullptr;
     gp.scales = scales;
     gp.clipped = clipped;
     gp.upd_param = param;
     gp.upd_scale = upd_scale;
+    gp.use_fiber = fopt ? 1 : 0;
+    gp.fiber = fd;
     gp.err = at<uint32_t>(ws, pl.ctrl);
     gp.tickets = at<uint32_t>(ws, pl.ctrl + 4);
     gp.slots = at<float>(ws, pl.off[0]);
@@ -875,7 +913,86 @@ int dpclip_clipped_noisy_grad_ex(const void* A, const void* G, int B, int T, int
     DPCLIP_CUDA(launch_noise_add(grad, (long long)d * p, sigma * C, seed, offset, s));
   if (scales || clipped) DPCLIP_CUDA(launch_clip_scales(sqnorms, B, C, scales, clipped, s));
   if (param) DPCLIP_CUDA(launch_sgd_update(param, grad, (long long)d * p, upd_scale, s));
+  if (fopt) DPCLIP_CUDA(launch_fiber(grad, (long long)d * p, fd, s));
   return DPCLIP_OK;
+}
+
+int stored_grad_impl(int B, int d, int p, const float* sqnorms, float C, float sigma,
+                     uint64_t seed, uint64_t offset, float* grad, float* scales, uint8_t* clipped,
+                     const dpclip_sgd_update* update, const dpclip_fiber_adamw* fopt,
+                     const void* ws, size_t ws_bytes, cudaStream_t s) {
+  float upd_scale;
+  DPCLIP_TRY(check_update(update, &upd_scale));
+  FiberDev fd{};
+  DPCLIP_TRY(make_fiber(fopt, &fd, true));
+  DPCLIP_TRY(check_noise_args(C, sigma));
+  if (B < 0 || d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  const bool store = update ? update->store_grad != 0 : (fopt ? grad != nullptr : true);
+  if (store && !grad) return DPCLIP_ERR_INVALID_ARG;
+  float* g = store ? grad : nullptr;
+  float* param = update ? update->param : nullptr;
+  const FiberDev* fp = fopt ? &fd : nullptr;
+  if ((g && !aligned(g, 16)) || (param && !aligned(param, 16)) || B > kMaxStoredB)
+    return DPCLIP_ERR_UNSUPPORTED;
+  if (B == 0) {
+    DPCLIP_CUDA(launch_noise_only(g, param, (long long)d * p, sigma * C, upd_scale, seed, 3u,
+                                  offset, fp, s));
+    return DPCLIP_OK;
+  }
+  if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
+  const long long stride = (long long)stored_stride(d, p);
+  DPCLIP_TRY(check_ws(ws, ws_bytes, kAlign + (size_t)B * stride * 4));
+  const float* M = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + kAlign);
+  DPCLIP_CUDA(launch_stored_grad(M, B, (long long)d * p, stride, sqnorms, C, sigma * C, seed,
+                                 offset, g, scales, clipped, param, upd_scale, fp, s));
+  return DPCLIP_OK;
+}
+
+int bias_clip_impl(const float* bias_grads, int B, int p, const float* sqnorms, float C,
+                   float sigma, uint64_t seed, uint64_t offset, float* grad_b,
+                   const dpclip_sgd_update* update, const dpclip_fiber_adamw* fopt,
+                   cudaStream_t s) {
+  float upd_scale;
+  DPCLIP_TRY(check_update(update, &upd_scale));
+  FiberDev fd{};
+  DPCLIP_TRY(make_fiber(fopt, &fd, false));
+  DPCLIP_TRY(check_noise_args(C, sigma));
+  if (B < 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
+  const bool store = update ? update->store_grad != 0 : (fopt ? grad_b != nullptr : true);
+  if (store && !grad_b) return DPCLIP_ERR_INVALID_ARG;
+  float* g = store ? grad_b : nullptr;
+  float* param = update ? update->param : nullptr;
+  const FiberDev* fp = fopt ? &fd : nullptr;
+  if (B > kMaxStoredB) return DPCLIP_ERR_UNSUPPORTED;
+  if (B == 0) {
+    DPCLIP_CUDA(launch_noise_only(g, param, p, sigma * C, upd_scale, seed, 4u, offset, fp, s));
+    return DPCLIP_OK;
+  }
+  if (!bias_grads || !sqnorms) return DPCLIP_ERR_INVALID_ARG;
+  DPCLIP_CUDA(launch_bias_clip(bias_grads, B, p, sqnorms, C, sigma * C, seed, offset, g, param,
+                               upd_scale, fp, s));
+  return DPCLIP_OK;
+}
+}  // namespace
+}  // namespace dpclip
+
+int dpclip_clipped_noisy_grad_ex(const void* A, const void* G, int B, int T, int d, int p,
+                                 int dtype, const float* sqnorms, float C, float sigma,
+                                 uint64_t seed, uint64_t offset, float* grad, float* scales,
+                                 uint8_t* clipped, const dpclip_sgd_update* update, void* ws,
+                                 size_t ws_bytes, dpclip_stream_t stream) {
+  return grad_impl(A, G, B, T, d, p, dtype, sqnorms, C, sigma, seed, offset, grad, scales,
+                   clipped, update, nullptr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int dpclip_clipped_noisy_grad_fiber(const void* A, const void* G, int B, int T, int d, int p,
+                                    int dtype, const float* sqnorms, float C, float sigma,
+                                    uint64_t seed, uint64_t offset, float* grad, float* scales,
+                                    uint8_t* clipped, const dpclip_fiber_adamw* opt, void* ws,
+                                    size_t ws_bytes, dpclip_stream_t stream) {
+  if (!opt) return DPCLIP_ERR_INVALID_ARG;
+  return grad_impl(A, G, B, T, d, p, dtype, sqnorms, C, sigma, seed, offset, grad, scales,
+                   clipped, nullptr, opt, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 int dpclip_clipped_noisy_grad(const void* A, const void* G, int B, int T, int d, int p, int dtype,
@@ -938,28 +1055,18 @@ int dpclip_stored_clipped_noisy_grad_ex(int B, int d, int p, const float* sqnorm
                                         float* scales, uint8_t* clipped,
                                         const dpclip_sgd_update* update, const void* ws,
                                         size_t ws_bytes, dpclip_stream_t stream) {
-  float upd_scale;
-  DPCLIP_TRY(check_update(update, &upd_scale));
-  DPCLIP_TRY(check_noise_args(C, sigma));
-  if (B < 0 || d <= 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
-  float* g = writes_grad(update) ? grad : nullptr;
-  float* param = update ? update->param : nullptr;
-  if (writes_grad(update) && !grad) return DPCLIP_ERR_INVALID_ARG;
-  if ((g && !aligned(g, 16)) || (param && !aligned(param, 16)) || B > kMaxStoredB)
-    return DPCLIP_ERR_UNSUPPORTED;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (B == 0) {
-    DPCLIP_CUDA(launch_noise_only(g, param, (long long)d * p, sigma * C, upd_scale, seed, 3u,
-                                  offset, s));
-    return DPCLIP_OK;
-  }
-  if (!sqnorms) return DPCLIP_ERR_INVALID_ARG;
-  const long long stride = (long long)stored_stride(d, p);
-  DPCLIP_TRY(check_ws(ws, ws_bytes, kAlign + (size_t)B * stride * 4));
-  const float* M = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + kAlign);
-  DPCLIP_CUDA(launch_stored_grad(M, B, (long long)d * p, stride, sqnorms, C, sigma * C, seed,
-                                 offset, g, scales, clipped, param, upd_scale, s));
-  return DPCLIP_OK;
+  return stored_grad_impl(B, d, p, sqnorms, C, sigma, seed, offset, grad, scales, clipped, update,
+                          nullptr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int dpclip_stored_clipped_noisy_grad_fiber(int B, int d, int p, const float* sqnorms, float C,
+                                           float sigma, uint64_t seed, uint64_t offset,
+                                           float* grad, float* scales, uint8_t* clipped,
+                                           const dpclip_fiber_adamw* opt, const void* ws,
+                                           size_t ws_bytes, dpclip_stream_t stream) {
+  if (!opt) return DPCLIP_ERR_INVALID_ARG;
+  return stored_grad_impl(B, d, p, sqnorms, C, sigma, seed, offset, grad, scales, clipped, nullptr,
+                          opt, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 int dpclip_stored_clipped_noisy_grad(int B, int d, int p, const float* sqnorms, float C,
@@ -992,23 +1099,17 @@ int dpclip_clipped_noisy_bias_grad_ex(const float* bias_grads, int B, int p, con
                                       float C, float sigma, uint64_t seed, uint64_t offset,
                                       float* grad_b, const dpclip_sgd_update* update,
                                       dpclip_stream_t stream) {
-  float upd_scale;
-  DPCLIP_TRY(check_update(update, &upd_scale));
-  DPCLIP_TRY(check_noise_args(C, sigma));
-  if (B < 0 || p <= 0) return DPCLIP_ERR_INVALID_ARG;
-  float* g = writes_grad(update) ? grad_b : nullptr;
-  float* param = update ? update->param : nullptr;
-  if (writes_grad(update) && !grad_b) return DPCLIP_ERR_INVALID_ARG;
-  if (B > kMaxStoredB) return DPCLIP_ERR_UNSUPPORTED;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (B == 0) {
-    DPCLIP_CUDA(launch_noise_only(g, param, p, sigma * C, upd_scale, seed, 4u, offset, s));
-    return DPCLIP_OK;
-  }
-  if (!bias_grads || !sqnorms) return DPCLIP_ERR_INVALID_ARG;
-  DPCLIP_CUDA(launch_bias_clip(bias_grads, B, p, sqnorms, C, sigma * C, seed, offset, g, param,
-                               upd_scale, s));
-  return DPCLIP_OK;
+  return bias_clip_impl(bias_grads, B, p, sqnorms, C, sigma, seed, offset, grad_b, update, nullptr,
+                        (cudaStream_t)stream);
+}
+
+int dpclip_clipped_noisy_bias_grad_fiber(const float* bias_grads, int B, int p,
+                                         const float* sqnorms, float C, float sigma,
+                                         uint64_t seed, uint64_t offset, float* grad_b,
+                                         const dpclip_fiber_adamw* opt, dpclip_stream_t stream) {
+  if (!opt) return DPCLIP_ERR_INVALID_ARG;
+  return bias_clip_impl(bias_grads, B, p, sqnorms, C, sigma, seed, offset, grad_b, nullptr, opt,
+                        (cudaStream_t)stream);
 }
 
 int dpclip_clipped_noisy_bias_grad(const float* bias_grads, int B, int p, const float* sqnorms,
@@ -1017,6 +1118,16 @@ int dpclip_clipped_noisy_bias_grad(const float* bias_grads, int B, int p, const 
   if (B <= 0) return DPCLIP_ERR_INVALID_ARG;
   return dpclip_clipped_noisy_bias_grad_ex(bias_grads, B, p, sqnorms, C, sigma, seed, offset,
                                            grad_b, nullptr, stream);
+}
+
+int dpclip_fiber_adamw_step(const float* grad, int64_t n, const dpclip_fiber_adamw* opt,
+                            dpclip_stream_t stream) {
+  if (!grad || n <= 0 || !opt) return DPCLIP_ERR_INVALID_ARG;
+  FiberDev fd{};
+  DPCLIP_TRY(make_fiber(opt, &fd, false));
+  if (!aligned(grad, 4)) return DPCLIP_ERR_UNSUPPORTED;
+  DPCLIP_CUDA(launch_fiber(grad, n, fd, (cudaStream_t)stream));
+  return DPCLIP_OK;
 }
 
 int dpclip_workspace_status(const void* ws, dpclip_stream_t stream) {

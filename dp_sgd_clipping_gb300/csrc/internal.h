@@ -94,6 +94,20 @@ struct FeatGemmParams {
 // gemm_dp: per output tile (128 d x 256 p) and sample i, acc_i = A_i^T G_i.
 //   grad mode:  grad = sum_i s_i acc_i + sigma*C*Z  (stored fp32 [d][p])
 //   norm mode:  part[(tile*B + i)*8 + w] = partial sum of acc_i^2
+// FIBER step on device (see dpclip_fiber_adamw): per element,
+// g = grad * inv_denom, then the innovation filter and calibrated AdamW.
+struct FiberDev {
+  float* param;
+  float* filt;
+  float* resid;
+  float* m;
+  float* v;
+  float lr, beta1, beta2, eps, eps_v, wd, omega;
+  float calib;        // A(omega) * noise_var
+  float inv_denom;
+  float bc1, bc2;     // 1 / (1 - beta^t)
+};
+
 struct GemmDpParams {
   CUtensorMap map_a;     // A [B][T][d], box {64, 64, 1}
   CUtensorMap map_g;     // G [B][T][p], box {64, 64, 1}
@@ -118,6 +132,8 @@ struct GemmDpParams {
   int accumulate;        // norm mode: sq[i] += the estimate (else =)
   float* upd_param;      // grad mode: if set, upd_param -= upd_scale * grad (grad may be null)
   float upd_scale;
+  int use_fiber;         // grad mode: apply the FIBER step to every gradient element
+  FiberDev fiber;
 };
 
 // ghost: per sample i and token tiles a <= b, sum((A_a A_b^T) o (G_a G_b^T)),
@@ -204,12 +220,15 @@ constexpr int kMaxStoredB = 12288;
 cudaError_t launch_stored_grad(const float* M, int B, long long n, long long stride,
                                const float* sq, float C, float nscale, uint64_t seed,
                                uint64_t offset, float* grad, float* scales, uint8_t* clipped,
-                               float* param, float upd_scale, cudaStream_t s);
+                               float* param, float upd_scale, const FiberDev* fiber,
+                               cudaStream_t s);
+// FIBER step over n elements of grad (fp32).
+cudaError_t launch_fiber(const float* grad, long long n, const FiberDev& f, cudaStream_t s);
 // grad (may be null) = nscale z (stream_id, element e), param (may be null)
 // -= upd_scale * that, e < n: the gradient of an empty lot.
 cudaError_t launch_noise_only(float* grad, float* param, long long n, float nscale,
                               float upd_scale, uint64_t seed, uint32_t stream_id, uint64_t offset,
-                              cudaStream_t s);
+                              const FiberDev* fiber, cudaStream_t s);
 // param[e] -= scale * grad[e], e < n.
 cudaError_t launch_sgd_update(float* param, const float* grad, long long n, float scale,
                               cudaStream_t s);
@@ -221,7 +240,7 @@ cudaError_t launch_bias_grads(const void* G, bool bf16, int B, int T, int p, flo
                               float* bias, float* sq, int accumulate, cudaStream_t s);
 cudaError_t launch_bias_clip(const float* bias, int B, int p, const float* sq, float C, float nscale,
                              uint64_t seed, uint64_t offset, float* grad_b, float* param,
-                             float upd_scale, cudaStream_t s);
+                             float upd_scale, const FiberDev* fiber, cudaStream_t s);
 // part[i * nblk + b] = sum of squares of chunk b of M_i (n elements at M + i * stride).
 cudaError_t launch_stored_sqnorm(const float* M, int B, long long n, long long stride, int nblk,
                                  float* part, cudaStream_t s);

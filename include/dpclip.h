@@ -233,6 +233,51 @@ int dpclip_clipped_noisy_bias_grad_ex(const float* bias_grads, int B, int p, con
                                       float* grad_b, const dpclip_sgd_update* update,
                                       dpclip_stream_t stream);
 
+/* FIBER ("Technical summary: FIBER", Method A and C): the privatized gradient
+ * g = grad / denom is filtered in innovation space, nu = g - gf,
+ * r = (1 - omega) r + omega nu, gf = gf + r, and AdamW runs on gf with the
+ * bias-corrected second moment reduced by the filtered noise variance,
+ * vbar = max(vhat - A(omega) noise_var, eps_v), A(omega) = (2 - omega) /
+ * (4 - 3 omega):  param -= lr (mhat / (sqrt(vbar) + eps) + weight_decay param).
+ * All tensors fp32 in the gradient's layout, device, updated in place; the
+ * four states start at zero before step 1.  0 < omega <= 1, step >= 1,
+ * denom > 0, noise_var >= 0 (for the clipped noisy sum of this library,
+ * (sigma C / denom)^2).  param/filt/resid/m/v 16-byte aligned for the weights. */
+typedef struct dpclip_fiber_adamw {
+  float* param;
+  float* filt;
+  float* resid;
+  float* m;
+  float* v;
+  float lr, beta1, beta2, eps, eps_v, weight_decay;
+  float omega;
+  float noise_var;
+  float denom;
+  int step;
+} dpclip_fiber_adamw;
+
+/* One FIBER step on n parameters from a gradient already formed (grad fp32
+ * [n], device). */
+int dpclip_fiber_adamw_step(const float* grad, int64_t n, const dpclip_fiber_adamw* opt,
+                            dpclip_stream_t stream);
+
+/* The gradient calls with the FIBER step fused where the gradient is formed
+ * (grad / grad_b may be NULL: not stored).  B = 0 as for the _ex calls. */
+int dpclip_clipped_noisy_grad_fiber(const void* A, const void* G, int B, int T, int d, int p,
+                                    int dtype, const float* sqnorms, float C, float sigma,
+                                    uint64_t seed, uint64_t offset, float* grad, float* scales,
+                                    uint8_t* clipped, const dpclip_fiber_adamw* opt, void* ws,
+                                    size_t ws_bytes, dpclip_stream_t stream);
+int dpclip_stored_clipped_noisy_grad_fiber(int B, int d, int p, const float* sqnorms, float C,
+                                           float sigma, uint64_t seed, uint64_t offset,
+                                           float* grad, float* scales, uint8_t* clipped,
+                                           const dpclip_fiber_adamw* opt, const void* ws,
+                                           size_t ws_bytes, dpclip_stream_t stream);
+int dpclip_clipped_noisy_bias_grad_fiber(const float* bias_grads, int B, int p,
+                                         const float* sqnorms, float C, float sigma,
+                                         uint64_t seed, uint64_t offset, float* grad_b,
+                                         const dpclip_fiber_adamw* opt, dpclip_stream_t stream);
+
 /* Clip scales alone: scales[i] = min(1, C / sqrt(sqnorms[i])) (1 when the norm
  * is 0) and clipped[i] = sqrt(sqnorms[i]) > C; either output may be NULL. */
 int dpclip_clip_scales(const float* sqnorms, int B, float C, float* scales, uint8_t* clipped,

@@ -140,6 +140,24 @@ def test_entry_points_reject_before_any_launch(L):
     assert cb(FAKE, 2, 16, FAKE, 0.0, 1.0, 1, 0, FAKE, None) == L.ERR_INVALID_ARG
     assert cb(None, 2, 16, FAKE, 1.0, 1.0, 1, 0, FAKE, None) == L.ERR_INVALID_ARG
     assert cb(FAKE, 20000, 16, FAKE, 1.0, 1.0, 1, 0, FAKE, None) == L.ERR_UNSUPPORTED
+    # FIBER: bad gain, step, missing state
+    fo = L.FiberAdamW(FAKE, FAKE, FAKE, FAKE, FAKE, 1e-3, 0.9, 0.999, 1e-8, 0.0, 0.0, 1.5, 0.0,
+                      1.0, 1)
+    assert lib.dpclip_fiber_adamw_step(FAKE, 16, ctypes.byref(fo), None) == L.ERR_INVALID_ARG
+    fo.omega = 0.5
+    fo.step = 0
+    assert lib.dpclip_fiber_adamw_step(FAKE, 16, ctypes.byref(fo), None) == L.ERR_INVALID_ARG
+    fo.step = 1
+    fo.m = None
+    assert lib.dpclip_fiber_adamw_step(FAKE, 16, ctypes.byref(fo), None) == L.ERR_INVALID_ARG
+    fo.m = FAKE
+    fo.v = FAKE + 4
+    assert lib.dpclip_clipped_noisy_grad_fiber(FAKE, FAKE, 2, 8, 16, 16, L.BF16, FAKE, 1.0, 1.0, 1,
+                                               0, None, None, None, ctypes.byref(fo), FAKE, big,
+                                               None) == L.ERR_UNSUPPORTED
+    assert lib.dpclip_stored_clipped_noisy_grad_fiber(2, 16, 16, FAKE, 1.0, 1.0, 1, 0, None, None,
+                                                      None, None, FAKE, big,
+                                                      None) == L.ERR_INVALID_ARG
     # stored direct norms and their gradient
     st = lib.dpclip_norms_direct_store
     assert st(FAKE, FAKE, 2, 8, 16, 16, L.BF16, 2, FAKE, FAKE, big, None) == L.ERR_INVALID_ARG

@@ -383,6 +383,84 @@ def test_empty_poisson_lot(api):
     np.testing.assert_allclose(host(beta), -lr / L * Db_ref, atol=1e-5)
 
 
+FIBER_HP = dict(lr=0.05, beta1=0.9, beta2=0.99, eps=1e-6, eps_v=1e-10, weight_decay=0.01,
+                omega=0.4)
+
+
+def _fiber_oracle_steps(theta0, grads, denom, noise_var, hp):
+    theta = theta0.astype(np.float64)
+    st = tuple(np.zeros_like(theta) for _ in range(4))
+    out = []
+    for t, g in enumerate(grads, start=1):
+        theta, st = O.fiber_adamw_step(theta, np.asarray(g, np.float64) / denom, st, t, hp["lr"],
+                                       hp["beta1"], hp["beta2"], hp["eps"], hp["eps_v"],
+                                       hp["weight_decay"], hp["omega"], noise_var)
+        out.append((theta, st))
+    return out
+
+
+def _check_fiber(opt, ref, theta0, rtol=2e-4):
+    theta_ref, (gf, r, m, v) = ref
+    scale = np.abs(theta_ref - theta0).max()
+    assert np.max(np.abs(host(opt.param) - theta_ref)) <= rtol * scale + 1e-6 * np.abs(theta0).max()
+    for got, want in ((opt.filt, gf), (opt.resid, r), (opt.m, m), (opt.v, v)):
+        assert np.max(np.abs(host(got) - want)) <= rtol * np.abs(want).max() + 1e-30
+
+
+def test_fiber_step_matches_oracle(api):
+    # the standalone step over several steps, 1003 elements (a ragged end)
+    rng = np.random.default_rng(7)
+    n, denom, nv = 1003, 4.0, 0.02
+    theta0 = rng.standard_normal(n).astype(np.float32)
+    grads = [4.0 * rng.standard_normal(n).astype(np.float32) for _ in range(4)]
+    opt = api.FiberAdamW(torch.tensor(theta0, device="cuda"), denom=denom, noise_var=nv,
+                         **FIBER_HP)
+    ref = _fiber_oracle_steps(theta0, grads, denom, nv, FIBER_HP)
+    for t, g in enumerate(grads):
+        api.fiber_step(torch.tensor(g, device="cuda"), opt)
+        _check_fiber(opt, ref[t], theta0)
+
+
+@pytest.mark.parametrize("path", ["gemm_bf16", "gemm_f32", "stored_bf16", "bias", "empty"])
+def test_fiber_fused(api, path):
+    # the FIBER step applied where the gradient is formed; the oracle's step is
+    # fed the gradient the GPU formed (its parity is tested above), so this
+    # checks the fused step itself over two steps of carried state
+    if path == "gemm_f32":
+        wl = W.Workload(170, "f32_odd", 3, 37, 29, 50, "f32", 1.0, 1.0, 1.0, 7, ())
+    else:
+        wl = W.Workload(176, "stored_ragged", 5, 300, 200, 328, "bf16", 1e-2, 1.0, 0.7, 8, ())
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    if path == "empty":
+        A, G = A[:0], G[:0]
+    q = torch.tensor(O.sqnorms_direct(inp.A, inp.G) + O.bias_sqnorms(inp.G), dtype=torch.float32,
+                     device="cuda")
+    C = float(np.median(np.sqrt(host(q))))
+    denom = 5.0
+    nv = (wl.sigma * C / denom) ** 2
+    shape = (wl.p,) if path == "bias" else (wl.d, wl.p)
+    theta0 = np.random.default_rng(8).standard_normal(shape).astype(np.float32)
+    opt = api.FiberAdamW(torch.tensor(theta0, device="cuda"), denom=denom, noise_var=nv,
+                         **FIBER_HP)
+    grads = []
+    if path == "stored_bf16":
+        _, stored = api.norms_direct_store(A, G)
+    if path == "bias":
+        _, bg = api.bias_grads(G)
+    for step in range(2):
+        if path == "stored_bf16":
+            g, _, _ = api.stored_clipped_noisy_grad(stored, q, C, wl.sigma, wl.seed, step, fiber=opt)
+        elif path == "bias":
+            g = api.clipped_noisy_bias_grad(bg, q, C, wl.sigma, wl.seed, step, fiber=opt)
+        else:
+            g, _, _ = api.clipped_noisy_grad(A, G, q[:A.shape[0]], C, wl.sigma, wl.seed, step,
+                                             fiber=opt)
+        grads.append(host(g).copy())
+        ref = _fiber_oracle_steps(theta0, grads, denom, nv, FIBER_HP)[-1]
+        _check_fiber(opt, ref, theta0)
+
+
 @pytest.mark.parametrize("case", ["bf16", "f32_rankdef"])
 def test_hutchpp_wide_layer(api, case):
     # p = 20000 (17001) rows: each CTA of the sample's cluster owns more rows
