@@ -322,9 +322,9 @@ def main():
             if name == "fiber_step":
                 return lambda: api.fiber_step(b["grad"], stored["fiber"])
             return lambda: api.clipped_noisy_grad(b["A"], b["G"], b["q_h"], wl.C, wl.sigma, wl.seed,
-                                                  step, scales=b["scales"], clipped=b["clipped"],
-                                                  ws=ws["clipped_noisy_grad"], fiber=stored["fiber"],
-                                                  store_grad=False)
+                                                  step, grad=b["grad"], scales=b["scales"],
+                                                  clipped=b["clipped"], ws=ws["clipped_noisy_grad"],
+                                                  fiber=stored["fiber"])
         if name == "stored_clipped_noisy_grad":
             if "h" not in stored:
                 row_fn("exact_direct_stored", step, bufs)()

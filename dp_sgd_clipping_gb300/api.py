@@ -153,7 +153,8 @@ def clipped_noisy_grad(A, G, sqnorms, C: float, sigma: float, seed: int, offset:
         raise ValueError("sqnorms must be a CUDA float32 tensor of B entries")
     nb = workspace_bytes(L.OP_CLIPPED_NOISY_GRAD, max(B, 1), T, d, p, dt, 0)
     ws = _workspace(nb, A.device, ws)
-    wants = update.store_grad if update is not None else (store_grad if fiber is not None else True)
+    # the GEMM path writes the gradient before a FIBER step, so it always stores it
+    wants = update.store_grad if update is not None else True
     if grad is None and (wants or dt == L.F32):
         grad = torch.empty(d, p, dtype=torch.float32, device=A.device)
     if want_scales:

@@ -212,7 +212,6 @@ __device__ __forceinline__ void store_with_noise(const GemmDpParams& p, int r, i
         w.w = fmaf(-p.upd_scale, o.w, w.w);
         *reinterpret_cast<float4*>(wrow + c) = w;
       }
-      if (p.use_fiber) fiber_update4(p.fiber, (size_t)r * p.p + c, o);
     }
   }
 }

@@ -132,8 +132,6 @@ struct GemmDpParams {
   int accumulate;        // norm mode: sq[i] += the estimate (else =)
   float* upd_param;      // grad mode: if set, upd_param -= upd_scale * grad (grad may be null)
   float upd_scale;
-  int use_fiber;         // grad mode: apply the FIBER step to every gradient element
-  FiberDev fiber;
 };
 
 // ghost: per sample i and token tiles a <= b, sum((A_a A_b^T) o (G_a G_b^T)),

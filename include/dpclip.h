@@ -261,8 +261,12 @@ typedef struct dpclip_fiber_adamw {
 int dpclip_fiber_adamw_step(const float* grad, int64_t n, const dpclip_fiber_adamw* opt,
                             dpclip_stream_t stream);
 
-/* The gradient calls with the FIBER step fused where the gradient is formed
- * (grad / grad_b may be NULL: not stored).  B = 0 as for the _ex calls. */
+/* The gradient calls followed by the FIBER step.  The stored-tile and bias
+ * calls fuse it into the pass that forms the gradient (grad / grad_b may
+ * then be NULL: not stored).  The GEMM call writes `grad` (required) and runs
+ * the step as one more pass over it: inside the GEMM epilogue the five state
+ * streams per element cost more than a separate HBM-bound pass.  B = 0 as
+ * for the _ex calls. */
 int dpclip_clipped_noisy_grad_fiber(const void* A, const void* G, int B, int T, int d, int p,
                                     int dtype, const float* sqnorms, float C, float sigma,
                                     uint64_t seed, uint64_t offset, float* grad, float* scales,
