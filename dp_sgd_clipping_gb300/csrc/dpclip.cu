@@ -200,7 +200,9 @@ Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
   return pl;
 }
 
-int dp_ntiles(int d, int p) { return cdiv(d, kDpTileM) * cdiv(p, kDpTileN); }
+// CTA tiles of the gradient / direct-norm GEMM (pairs of 128-row tiles).
+int dp_mtiles(int d) { return 2 * cdiv(d, 2 * kDpTileM); }
+int dp_ntiles(int d, int p) { return dp_mtiles(d) * cdiv(p, kDpTileN); }
 // ghost units per sample: for each 256-token tile b', the 128-token tiles
 // a <= 2b'+1 (bounded by the tile count).
 int ghost_npairs(int T) {
@@ -530,15 +532,14 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gp.T = T;
       gp.d = d;
       gp.p = p;
-      gp.mtiles = cdiv(d, kDpTileM);
+      gp.mtiles = dp_mtiles(d);
       gp.ntiles = cdiv(p, kDpTileN);
       gp.tblocks = cdiv(T, kBlockK);
       gp.part = at<float>(ws, pl.off[0]);
       gp.sq = sqnorms;
       gp.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gp.err = at<uint32_t>(ws, pl.ctrl);
-      const int ntiles = gp.mtiles * gp.ntiles;
-      DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min({ntiles * B, num_sms(), kMaxPersistentGrid}), s));
+      DPCLIP_CUDA(launch_gemm_dp(gp, false, s));
     } else {
       GhostParams gh;
       std::memset(&gh, 0, sizeof(gh));
@@ -878,7 +879,7 @@ int grad_impl(const void* A, const void* G, int B, int T, int d, int p, int dtyp
     gp.T = T;
     gp.d = d;
     gp.p = p;
-    gp.mtiles = cdiv(d, kDpTileM);
+    gp.mtiles = dp_mtiles(d);
     gp.ntiles = cdiv(p, kDpTileN);
     gp.tblocks = cdiv(T, kBlockK);
     gp.sqnorms = sqnorms;
@@ -894,12 +895,7 @@ int grad_impl(const void* A, const void* G, int B, int T, int d, int p, int dtyp
     gp.err = at<uint32_t>(ws, pl.ctrl);
     gp.tickets = at<uint32_t>(ws, pl.ctrl + 4);
     gp.slots = at<float>(ws, pl.off[0]);
-    const int ntiles = gp.mtiles * gp.ntiles;
-    // one CTA per SM, fewer when there is little work
-    const int grid = std::max(1, std::min({num_sms(), kMaxPersistentGrid, ntiles * B * 4}));
-    plan_grad_schedule(ntiles, B, gp.tblocks, grid, gp.waves, gp.ksplit, gp.kb_per_chunk,
-                       gp.vtotal);
-    DPCLIP_CUDA(launch_gemm_dp(gp, true, grid, s));
+    DPCLIP_CUDA(launch_gemm_dp(gp, true, s));
     if (fopt) DPCLIP_CUDA(launch_fiber(grad, (long long)d * p, fd, s));
     return DPCLIP_OK;
   }
@@ -1025,7 +1021,7 @@ int dpclip_norms_direct_store(const void* A, const void* G, int B, int T, int d,
     gp.T = T;
     gp.d = d;
     gp.p = p;
-    gp.mtiles = cdiv(d, kDpTileM);
+    gp.mtiles = dp_mtiles(d);
     gp.ntiles = cdiv(p, kDpTileN);
     gp.tblocks = cdiv(T, kBlockK);
     gp.part = at<float>(ws, pl.off[1]);
@@ -1034,8 +1030,7 @@ int dpclip_norms_direct_store(const void* A, const void* G, int B, int T, int d,
     gp.err = at<uint32_t>(ws, pl.ctrl);
     gp.pstore = M;
     gp.accumulate = accumulate;
-    const int ntiles = gp.mtiles * gp.ntiles;
-    DPCLIP_CUDA(launch_gemm_dp(gp, false, std::min({ntiles * B, num_sms(), kMaxPersistentGrid}), s));
+    DPCLIP_CUDA(launch_gemm_dp(gp, false, s));
     return DPCLIP_OK;
   }
   SimtParams sp = simt_base();

@@ -12,43 +12,59 @@
 //               to M_i = A_i^T G_i ([B][d][p] fp32): the clipped sum is then
 //               an elementwise pass over M instead of a second GEMM.
 //
-// Output tiles are 128 d-rows x 256 p-columns; both operands are MN-major
-// (tokens are the slow axis of A and G), loaded by TMA with 128-byte swizzle.
-// A work item is (tile, sample i, a range of that sample's 64-token
-// K-blocks); its accumulator lives in TMEM (256 columns) and two accumulators
-// alternate, so the epilogue of one item overlaps the mainloop of the next.
+// The tensor cores of two SMs work as a pair (a cluster of two CTAs, one
+// tcgen05.mma.cta_group::2 per 16 tokens): a pair tile is 256 d-rows x 256
+// p-columns.  CTA rank r loads, by TMA with 128-byte swizzle, its own 128
+// d-columns of A and p-columns [128 r, 128 r + 128) of the tile from G (both
+// operands MN-major: tokens are the slow axis of A and G), and holds rows
+// [128 r, 128 r + 128) of the product in its TMEM.  Each SM thus stages 32 KB
+// per 64 tokens instead of the 48 KB a one-CTA 128 x 256 tile needs, which
+// keeps shared-memory traffic (TMA writes plus tensor-core reads) within its
+// bandwidth.  A work item is (pair tile, sample i, a range of that sample's
+// 64-token K-blocks); its accumulator lives in TMEM (256 columns) and two
+// accumulators alternate, so the epilogue of one item overlaps the mainloop
+// of the next.  Both CTAs of a pair walk the same item sequence; everything
+// after the MMA (sums of squares, stores, tail tickets) is per CTA, on its
+// own 128-row half ("CTA tile" = pair tile * 2 + rank).
 //
-// Item sequences of a CTA (blockIdx c, grid G):
-//   norm mode: items are whole (tile, sample) units dealt one by one,
-//     sample-major (u = i * ntiles + tile; CTA c takes u = c, c + G, ...), so
-//     the CTAs running together share one sample's A and G slabs in L2.
-//   grad mode: first `waves` full waves of whole tiles (CTA c owns tiles
+// Item sequences of a pair (cluster c of G):
+//   norm mode: items are whole (pair tile, sample) units dealt one by one,
+//     sample-major (u = i * ntiles + tile; pair c takes u = c, c + G, ...),
+//     so the pairs running together share one sample's A and G slabs in L2.
+//   grad mode: first `waves` full waves of whole tiles (pair c owns tiles
 //     c, c + G, ...: all B samples of a tile, folded into a register running
 //     sum s_0 acc_0 + s_1 acc_1 + ... in fp32), then the remaining tiles are
 //     cut into (tile, sample, K-chunk) sub-units dealt in contiguous ranges,
-//     one range per CTA, so that every CTA gets the same amount of work.  A
+//     one range per pair, so that every pair gets the same amount of work.  A
 //     range covers whole tiles (finished directly) plus at most one partial
-//     tile at each end; a CTA writes each partial tile to its own workspace
-//     slot, takes an integer ticket on the tile, and the last CTA to arrive
-//     adds the slots of the tile in CTA order (a fixed order), adds the noise
-//     and stores.  No CTA ever waits on another.
+//     tile at each end; a CTA writes each partial half-tile to its own
+//     workspace slot, takes an integer ticket on its CTA tile, and the last
+//     CTA to arrive adds the slots of the CTA tile in pair order (a fixed
+//     order), adds the noise and stores.  No CTA ever waits on another pair.
 //
-// Roles (384 threads, three warpgroups): warp 0 = TMA producer, warp 1 = MMA
-// issuer and TMEM owner, warps 2-3 idle; warps 4..11 = epilogue (warp w reads
-// TMEM lanes 32*(w%4).., columns 128*((w-4)/4)..).  The grad epilogue keeps a
-// 128-float running sum per thread, so registers move from the first
-// warpgroup to the epilogue warpgroups (setmaxnreg: 40 and 232 per thread,
-// which adds up to the 168 per thread the block is launched with; the host
-// checks the compiled count before every launch).
+// Pipeline: the leader's `full` barrier of a stage counts the bytes of both
+// CTAs' loads; the MMA's completion is multicast to the `empty` barriers of
+// both CTAs and to both CTAs' `tfull`; each CTA's epilogue releases an
+// accumulator by arriving on the leader's `tempty`.
+//
+// Roles (384 threads, three warpgroups): warp 0 = TMA producer (both CTAs),
+// warp 1 = MMA issuer (rank 0) and TMEM owner, warps 2-3 idle; warps 4..11 =
+// epilogue (warp w reads TMEM lanes 32*(w%4).., columns 128*((w-4)/4)..).
+// The grad epilogue keeps a 128-float running sum per thread, so registers
+// move from the first warpgroup to the epilogue warpgroups (setmaxnreg: 40
+// and 232 per thread, which adds up to the 168 per thread the block is
+// launched with; the host checks the compiled count before every launch).
 #include "common.cuh"
 
 namespace dpclip {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr uint32_t kBox = 64 * 128;              // 64 tokens x 128 B (64 bf16)
-constexpr uint32_t kABytes = 2 * kBox;           // 128 d-columns
-constexpr uint32_t kGBytes = 4 * kBox;           // 256 p-columns
+constexpr uint32_t kABytes = 2 * kBox;           // this CTA's 128 d-columns
+constexpr uint32_t kGBytes = 2 * kBox;           // this CTA's 128 of the tile's 256 p-columns
+constexpr uint32_t kStageTx = 2 * (kABytes + kGBytes);   // both CTAs' loads of one stage
+constexpr uint16_t kPairMask = 0x3;              // both CTAs of the cluster
 constexpr int kThreads = 128 + 32 * kEpiWarps;   // 384: producer warpgroup + 2 epilogue
 constexpr int kEpiThreads = 32 * kEpiWarps;      // 256
 constexpr int kEpiWarp0 = 4;                     // first epilogue warp
@@ -115,35 +131,40 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 }
 
 struct Item {
-  int tile, i, kb0, kb1;
-  bool seg_first;   // first item of this CTA's part of the tile: reset the sum
-  bool seg_last;    // last item of this CTA's part of the tile: finish it
-  bool whole;       // this CTA holds every item of the tile
+  int tile, i, kb0, kb1;   // tile: pair tile
+  bool seg_first;   // first item of this pair's part of the tile: reset the sum
+  bool seg_last;    // last item of this pair's part of the tile: finish it
+  bool whole;       // this pair holds every item of the tile
+};
+
+// Position of this pair in the grid of pairs.
+struct PairPos {
+  int c, G;   // cluster index, number of clusters
 };
 
 // Stream-K range of the tail: sub-units [vb(c), vb(c+1)).
-__device__ __forceinline__ long long tail_begin(const GemmDpParams& p, int c) {
-  return (long long)c * p.vtotal / gridDim.x;
+__device__ __forceinline__ long long tail_begin(const GemmDpParams& p, int G, int c) {
+  return (long long)c * p.vtotal / G;
 }
-// CTA whose tail range holds sub-unit v.
-__device__ __forceinline__ int tail_owner(const GemmDpParams& p, long long v) {
-  const long long G = gridDim.x;
+// Pair whose tail range holds sub-unit v.
+__device__ __forceinline__ int tail_owner(const GemmDpParams& p, int G, long long v) {
   return (int)(((v + 1) * G + p.vtotal - 1) / p.vtotal - 1);
 }
-__device__ __forceinline__ bool tail_nonempty(const GemmDpParams& p, int c) {
-  return tail_begin(p, c) < tail_begin(p, c + 1);
+__device__ __forceinline__ bool tail_nonempty(const GemmDpParams& p, int G, int c) {
+  return tail_begin(p, G, c) < tail_begin(p, G, c + 1);
 }
-// Workspace slot of CTA c's partial of tail tile tt (its first or last tile).
-__device__ __forceinline__ int tail_slot(const GemmDpParams& p, int c, int tt) {
+// Workspace slot of pair c's partial of tail tile tt (its first or last
+// tile), half `rank`.
+__device__ __forceinline__ int tail_slot(const GemmDpParams& p, int G, int c, int tt, int rank) {
   const long long per_tile = (long long)p.B * p.ksplit;
-  return 2 * c + ((int)(tail_begin(p, c) / per_tile) == tt ? 0 : 1);
+  return 2 * (2 * c + ((int)(tail_begin(p, G, c) / per_tile) == tt ? 0 : 1)) + rank;
 }
 
-// The k-th item of this CTA; false past the end.
+// The k-th item of this pair; false past the end.
 template <bool kGrad>
-__device__ __forceinline__ bool item_at(const GemmDpParams& p, int k, Item& it) {
-  const int G = gridDim.x, c = blockIdx.x, B = p.B;
-  const int ntiles = p.mtiles * p.ntiles;
+__device__ __forceinline__ bool item_at(const GemmDpParams& p, const PairPos& pp, int k, Item& it) {
+  const int G = pp.G, c = pp.c, B = p.B;
+  const int ntiles = (p.mtiles >> 1) * p.ntiles;
   if (!kGrad) {
     const long long u = (long long)c + (long long)k * G;
     if (u >= (long long)ntiles * B) return false;
@@ -164,7 +185,7 @@ __device__ __forceinline__ bool item_at(const GemmDpParams& p, int k, Item& it) 
     it.whole = true;
     return true;
   }
-  const long long vb0 = tail_begin(p, c), vb1 = tail_begin(p, c + 1);
+  const long long vb0 = tail_begin(p, G, c), vb1 = tail_begin(p, G, c + 1);
   const long long v = vb0 + (k - (long long)p.waves * B);
   if (v >= vb1) return false;
   const long long per_tile = (long long)B * p.ksplit;
@@ -235,7 +256,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ntiles_total = p.mtiles * p.ntiles;
+  // clusters of (2, 1, 1) over a 1-D grid: CTA x is rank x % 2 of cluster x / 2
+  const int rank = (int)(blockIdx.x & 1u);
+  const PairPos pp{(int)(blockIdx.x >> 1), (int)(gridDim.x >> 1)};
+  const int mp = p.mtiles >> 1;   // pair tiles along d
+  const int ntiles_cta = p.mtiles * p.ntiles;
+  if (cluster_nctarank() != 2u || cluster_ctarank() != (uint32_t)rank) {
+    // not launched as clusters of two: nothing of the pair protocol may run
+    if (threadIdx.x == 0) record_error(p.err, DPCLIP_ERR_CUDA);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -244,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], kEpiThreads);
+      mbar_init(&ctl->tempty[a], 2 * kEpiThreads);
     }
     ctl->abort_flag = 0;
     ctl->issued = 0;
@@ -256,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     tma_prefetch_map(&p.map_a);
     tma_prefetch_map(&p.map_g);
   }
-  if (warp == 1) tmem_alloc(&ctl->tmem, 512);
+  if (warp == 1) tmem_alloc_pair(&ctl->tmem, 512);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before either uses the other's
   tc_fence_after();
   pdl_wait();   // inputs (A, G, sqnorms) may come from the previous kernel
   if (kGrad && blockIdx.x == 0) {
@@ -275,41 +305,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(&ctl->full[0]), 0);   // the leader's
       int it = 0;
       Item itm;
       bool run = true;
-      for (int k = 0; run && item_at<kGrad>(p, k, itm); ++k) {
-        const int d0 = (itm.tile % p.mtiles) * kDpTileM;
-        const int p0 = (itm.tile / p.mtiles) * kDpTileN;
+      for (int k = 0; run && item_at<kGrad>(p, pp, k, itm); ++k) {
+        const int d0 = (2 * (itm.tile % mp) + rank) * kDpTileM;
+        const int p0 = (itm.tile / mp) * kDpTileN + rank * (kDpTileN / 2);
         for (int kb = itm.kb0; kb < itm.kb1; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) {
             run = false;
             break;
           }
-          mbar_arrive_expect_tx(&ctl->full[s], kABytes + kGBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&ctl->full[s], kStageTx);
+          const uint32_t bar = full0 + (uint32_t)s * (uint32_t)sizeof(uint64_t);
           const int t0 = kb * 64;
           uint8_t* a = sA + s * kABytes;
           uint8_t* g = sG + s * kGBytes;
-          tma_load_3d(a, &p.map_a, &ctl->full[s], d0, t0, itm.i);
-          tma_load_3d(a + kBox, &p.map_a, &ctl->full[s], d0 + 64, t0, itm.i);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            tma_load_3d(g + q * kBox, &p.map_g, &ctl->full[s], p0 + 64 * q, t0, itm.i);
+          tma_load_3d_pair(a, &p.map_a, bar, d0, t0, itm.i);
+          tma_load_3d_pair(a + kBox, &p.map_a, bar, d0 + 64, t0, itm.i);
+          tma_load_3d_pair(g, &p.map_g, bar, p0, t0, itm.i);
+          tma_load_3d_pair(g + kBox, &p.map_g, bar, p0 + 64, t0, itm.i);
           ctl->issued = it + 1;
         }
       }
+      // producer tail: the MMA's release of every stage this CTA filled has
+      // arrived before the CTA may exit
+      if (run)
+        for (int j = it; j < it + kStages; ++j)
+          if (!mbar_wait(&ctl->empty[j % kStages], ((j / kStages) & 1) ^ 1, wc)) break;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 256, true, true);
-      int it = 0;
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(256, kDpTileN, true, true);
+      int it = 0, u = 0;
       Item itm;
       bool run = true;
-      for (int u = 0; run && item_at<kGrad>(p, u, itm); ++u) {
+      for (; run && item_at<kGrad>(p, pp, u, itm); ++u) {
         const int acc = u & 1;
-        if (!mbar_wait(&ctl->tempty[acc], ((u >> 1) & 1) ^ 1, wc)) break;
+        if (!mbar_wait_cluster(&ctl->tempty[acc], ((u >> 1) & 1) ^ 1, wc)) break;
         tc_fence_after();
         const uint32_t dt = tmem + (uint32_t)acc * 256u;
         for (int kb = itm.kb0; kb < itm.kb1; ++kb, ++it) {
@@ -324,15 +360,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
           const uint32_t g0 = smem_u32(sG + s * kGBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            umma_bf16(dt, sdesc_sw128(a0 + kk * 2048, kBox, 1024),
-                      sdesc_sw128(g0 + kk * 2048, kBox, 1024), idesc,
-                      (kb != itm.kb0 || kk != 0) ? 1u : 0u);
+            umma_bf16_pair(dt, sdesc_sw128(a0 + kk * 2048, kBox, 1024),
+                           sdesc_sw128(g0 + kk * 2048, kBox, 1024), idesc,
+                           (kb != itm.kb0 || kk != 0) ? 1u : 0u);
           }
-          umma_commit(&ctl->empty[s]);
+          umma_commit_pair(&ctl->empty[s], kPairMask);
         }
-        umma_commit(&ctl->tfull[acc]);
+        if (!run) break;
+        umma_commit_pair(&ctl->tfull[acc], kPairMask);
         ctl->mma_units = u + 1;
       }
+      // accumulator tail: both epilogues have released every accumulator
+      // (their arrivals target this CTA)
+      if (run)
+        for (int v = u; v < u + 2; ++v)
+          if (!mbar_wait_cluster(&ctl->tempty[v & 1], ((v >> 1) & 1) ^ 1, wc)) break;
     }
   }
   } else {
@@ -342,16 +384,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     const int quad = warp & 3;
     const int half = ew >> 2;
     const int etid = ew * 32 + lane;   // 0..255, same role in every CTA
+    const uint32_t tempty0 = mapa_shared(smem_u32(&ctl->tempty[0]), 0);
     float tot[128];
 #pragma unroll
     for (int j = 0; j < 128; ++j) tot[j] = 0.f;
     Item itm;
-    for (int u = 0; item_at<kGrad>(p, u, itm); ++u) {
+    for (int u = 0; item_at<kGrad>(p, pp, u, itm); ++u) {
       const int acc = u & 1;
       if (!epi_all(mbar_wait(&ctl->tfull[acc], (u >> 1) & 1, wc))) break;
       tc_fence_after();
       const uint32_t taddr =
           tmem + (uint32_t)acc * 256u + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
+      const uint32_t release = tempty0 + (uint32_t)acc * (uint32_t)sizeof(uint64_t);
+      const int ctile = 2 * itm.tile + rank;                     // this CTA's tile
+      const int row0 = (2 * (itm.tile % mp) + rank) * kDpTileM;  // its first d-row
+      const int col0 = (itm.tile / mp) * kDpTileN;               // the tile's first p-column
       if (kGrad) {
         const float si = clip_scale(p.sqnorms[itm.i], p.C);
 #pragma unroll
@@ -363,31 +410,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
             tot[c4 * 32 + j] = itm.seg_first ? si * v[j] : fmaf(si, v[j], tot[c4 * 32 + j]);
         }
         tc_fence_before();
-        mbar_arrive(&ctl->tempty[acc]);
+        mbar_arrive_remote(release);
         bool do_store = false;
         if (itm.seg_last) {
           do_store = itm.whole;
           if (!itm.whole) {
             // partial tile: publish this CTA's part; the last CTA to arrive
-            // adds every participant's part, in CTA order, and stores
-            const int tt = itm.tile - p.waves * (int)gridDim.x;
+            // on the CTA tile adds every participant's part, in pair order,
+            // and stores
+            const int tt = itm.tile - p.waves * pp.G;
             float4* slot = reinterpret_cast<float4*>(p.slots) +
-                           (size_t)tail_slot(p, blockIdx.x, tt) * (32 * kEpiThreads);
+                           (size_t)tail_slot(p, pp.G, pp.c, tt, rank) * (32 * kEpiThreads);
 #pragma unroll
             for (int jb = 0; jb < 32; ++jb)
               __stcg(slot + jb * kEpiThreads + etid,
                      make_float4(tot[4 * jb], tot[4 * jb + 1], tot[4 * jb + 2], tot[4 * jb + 3]));
             __threadfence();
             epi_sync();
-            // participants: the CTAs from the owner of the tile's first
+            // participants: the pairs from the owner of the tile's first
             // sub-unit to the owner of its last, skipping empty ranges
             const long long per_tile = (long long)p.B * p.ksplit;
-            const int c_lo = tail_owner(p, (long long)tt * per_tile);
-            const int c_hi = tail_owner(p, (long long)(tt + 1) * per_tile - 1);
+            const int c_lo = tail_owner(p, pp.G, (long long)tt * per_tile);
+            const int c_hi = tail_owner(p, pp.G, (long long)(tt + 1) * per_tile - 1);
             if (etid == 0) {
               int parts = 0;
-              for (int cc = c_lo; cc <= c_hi; ++cc) parts += tail_nonempty(p, cc) ? 1 : 0;
-              const uint32_t prev = atomicAdd(&p.tickets[itm.tile], 1u);
+              for (int cc = c_lo; cc <= c_hi; ++cc) parts += tail_nonempty(p, pp.G, cc) ? 1 : 0;
+              const uint32_t prev = atomicAdd(&p.tickets[ctile], 1u);
               ctl->combine = prev == (uint32_t)(parts - 1);
             }
             epi_sync();
@@ -396,9 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 #pragma unroll
               for (int j = 0; j < 128; ++j) tot[j] = 0.f;
               for (int cc = c_lo; cc <= c_hi; ++cc) {
-                if (!tail_nonempty(p, cc)) continue;
+                if (!tail_nonempty(p, pp.G, cc)) continue;
                 const float4* src = reinterpret_cast<const float4*>(p.slots) +
-                                    (size_t)tail_slot(p, cc, tt) * (32 * kEpiThreads);
+                                    (size_t)tail_slot(p, pp.G, cc, tt, rank) * (32 * kEpiThreads);
 #pragma unroll
                 for (int jb = 0; jb < 32; ++jb) {
                   const float4 v = __ldcg(src + jb * kEpiThreads + etid);
@@ -412,9 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
             }
           }
         }
-        if (do_store)
-          store_with_noise(p, (itm.tile % p.mtiles) * kDpTileM + quad * 32 + lane,
-                           (itm.tile / p.mtiles) * kDpTileN + half * 128, tot);
+        if (do_store) store_with_noise(p, row0 + quad * 32 + lane, col0 + half * 128, tot);
       } else {
         float ss = 0.f;
         if (p.pstore) {
@@ -425,15 +471,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(taddr + c4 * 32, v[c4]);
           tc_fence_before();
-          mbar_arrive(&ctl->tempty[acc]);
+          mbar_arrive_remote(release);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
             for (int j = 0; j < 32; ++j) ss = fmaf(v[c4][j], v[c4][j], ss);
           float* tb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctl) + sizeof(Ctl)) +
                       (size_t)ew * kStoreTileFloats;
-          const int r0 = (itm.tile % p.mtiles) * kDpTileM + quad * 32;
-          const int cb = (itm.tile / p.mtiles) * kDpTileN + half * 128;
+          const int r0 = row0 + quad * 32;
+          const int cb = col0 + half * 128;
           const int nrows = min(32, p.d - r0);
           float* mbase = p.pstore + ((size_t)itm.i * p.d + r0) * p.p;
 #pragma unroll
@@ -455,41 +501,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
             for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
           }
           tc_fence_before();
-          mbar_arrive(&ctl->tempty[acc]);
+          mbar_arrive_remote(release);
         }
         ss = warp_sum(ss);
-        if (lane == 0) p.part[((size_t)itm.tile * p.B + itm.i) * kEpiWarps + ew] = ss;
+        if (lane == 0) p.part[((size_t)ctile * p.B + itm.i) * kEpiWarps + ew] = ss;
       }
     }
   }
 
   if (!kGrad)
-    reduce_partials_last_cta(p.part, p.B, ntiles_total, p.B, 1, kEpiWarps, 1.f, p.sq, p.ticket,
+    reduce_partials_last_cta(p.part, p.B, ntiles_cta, p.B, 1, kEpiWarps, 1.f, p.sq, p.ticket,
                              ctl->red, &ctl->is_last, p.accumulate != 0);
 
   tc_fence_before();
-  __syncthreads();
-  if (ctl->abort_flag && threadIdx.x == 0) {
-    // bounded drain of async work still in flight (loads, MMAs)
-    const uint64_t lim = 100000000ull;
-    for (int it = ctl->consumed; it < ctl->issued; ++it) {
+  cluster_sync_all();   // every role of both CTAs has finished issuing
+  // after a timeout in either CTA: let the loads and MMAs still in flight
+  // (which may target the other CTA's barriers) land, boundedly
+  if (threadIdx.x == 0) {
+    int any_abort = ctl->abort_flag;
+    uint32_t peer_flag;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                 : "=r"(peer_flag)
+                 : "r"(mapa_shared(smem_u32(&ctl->abort_flag), (uint32_t)(rank ^ 1)))
+                 : "memory");
+    any_abort |= (int)peer_flag;
+    if (any_abort) {
+      const uint64_t lim = 100000000ull;
+      if (rank == 0) {
+        for (int it = ctl->consumed; it < ctl->issued; ++it) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&ctl->full[it % kStages], (uint32_t)(it / kStages) & 1u))
+            if (globaltimer_ns() - t0 > lim) break;
+        }
+        for (int a = 0; a < 2; ++a) {
+          // the last committed use of accumulator a
+          const int last_u = ctl->mma_units - 1 - ((ctl->mma_units - 1 - a) & 1);
+          if (last_u < 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&ctl->tfull[a], (uint32_t)(last_u >> 1) & 1u))
+            if (globaltimer_ns() - t0 > lim) break;
+        }
+      }
+      // arrivals multicast to this CTA, and the other CTA's loads, land
+      // within microseconds of the work above
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&ctl->full[it % kStages], (uint32_t)(it / kStages) & 1u))
-        if (globaltimer_ns() - t0 > lim) break;
-    }
-    for (int a = 0; a < 2; ++a) {
-      // the last committed use of accumulator a
-      const int last_u = ctl->mma_units - 1 - ((ctl->mma_units - 1 - a) & 1);
-      if (last_u < 0) continue;
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&ctl->tfull[a], (uint32_t)(last_u >> 1) & 1u))
-        if (globaltimer_ns() - t0 > lim) break;
+      while (globaltimer_ns() - t0 < 10000000ull) {
+      }
     }
   }
-  __syncthreads();
+  tc_fence_before();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -499,9 +563,9 @@ size_t gemm_dp_smem() { return kSmemBytes; }
 
 size_t gemm_dp_slot_bytes(int max_grid) { return (size_t)2 * max_grid * 32 * kEpiThreads * 16; }
 
-// Grad-mode schedule: full waves of whole tiles, then the K-split of the
-// remaining tiles (1, 2 or 4 chunks per sample) that best evens out the
-// per-CTA work.
+// Grad-mode schedule over `grid` pairs: full waves of whole pair tiles, then
+// the K-split of the remaining tiles (1, 2 or 4 chunks per sample) that best
+// evens out the per-pair work.
 void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ksplit,
                         int& kb_per_chunk, long long& vtotal) {
   waves = ntiles / grid;
@@ -512,7 +576,7 @@ void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, in
     const int kbc = (tblocks + want - 1) / want;
     const int ks = (tblocks + kbc - 1) / kbc;   // chunks actually used: none is empty
     const long long v = (long long)tail * B * ks;
-    // the busiest CTA's work in K-blocks
+    // the busiest pair's work in K-blocks
     const double span = (double)waves * B * tblocks + (double)((v + grid - 1) / grid) * kbc;
     if (span < best - 1e-9) {
       best = span;
@@ -533,21 +597,55 @@ cudaError_t check_regs(K kernel) {
   return fa.numRegs >= kRegsAtLaunch ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
-cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cudaStream_t s) {
-  cudaError_t e;
-  if ((e = check_regs(grad_mode ? gemm_dp_kernel<true> : gemm_dp_kernel<false>)) != cudaSuccess)
-    return e;
-  if (grad_mode) {
-    if ((e = cudaFuncSetAttribute(gemm_dp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kSmemBytes)) != cudaSuccess)
-      return e;
-    return launch_pdl(gemm_dp_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, 0, p);
+// Pairs that can be resident at once for a variant (clusters of two CTAs of
+// one SM each), per device.
+template <typename K>
+int max_pairs(K kernel, size_t smem, int slot) {
+  static int cache[16][3] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  if (cache[dev][slot] > 0) return cache[dev][slot];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * kMaxPersistentGrid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    return 0;
   }
-  const size_t smem = p.pstore ? kSmemBytesStore : kSmemBytes;
-  if ((e = cudaFuncSetAttribute(gemm_dp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem)) != cudaSuccess)
+  cache[dev][slot] = n;
+  return n;
+}
+
+cudaError_t launch_gemm_dp(const GemmDpParams& params, bool grad_mode, cudaStream_t s) {
+  GemmDpParams p = params;
+  if (p.mtiles % 2 != 0) return cudaErrorInvalidValue;
+  cudaError_t e;
+  auto kernel = grad_mode ? gemm_dp_kernel<true> : gemm_dp_kernel<false>;
+  if ((e = check_regs(kernel)) != cudaSuccess) return e;
+  const size_t smem = (!grad_mode && p.pstore) ? kSmemBytesStore : kSmemBytes;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
     return e;
-  return launch_pdl(gemm_dp_kernel<false>, dim3(grid), dim3(kThreads), smem, s, 0, p);
+  const int resident = max_pairs(kernel, smem, grad_mode ? 0 : (p.pstore ? 2 : 1));
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  const int ntiles = (p.mtiles / 2) * p.ntiles;   // pair tiles
+  // one pair per two SMs, fewer when there is little work
+  const long long work = (long long)ntiles * p.B * (grad_mode ? 4 : 1);
+  long long pairs_ll = std::min((long long)resident, (long long)(kMaxPersistentGrid / 2));
+  pairs_ll = std::max(1LL, std::min(pairs_ll, work));
+  const int pairs = (int)pairs_ll;
+  if (grad_mode)
+    plan_grad_schedule(ntiles, p.B, p.tblocks, pairs, p.waves, p.ksplit, p.kb_per_chunk, p.vtotal);
+  return launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, 2, p);
 }
 
 }  // namespace dpclip

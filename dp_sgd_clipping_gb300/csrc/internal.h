@@ -44,7 +44,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 constexpr int kTokTileM = 128;     // tokens per tok_gemm tile
 constexpr int kFeatTileM = 128;    // features per feat_gemm tile
 constexpr int kBlockK = 64;        // bf16 elements per 128-byte swizzled row
-constexpr int kDpTileM = 128;      // d rows per gradient / direct-norm tile
+constexpr int kDpTileM = 128;      // d rows per CTA of a gradient / direct-norm pair tile (256)
 constexpr int kDpTileN = 256;      // p columns per gradient / direct-norm tile
 constexpr int kGhostTile = 128;    // tokens per ghost Gram tile (both sides)
 constexpr int kEpiWarps = 8;       // epilogue warps of the persistent kernels
@@ -112,12 +112,12 @@ struct GemmDpParams {
   CUtensorMap map_a;     // A [B][T][d], box {64, 64, 1}
   CUtensorMap map_g;     // G [B][T][p], box {64, 64, 1}
   int B, T, d, p;
-  int mtiles, ntiles, tblocks;
-  // grad-mode schedule (plan_grad_schedule)
+  int mtiles, ntiles, tblocks;   // mtiles: 128-row CTA tiles along d (even: pairs of them)
+  // grad-mode schedule (set by launch_gemm_dp)
   int waves, ksplit, kb_per_chunk;
   long long vtotal;
-  float* slots;          // 2 * grid partial tiles of 128 x 256 fp32
-  uint32_t* tickets;     // [mtiles * ntiles], zero at launch
+  float* slots;          // 2 per CTA of the grid: partial CTA tiles of 128 x 256 fp32
+  uint32_t* tickets;     // [mtiles * ntiles] (CTA tiles), zero at launch
   const float* sqnorms;
   float C, sigma;
   uint64_t seed, offset;
@@ -194,7 +194,8 @@ struct SimtParams {
 // ----------------------------------------------------------------------------
 cudaError_t launch_tok_gemm(const TokGemmParams& p, cudaStream_t s);
 cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s);
-cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, int grid, cudaStream_t s);
+// Sizes the grid (CTA pairs) and, in grad mode, the schedule fields of p.
+cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, cudaStream_t s);
 cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s);
 cudaError_t launch_hpp_qr(const HppQrParams& p, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblocks_out);
