@@ -203,14 +203,10 @@ Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
 // CTA tiles of the gradient / direct-norm GEMM (pairs of 128-row tiles).
 int dp_mtiles(int d) { return 2 * cdiv(d, 2 * kDpTileM); }
 int dp_ntiles(int d, int p) { return dp_mtiles(d) * cdiv(p, kDpTileN); }
-// ghost units per sample: for each 256-token tile b', the 128-token tiles
-// a <= 2b'+1 (bounded by the tile count).
+// ghost units per sample: the 256-token tile pairs a' <= b'.
 int ghost_npairs(int T) {
-  const int ntt = cdiv(T, kGhostTile);
-  const int ntb = cdiv(T, 2 * kGhostTile);
-  int n = 0;
-  for (int bb = 0; bb < ntb; ++bb) n += std::min(2 * bb + 2, ntt);
-  return n;
+  const int n = cdiv(T, 2 * kGhostTile);
+  return n * (n + 1) / 2;
 }
 
 Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
@@ -218,12 +214,14 @@ Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
   Carve c;
   pl.ctrl_bytes = kAlign;
   pl.ctrl = c.take(pl.ctrl_bytes);
-  // ghost: whole units plus at most 8 sub-units for each unit of the last
-  // round (fewer than kMaxPersistentGrid units)
-  const size_t units = method == DPCLIP_EXACT_DIRECT
-                           ? (size_t)dp_ntiles(d, p) * B
-                           : (size_t)ghost_npairs(T) * B + 8 * (size_t)kMaxPersistentGrid;
-  pl.off[0] = c.take(units * kEpiWarps * 4);
+  // direct: one partial per CTA tile, sample and epilogue warp.  ghost: whole
+  // units plus at most 8 sub-units for each unit of the last round (fewer
+  // than one per pair), two CTAs x kEpiWarps partials each
+  const size_t parts =
+      method == DPCLIP_EXACT_DIRECT
+          ? (size_t)dp_ntiles(d, p) * B * kEpiWarps
+          : ((size_t)ghost_npairs(T) * B + 8 * (size_t)(kMaxPersistentGrid / 2)) * 2 * kEpiWarps;
+  pl.off[0] = c.take(parts * 4);
   pl.total = c.total();
   return pl;
 }
@@ -549,7 +547,6 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gh.T = T;
       gh.d = d;
       gh.p = p;
-      gh.ntt = cdiv(T, kGhostTile);
       gh.npairs = ghost_npairs(T);
       gh.dblocks = cdiv(d, kBlockK);
       gh.pblocks = cdiv(p, kBlockK);
@@ -557,9 +554,7 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gh.sq = sqnorms;
       gh.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gh.err = at<uint32_t>(ws, pl.ctrl);
-      const int grid = std::min({B * gh.npairs, num_sms(), kMaxPersistentGrid});
-      plan_ghost_schedule(gh, grid);
-      DPCLIP_CUDA(launch_ghost(gh, grid, s));
+      DPCLIP_CUDA(launch_ghost(gh, s));
     }
     return DPCLIP_OK;
   }

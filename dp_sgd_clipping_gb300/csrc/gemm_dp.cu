@@ -597,17 +597,41 @@ cudaError_t check_regs(K kernel) {
   return fa.numRegs >= kRegsAtLaunch ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
-// Pairs that can be resident at once for a variant (clusters of two CTAs of
-// one SM each), per device.
-template <typename K>
-int max_pairs(K kernel, size_t smem, int slot) {
-  static int cache[16][3] = {};
+cudaError_t launch_gemm_dp(const GemmDpParams& params, bool grad_mode, cudaStream_t s) {
+  GemmDpParams p = params;
+  if (p.mtiles % 2 != 0) return cudaErrorInvalidValue;
+  cudaError_t e;
+  auto kernel = grad_mode ? gemm_dp_kernel<true> : gemm_dp_kernel<false>;
+  if ((e = check_regs(kernel)) != cudaSuccess) return e;
+  const size_t smem = (!grad_mode && p.pstore) ? kSmemBytesStore : kSmemBytes;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  const int resident = max_resident_pairs(reinterpret_cast<const void*>(kernel), kThreads, smem,
+                                          grad_mode ? 0 : (p.pstore ? 2 : 1));
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  const int ntiles = (p.mtiles / 2) * p.ntiles;   // pair tiles
+  // one pair per two SMs, fewer when there is little work
+  const long long work = (long long)ntiles * p.B * (grad_mode ? 4 : 1);
+  long long pairs_ll = std::min((long long)resident, (long long)(kMaxPersistentGrid / 2));
+  pairs_ll = std::max(1LL, std::min(pairs_ll, work));
+  const int pairs = (int)pairs_ll;
+  if (grad_mode)
+    plan_grad_schedule(ntiles, p.B, p.tblocks, pairs, p.waves, p.ksplit, p.kb_per_chunk, p.vtotal);
+  return launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, 2, p);
+}
+
+// Pairs (clusters of two CTAs, one per SM) of a kernel variant that can be
+// resident at once, per device; `slot` names the variant for the cache.
+int max_resident_pairs(const void* kernel, int threads, size_t smem, int slot) {
+  static int cache[16][kPairSlots] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  if (slot < 0 || slot >= kPairSlots) return 0;
   if (cache[dev][slot] > 0) return cache[dev][slot];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * kMaxPersistentGrid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -623,29 +647,6 @@ int max_pairs(K kernel, size_t smem, int slot) {
   }
   cache[dev][slot] = n;
   return n;
-}
-
-cudaError_t launch_gemm_dp(const GemmDpParams& params, bool grad_mode, cudaStream_t s) {
-  GemmDpParams p = params;
-  if (p.mtiles % 2 != 0) return cudaErrorInvalidValue;
-  cudaError_t e;
-  auto kernel = grad_mode ? gemm_dp_kernel<true> : gemm_dp_kernel<false>;
-  if ((e = check_regs(kernel)) != cudaSuccess) return e;
-  const size_t smem = (!grad_mode && p.pstore) ? kSmemBytesStore : kSmemBytes;
-  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
-    return e;
-  const int resident = max_pairs(kernel, smem, grad_mode ? 0 : (p.pstore ? 2 : 1));
-  if (resident <= 0) return cudaErrorInvalidConfiguration;
-  const int ntiles = (p.mtiles / 2) * p.ntiles;   // pair tiles
-  // one pair per two SMs, fewer when there is little work
-  const long long work = (long long)ntiles * p.B * (grad_mode ? 4 : 1);
-  long long pairs_ll = std::min((long long)resident, (long long)(kMaxPersistentGrid / 2));
-  pairs_ll = std::max(1LL, std::min(pairs_ll, work));
-  const int pairs = (int)pairs_ll;
-  if (grad_mode)
-    plan_grad_schedule(ntiles, p.B, p.tblocks, pairs, p.waves, p.ksplit, p.kb_per_chunk, p.vtotal);
-  return launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, 2, p);
 }
 
 }  // namespace dpclip

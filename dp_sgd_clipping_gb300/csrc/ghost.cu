@@ -4,41 +4,48 @@
 // randomized-clipping summary (the ghost-clipping baseline of its "Problem
 // definition": O(T^2) per sample, no d x p tile ever formed).
 //
-// Work unit = (sample i, token tile a of 128 tokens, token tile b' of 256
-// tokens) covering the 128 x 128 blocks (a, 2b') and (a, 2b'+1) of the Gram
-// matrices; units with a <= 2b'+1 cover the upper triangle.  Two TMEM
-// accumulators of 128 x 256 fp32 (all 512 columns): X = A_a A_b'^T (K = d)
-// then Y = G_a G_b'^T (K = p), both K-major TMA tiles with 128-byte swizzle
-// (N = 256 keeps the tensor core's shared-memory reads at 96 B/clock; a
-// 128 x 128 tile needs 128 B/clock, the SM's limit).  The epilogue forms
-// sum(X o Y) per 128 x 128 block, weighted 2 above the diagonal (the mirrored
-// block), 1 on it, 0 below, and writes one partial per unit and epilogue
-// warp; the last CTA to finish adds the partials of each sample in a fixed
-// order.
+// Work unit = (sample i, token tiles a' <= b' of 256 tokens), run by a pair
+// of CTAs (a cluster of two, one tcgen05.mma.cta_group::2 per 16 features):
+// CTA rank r stages tokens [256 a' + 128 r, +128) of A (then G) as the M
+// half and tokens [256 b' + 128 r, +128) as the N half of the operands, and
+// its TMEM holds rows 256 a' + 128 r .. of X = A_a' A_b'^T (K = d, columns
+// 0..255) and of Y = G_a' G_b'^T (K = p, columns 256..511).  Both operands
+// are K-major TMA tiles with 128-byte swizzle; each SM stages 32 KB per 64
+// features, within its shared-memory bandwidth next to the tensor core's
+// reads.  The epilogue of CTA r forms sum(X o Y) over its two 128 x 128
+// blocks (2a'+r, 2b'+h), weighted 2 above the diagonal (the mirrored block),
+// 1 on it, 0 below, and writes one partial per unit, CTA and epilogue warp;
+// the last CTA to finish adds the partials of each sample in a fixed order.
 //
-// Units are dealt round-robin (unit u to CTA u mod G).  All units cost the
+// Units are dealt round-robin (unit u to pair u mod G).  All units cost the
 // same, so when their count is not a multiple of the grid the last round is
 // only partly busy; the units of that last round are therefore cut along p
 // into `tail_split` sub-units that each recompute X over all of d but only
 // a slice of Y's K range.  Because sum(X o Y) is linear in Y, the sub-units'
 // partial sums simply add up: no combine step is needed.
 //
-// Roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2..9 = epilogue.
+// Pipeline: the leader's (rank 0) `full` barrier counts both CTAs' loads;
+// the MMA's completion is multicast to both CTAs' `empty` and `tfull`; each
+// epilogue releases the accumulators on the leader's `tempty`.
+//
+// Roles (320 threads): warp 0 = TMA producer (both CTAs), warp 1 = MMA issuer
+// (rank 0) and TMEM owner, warps 2..9 = epilogue.
 #include "common.cuh"
 
 namespace dpclip {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr uint32_t kTileBytes = 128 * 128;   // 128 token rows x 128 B (one K block)
+constexpr uint32_t kStageTx = 4 * kTileBytes;   // both CTAs' two tiles of one stage
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint16_t kPairMask = 0x3;
 
 struct Ctl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull;
+  uint64_t tempty;
   uint32_t tmem;
   int abort_flag;
   int issued;
@@ -48,20 +55,18 @@ struct Ctl {
   float red[kThreads / 32];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * 3 * kTileBytes + sizeof(Ctl);
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * 2 * kTileBytes + sizeof(Ctl);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// unit index within a sample -> (a, b'): for b' = 0, 1, ... the tiles
-// a = 0 .. min(2b'+1, ntt-1).
-__device__ __forceinline__ void pair_of(int pr, int ntt, int& a, int& bb) {
+// unit index within a sample -> (a', b'): for b' = 0, 1, ... the tiles
+// a' = 0 .. b'.
+__device__ __forceinline__ void pair_of(int pr, int& a, int& bb) {
   int col = 0;
-  while (true) {
-    const int len = min(2 * col + 2, ntt);
-    if (pr < len) break;
-    pr -= len;
+  while (pr > col) {
+    pr -= col + 1;
     ++col;
   }
   a = pr;
@@ -94,20 +99,28 @@ __device__ __forceinline__ bool ghost_item(const GhostParams& p, int g, GhostIte
 __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constant__ GhostParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sP = smem;                              // 128 tokens of tile a
-  uint8_t* sQ = sP + kStages * kTileBytes;         // 256 tokens of tile b'
-  Ctl* ctl = reinterpret_cast<Ctl*>(sQ + kStages * 2 * kTileBytes);
+  uint8_t* sP = smem;                              // this CTA's 128 tokens of tile a'
+  uint8_t* sQ = sP + kStages * kTileBytes;         // its 128 tokens of tile b'
+  Ctl* ctl = reinterpret_cast<Ctl*>(sQ + kStages * kTileBytes);
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // clusters of (2, 1, 1) over a 1-D grid: CTA x is rank x % 2 of cluster x / 2
+  const int rank = (int)(blockIdx.x & 1u);
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  if (cluster_nctarank() != 2u || cluster_ctarank() != (uint32_t)rank) {
+    // not launched as clusters of two: nothing of the pair protocol may run
+    if (threadIdx.x == 0) record_error(p.err, DPCLIP_ERR_CUDA);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], 1);
     }
-    mbar_init(&ctl->tfull[0], 1);
-    mbar_init(&ctl->tempty[0], 32 * kEpiWarps);
+    mbar_init(&ctl->tfull, 1);
+    mbar_init(&ctl->tempty, 2 * 32 * kEpiWarps);
     ctl->abort_flag = 0;
     ctl->issued = 0;
     ctl->consumed = 0;
@@ -118,9 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
     tma_prefetch_map(&p.map_a);
     tma_prefetch_map(&p.map_g);
   }
-  if (warp == 1) tmem_alloc(&ctl->tmem, 512);
+  if (warp == 1) tmem_alloc_pair(&ctl->tmem, 512);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before either uses the other's
   tc_fence_after();
   pdl_wait();   // inputs may come from the previous kernel
   const uint32_t tmem = ctl->tmem;
@@ -128,13 +141,15 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(&ctl->full[0]), 0);   // the leader's
       int it = 0;
       bool run = true;
       GhostItem itm;
-      for (int g = blockIdx.x; run && ghost_item(p, g, itm); g += gridDim.x) {
+      for (int g = pair; run && ghost_item(p, g, itm); g += npairs) {
         const int i = itm.i;
         int a, b;
-        pair_of(itm.pr, p.ntt, a, b);
+        pair_of(itm.pr, a, b);
+        const int ta = (2 * a + rank) * kGhostTile, tb = (2 * b + rank) * kGhostTile;
         const int kblocks = p.dblocks + (itm.pb1 - itm.pb0);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
@@ -142,26 +157,33 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
             run = false;
             break;
           }
-          mbar_arrive_expect_tx(&ctl->full[s], 3 * kTileBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&ctl->full[s], kStageTx);
+          const uint32_t bar = full0 + (uint32_t)s * (uint32_t)sizeof(uint64_t);
           const bool on_a = kb < p.dblocks;
           const CUtensorMap* map = on_a ? &p.map_a : &p.map_g;
           const int k0 = (on_a ? kb : itm.pb0 + kb - p.dblocks) * kBlockK;
-          uint8_t* q = sQ + s * 2 * kTileBytes;
-          tma_load_3d(sP + s * kTileBytes, map, &ctl->full[s], k0, a * kGhostTile, i);
-          tma_load_3d(q, map, &ctl->full[s], k0, 2 * b * kGhostTile, i);
-          tma_load_3d(q + kTileBytes, map, &ctl->full[s], k0, (2 * b + 1) * kGhostTile, i);
+          tma_load_3d_pair(sP + s * kTileBytes, map, bar, k0, ta, i);
+          tma_load_3d_pair(sQ + s * kTileBytes, map, bar, k0, tb, i);
           ctl->issued = it + 1;
         }
       }
+      // producer tail: the MMA's release of every stage this CTA filled has
+      // arrived before the CTA may exit
+      if (run)
+        for (int j = it; j < it + kStages; ++j)
+          if (!mbar_wait(&ctl->empty[j % kStages], ((j / kStages) & 1) ^ 1, wc)) break;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 256, false, false);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(256, 256, false, false);
       int it = 0, lu = 0;
       bool run = true;
       GhostItem itm;
-      for (int g = blockIdx.x; run && ghost_item(p, g, itm); g += gridDim.x, ++lu) {
-        if (!mbar_wait(&ctl->tempty[0], (lu & 1) ^ 1, wc)) break;
+      for (int g = pair; run && ghost_item(p, g, itm); g += npairs, ++lu) {
+        if (!mbar_wait_cluster(&ctl->tempty, (lu & 1) ^ 1, wc)) {
+          run = false;
+          break;
+        }
         tc_fence_after();
         const int kblocks = p.dblocks + (itm.pb1 - itm.pb0);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
@@ -176,28 +198,34 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
           const int kl = on_a ? kb : kb - p.dblocks;
           const uint32_t dt = tmem + (on_a ? 0u : 256u);
           const uint32_t a0 = smem_u32(sP + s * kTileBytes);
-          const uint32_t b0 = smem_u32(sQ + s * 2 * kTileBytes);
+          const uint32_t b0 = smem_u32(sQ + s * kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(dt, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
-                      idesc, (kl | kk) != 0);
-          umma_commit(&ctl->empty[s]);
+            umma_bf16_pair(dt, sdesc_sw128(a0 + kk * 32, 16, 1024),
+                           sdesc_sw128(b0 + kk * 32, 16, 1024), idesc, (kl | kk) != 0);
+          umma_commit_pair(&ctl->empty[s], kPairMask);
         }
-        umma_commit(&ctl->tfull[0]);
+        if (!run) break;
+        umma_commit_pair(&ctl->tfull, kPairMask);
         ctl->mma_units = lu + 1;
       }
+      // accumulator tail: both epilogues have released the accumulators
+      // (their arrivals target this CTA)
+      if (run) mbar_wait_cluster(&ctl->tempty, (lu & 1) ^ 1, wc);
     }
   } else {
     const int ew = warp - 2;
     const int quad = warp & 3;
     const int half = ew >> 2;
+    const uint32_t release = mapa_shared(smem_u32(&ctl->tempty), 0);
     int lu = 0;
     GhostItem itm;
-    for (int g = blockIdx.x; ghost_item(p, g, itm); g += gridDim.x, ++lu) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[0], lu & 1, wc))) break;
+    for (int g = pair; ghost_item(p, g, itm); g += npairs, ++lu) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull, lu & 1, wc))) break;
       tc_fence_after();
-      int a, bb;
-      pair_of(itm.pr, p.ntt, a, bb);
+      int aa, bb;
+      pair_of(itm.pr, aa, bb);
+      const int a = 2 * aa + rank;                   // 128-token block of these rows
       const int b = 2 * bb + half;                   // 128-token block of these columns
       const float w = a < b ? 2.f : (a == b ? 1.f : 0.f);
       const uint32_t base = tmem + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
@@ -211,15 +239,17 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
         for (int j = 0; j < 32; ++j) s = fmaf(x[j], y[j], s);
       }
       tc_fence_before();
-      mbar_arrive(&ctl->tempty[0]);
+      mbar_arrive_remote(release);
       s = warp_sum(s);
-      if (lane == 0) p.part[(size_t)g * kEpiWarps + ew] = w * s;
+      if (lane == 0) p.part[((size_t)g * 2 + rank) * kEpiWarps + ew] = w * s;
     }
   }
 
   // per sample: its whole units [i*np, (i+1)*np) below nfull, then the
-  // sub-units of its units above nfull (item order = sample order)
+  // sub-units of its units above nfull (item order = sample order); each
+  // item has 2 * kEpiWarps partials (CTA rank, epilogue warp)
   {
+    constexpr int kPer = 2 * kEpiWarps;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) ctl->is_last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1u) ? 1 : 0;
@@ -230,15 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       for (int i = 0; i < p.B; ++i) {
         const int f0 = min(i * np, nf), f1 = min((i + 1) * np, nf);
         const int s0 = nf + (max(i * np, nf) - nf) * ts, s1 = nf + (max((i + 1) * np, nf) - nf) * ts;
-        const long long n1 = (long long)(f1 - f0) * kEpiWarps, n2 = (long long)(s1 - s0) * kEpiWarps;
+        const long long n1 = (long long)(f1 - f0) * kPer, n2 = (long long)(s1 - s0) * kPer;
         float acc = 0.f;
         for (long long e0 = threadIdx.x; e0 < n1 + n2; e0 += 8ll * blockDim.x) {
           float v[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const long long e = e0 + (long long)q * blockDim.x;
-            v[q] = e < n1 ? __ldcg(p.part + (size_t)f0 * kEpiWarps + e)
-                          : (e < n1 + n2 ? __ldcg(p.part + (size_t)s0 * kEpiWarps + (e - n1)) : 0.f);
+            v[q] = e < n1 ? __ldcg(p.part + (size_t)f0 * kPer + e)
+                          : (e < n1 + n2 ? __ldcg(p.part + (size_t)s0 * kPer + (e - n1)) : 0.f);
           }
 #pragma unroll
           for (int q = 0; q < 8; ++q) acc += v[q];
@@ -258,24 +288,39 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
   }
 
   tc_fence_before();
-  __syncthreads();
-  if (ctl->abort_flag && threadIdx.x == 0) {
-    const uint64_t lim = 100000000ull;
-    for (int it = ctl->consumed; it < ctl->issued; ++it) {
+  cluster_sync_all();   // every role of both CTAs has finished issuing
+  if (threadIdx.x == 0) {
+    // after a timeout in either CTA: let the loads and MMAs still in flight
+    // (which may target the other CTA's barriers) land, boundedly
+    uint32_t peer_flag;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                 : "=r"(peer_flag)
+                 : "r"(mapa_shared(smem_u32(&ctl->abort_flag), (uint32_t)(rank ^ 1)))
+                 : "memory");
+    if (ctl->abort_flag || peer_flag) {
+      const uint64_t lim = 100000000ull;
+      if (rank == 0) {
+        for (int it = ctl->consumed; it < ctl->issued; ++it) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&ctl->full[it % kStages], (uint32_t)(it / kStages) & 1u))
+            if (globaltimer_ns() - t0 > lim) break;
+        }
+        if (ctl->mma_units > 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&ctl->tfull, (uint32_t)(ctl->mma_units - 1) & 1u))
+            if (globaltimer_ns() - t0 > lim) break;
+        }
+      }
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&ctl->full[it % kStages], (uint32_t)(it / kStages) & 1u))
-        if (globaltimer_ns() - t0 > lim) break;
-    }
-    if (ctl->mma_units > 0) {
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&ctl->tfull[0], (uint32_t)(ctl->mma_units - 1) & 1u))
-        if (globaltimer_ns() - t0 > lim) break;
+      while (globaltimer_ns() - t0 < 10000000ull) {
+      }
     }
   }
-  __syncthreads();
+  tc_fence_before();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -283,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
 
 size_t ghost_smem() { return kSmemBytes; }
 
+// Tail split for `grid` pairs.
 void plan_ghost_schedule(GhostParams& p, int grid) {
   const int units = p.B * p.npairs;
   const int rounds = units / grid;
@@ -306,11 +352,17 @@ void plan_ghost_schedule(GhostParams& p, int grid) {
   }
 }
 
-cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_ghost(const GhostParams& params, cudaStream_t s) {
+  GhostParams p = params;
   cudaError_t e = cudaFuncSetAttribute(ghost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(ghost_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, 0, p);
+  const int resident =
+      max_resident_pairs(reinterpret_cast<const void*>(ghost_kernel), kThreads, kSmemBytes, 3);
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  const int pairs = std::max(1, std::min({resident, kMaxPersistentGrid / 2, p.B * p.npairs}));
+  plan_ghost_schedule(p, pairs);
+  return launch_pdl(ghost_kernel, dim3(2 * pairs), dim3(kThreads), kSmemBytes, s, 2, p);
 }
 
 }  // namespace dpclip

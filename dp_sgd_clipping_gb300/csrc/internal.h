@@ -8,6 +8,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <utility>
 
 #include "../../include/dpclip.h"
@@ -46,7 +47,7 @@ constexpr int kFeatTileM = 128;    // features per feat_gemm tile
 constexpr int kBlockK = 64;        // bf16 elements per 128-byte swizzled row
 constexpr int kDpTileM = 128;      // d rows per CTA of a gradient / direct-norm pair tile (256)
 constexpr int kDpTileN = 256;      // p columns per gradient / direct-norm tile
-constexpr int kGhostTile = 128;    // tokens per ghost Gram tile (both sides)
+constexpr int kGhostTile = 128;    // tokens per CTA of a ghost Gram pair tile (256 x 256)
 constexpr int kEpiWarps = 8;       // epilogue warps of the persistent kernels
 constexpr int kMaxNP = 32;         // widest skinny operand (probe columns)
 
@@ -134,16 +135,17 @@ struct GemmDpParams {
   float upd_scale;
 };
 
-// ghost: per sample i and token tiles a <= b, sum((A_a A_b^T) o (G_a G_b^T)),
-//   weighted 2 off the diagonal; part[u*8 + w] per unit u = i*npairs + pair.
+// ghost: per sample i and 256-token tiles a' <= b', sum((A_a' A_b'^T) o
+//   (G_a' G_b'^T)) over 128 x 128 blocks weighted 2 above the diagonal, 1 on
+//   it; part[(g*2 + rank)*8 + w] per work item g, CTA rank and epilogue warp.
 struct GhostParams {
   CUtensorMap map_a;     // box {64, 128, 1}
   CUtensorMap map_g;     // box {64, 128, 1}
   int B, T, d, p;
-  int ntt, npairs, dblocks, pblocks;
-  int nfull;             // units dealt whole (a multiple of the grid)
+  int npairs, dblocks, pblocks;   // npairs: units (a', b') per sample
+  int nfull;             // units dealt whole (a multiple of the grid of pairs)
   int tail_split, pb_per_split;   // the remaining units cut along p
-  float* part;           // [nfull + (B*npairs - nfull) * tail_split][8]
+  float* part;           // [nfull + (B*npairs - nfull) * tail_split][2][8]
   float* sq;             // per-sample result [B]
   uint32_t* ticket;      // zeroed grid ticket
   uint32_t* err;
@@ -196,7 +198,12 @@ cudaError_t launch_tok_gemm(const TokGemmParams& p, cudaStream_t s);
 cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s);
 // Sizes the grid (CTA pairs) and, in grad mode, the schedule fields of p.
 cudaError_t launch_gemm_dp(const GemmDpParams& p, bool grad_mode, cudaStream_t s);
-cudaError_t launch_ghost(const GhostParams& p, int grid, cudaStream_t s);
+// Sizes the grid (CTA pairs) and the tail schedule of p.
+cudaError_t launch_ghost(const GhostParams& p, cudaStream_t s);
+// Clusters of two CTAs of `kernel` that fit on the device at once (cached per
+// device and slot: 0 gradient, 1 direct norms, 2 stored norms, 3 ghost).
+constexpr int kPairSlots = 4;
+int max_resident_pairs(const void* kernel, int threads, size_t smem, int slot);
 cudaError_t launch_hpp_qr(const HppQrParams& p, cudaStream_t s);
 cudaError_t launch_simt(const SimtParams& p, int mode, cudaStream_t s, int* nblocks_out);
 int simt_nblocks(int M, int N);
