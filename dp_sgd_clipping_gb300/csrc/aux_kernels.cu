@@ -53,6 +53,15 @@ __global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_
   }
 }
 
+// Zeroes a call's control words (error word, tickets) once the previous
+// kernel of the stream has completed; a programmatic launch, so the call's
+// next kernel sets itself up meanwhile.
+__global__ void clear_words_kernel(uint32_t* w, int n) {
+  pdl_trigger();
+  pdl_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) w[i] = 0u;
+}
+
 __global__ void clip_scales_kernel(const float* sq, int B, float C, float* scales, uint8_t* clipped) {
   pdl_trigger();
   pdl_wait();
@@ -137,7 +146,7 @@ __global__ void stored_grad_kernel(const float* __restrict__ M, int B, long long
     }
     if (nscale != 0.f) {
       float z[4];
-      philox_normal4(seed, 3u, offset, (uint32_t)b, z);
+      philox_normal4_fast(seed, 3u, offset, (uint32_t)b, z);
       acc.x = fmaf(nscale, z[0], acc.x);
       acc.y = fmaf(nscale, z[1], acc.y);
       acc.z = fmaf(nscale, z[2], acc.z);
@@ -176,7 +185,7 @@ __global__ void noise_only_kernel(float* grad, float* param, long long n, float 
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblk;
        b += (long long)gridDim.x * blockDim.x) {
     float z[4] = {0.f, 0.f, 0.f, 0.f};
-    if (nscale != 0.f) philox_normal4(seed, stream_id, offset, (uint32_t)b, z);
+    if (nscale != 0.f) philox_normal4_fast(seed, stream_id, offset, (uint32_t)b, z);
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
       const long long e = 4 * b + l;
@@ -248,7 +257,7 @@ __global__ void noise_add_kernel(float* grad, long long n, float scale, uint64_t
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblk;
        b += (long long)gridDim.x * blockDim.x) {
     float z[4];
-    philox_normal4(seed, 3u, offset, (uint32_t)b, z);
+    philox_normal4_fast(seed, 3u, offset, (uint32_t)b, z);
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
       const long long e = 4 * b + l;
@@ -288,6 +297,12 @@ cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t ro
                       cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
   return launch_pdl(philox_fill_kernel<false>, dim3(grid), dim3(threads), 0, s, 0, out, rows,
                     cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
+}
+
+cudaError_t launch_clear_words(uint32_t* w, int n, cudaStream_t s) {
+  const int threads = 256;
+  const int grid = std::max(1, std::min((n + threads - 1) / threads, 152));
+  return launch_pdl(clear_words_kernel, dim3(grid), dim3(threads), 0, s, 0, w, n);
 }
 
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,

@@ -141,7 +141,7 @@ __global__ void bias_clip_kernel(const float* bias, int B, int p, const float* s
     }
     if (nscale != 0.f) {
       float z[4];
-      philox_normal4(seed, 4u, offset, (uint32_t)b, z);
+      philox_normal4_fast(seed, 4u, offset, (uint32_t)b, z);
 #pragma unroll
       for (int l = 0; l < 4; ++l) acc[l] = fmaf(nscale, z[l], acc[l]);
     }

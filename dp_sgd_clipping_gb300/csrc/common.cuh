@@ -385,6 +385,33 @@ __device__ __forceinline__ void philox_normal4(uint64_t seed, uint32_t stream, u
   z[3] = r2 * s;
 }
 
+// The same four normals with the SFU's approximate log2, sine and cosine
+// (absolute error of each value below 1e-5): the Gaussian mechanism's noise,
+// drawn by the million inside the gradient kernels, where the full-precision
+// transcendentals would cost as many issue slots as the rest of the epilogue.
+// Probes, whose bf16 rounding is compared exactly, keep philox_normal4.
+__device__ __forceinline__ void philox_normal4_fast(uint64_t seed, uint32_t stream,
+                                                    uint64_t offset, uint32_t blk,
+                                                    float (&z)[4]) {
+  const U4 x = philox4x32_10(U4{blk, stream, (uint32_t)offset, (uint32_t)(offset >> 32)},
+                             (uint32_t)seed, (uint32_t)(seed >> 32));
+  const float s24 = 5.9604644775390625e-08f;  // 2^-24
+  const float two_pi = 6.28318530717958647692f;
+  const float u0 = (float)((x.x >> 8) + 1u) * s24;
+  const float v1 = (float)(x.y >> 8) * s24;
+  const float u2 = (float)((x.z >> 8) + 1u) * s24;
+  const float v3 = (float)(x.w >> 8) * s24;
+  const float r0 = sqrtf(-2.0f * __logf(u0));
+  const float r2 = sqrtf(-2.0f * __logf(u2));
+  float s, c;
+  __sincosf(two_pi * v1, &s, &c);
+  z[0] = r0 * c;
+  z[1] = r0 * s;
+  __sincosf(two_pi * v3, &s, &c);
+  z[2] = r2 * c;
+  z[3] = r2 * s;
+}
+
 // Normal number `e` of a stream (used where elements are not block aligned).
 __device__ __forceinline__ float philox_normal_at(uint64_t seed, uint32_t stream, uint64_t offset,
                                                   uint64_t e) {

@@ -519,7 +519,7 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
   DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
   const int m = resolve_exact(method, T, d, p);
   cudaStream_t s = (cudaStream_t)stream;
-  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  DPCLIP_CUDA(launch_clear_words(at<uint32_t>(ws, pl.ctrl), (int)(pl.ctrl_bytes / 4), s));
   if (dtype == DPCLIP_BF16) {
     if (m == DPCLIP_EXACT_DIRECT) {
       GemmDpParams gp;
@@ -864,7 +864,7 @@ int grad_impl(const void* A, const void* G, int B, int T, int d, int p, int dtyp
   if (param && !aligned(param, dtype == DPCLIP_BF16 ? 16 : 4)) return DPCLIP_ERR_UNSUPPORTED;
   Plan pl = plan_grad(d, p, dtype);
   DPCLIP_TRY(check_ws(ws, ws_bytes, pl.total));
-  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  DPCLIP_CUDA(launch_clear_words(at<uint32_t>(ws, pl.ctrl), (int)(pl.ctrl_bytes / 4), s));
   if (dtype == DPCLIP_BF16) {
     GemmDpParams gp;
     std::memset(&gp, 0, sizeof(gp));
@@ -1006,7 +1006,7 @@ int dpclip_norms_direct_store(const void* A, const void* G, int B, int T, int d,
   cudaStream_t s = (cudaStream_t)stream;
   float* M = at<float>(ws, pl.off[0]);
   const long long stride = (long long)stored_stride(d, p);
-  DPCLIP_CUDA(cudaMemsetAsync(at<uint8_t>(ws, pl.ctrl), 0, pl.ctrl_bytes, s));
+  DPCLIP_CUDA(launch_clear_words(at<uint32_t>(ws, pl.ctrl), (int)(pl.ctrl_bytes / 4), s));
   if (dtype == DPCLIP_BF16) {
     GemmDpParams gp;
     std::memset(&gp, 0, sizeof(gp));

@@ -31,16 +31,19 @@
 //   norm mode: items are whole (pair tile, sample) units dealt one by one,
 //     sample-major (u = i * ntiles + tile; pair c takes u = c, c + G, ...),
 //     so the pairs running together share one sample's A and G slabs in L2.
-//   grad mode: first `waves` full waves of whole tiles (pair c owns tiles
-//     c, c + G, ...: all B samples of a tile, folded into a register running
-//     sum s_0 acc_0 + s_1 acc_1 + ... in fp32), then the remaining tiles are
-//     cut into (tile, sample, K-chunk) sub-units dealt in contiguous ranges,
-//     one range per pair, so that every pair gets the same amount of work.  A
+//   grad mode: `waves` full waves of whole tiles (pair c owns tiles c,
+//     c + G, ...: all B samples of a tile, folded into a register running
+//     sum s_0 acc_0 + s_1 acc_1 + ... in fp32), and the remaining tiles cut
+//     into (tile, sample, K-chunk) sub-units dealt in contiguous ranges, one
+//     range per pair, so that every pair gets the same amount of work.  A
 //     range covers whole tiles (finished directly) plus at most one partial
 //     tile at each end; a CTA writes each partial half-tile to its own
 //     workspace slot, takes an integer ticket on its CTA tile, and the last
 //     CTA to arrive adds the slots of the CTA tile in pair order (a fixed
 //     order), adds the noise and stores.  No CTA ever waits on another pair.
+//     Each pair runs its range of sub-units first: the partial tiles are then
+//     combined while the tensor cores work through the waves, and the kernel
+//     ends on whole tiles.
 //
 // Pipeline: the leader's `full` barrier of a stage counts the bytes of both
 // CTAs' loads; the MMA's completion is multicast to the `empty` barriers of
@@ -89,12 +92,19 @@ struct Ctl {
   float red[kThreads / 32];
 };
 
+static_assert(sizeof(Ctl) % 16 == 0, "staging tiles after Ctl must be 16-byte aligned");
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kABytes + kGBytes) + sizeof(Ctl);
 // Stored norm mode: one 32 x 33 fp32 transpose tile per epilogue warp, so
 // that each store instruction writes 32 consecutive floats of one row.
 constexpr size_t kStoreTileFloats = 32 * 33;
 constexpr size_t kSmemBytesStore = kSmemBytes + kEpiWarps * kStoreTileFloats * sizeof(float);
 static_assert(kSmemBytesStore <= 232448, "stored variant exceeds the shared memory of a CTA");
+// Grad mode: one 32-row x 16-column fp32 staging tile per epilogue warp (four
+// 16-byte blocks per row, their order swizzled by row so that both the
+// row-per-thread writes and the block-per-lane reads are free of bank
+// conflicts).
+constexpr size_t kGradTileFloats = 32 * 16;
+constexpr size_t kSmemBytesGrad = kSmemBytes + kEpiWarps * kGradTileFloats * sizeof(float);
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -102,12 +112,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __device__ __forceinline__ float clip_scale(float q, float C) {
   return q > 0.f ? fminf(1.f, C / sqrtf(q)) : 1.f;
-}
-
-__device__ __noinline__ void noise4(uint64_t seed, uint64_t offset, uint32_t blk, float4* z) {
-  float v[4];
-  philox_normal4(seed, 3u, offset, blk, v);
-  *z = make_float4(v[0], v[1], v[2], v[3]);
 }
 
 // Barrier among the 256 epilogue threads only (named barrier 1).
@@ -175,63 +179,87 @@ __device__ __forceinline__ bool item_at(const GemmDpParams& p, const PairPos& pp
     it.seg_first = it.seg_last = it.whole = true;
     return true;
   }
-  if (k < p.waves * B) {
-    it.tile = c + (k / B) * G;
-    it.i = k % B;
-    it.kb0 = 0;
-    it.kb1 = p.tblocks;
-    it.seg_first = it.i == 0;
-    it.seg_last = it.i == B - 1;
-    it.whole = true;
+  // first this pair's range of the tail sub-units, so that the partial tiles
+  // are combined while the tensor cores run the full waves; then the waves
+  const long long vb0 = tail_begin(p, G, c), vb1 = tail_begin(p, G, c + 1);
+  if (k < vb1 - vb0) {
+    const long long v = vb0 + k;
+    const long long per_tile = (long long)B * p.ksplit;
+    const int tt = (int)(v / per_tile);
+    const int rem = (int)(v % per_tile);
+    it.tile = p.waves * G + tt;
+    it.i = rem / p.ksplit;
+    const int ch = rem % p.ksplit;
+    it.kb0 = ch * p.kb_per_chunk;
+    it.kb1 = min(it.kb0 + p.kb_per_chunk, p.tblocks);
+    it.seg_first = v == vb0 || rem == 0;
+    it.seg_last = v == vb1 - 1 || rem == per_tile - 1;
+    it.whole = (long long)tt * per_tile >= vb0 && (long long)(tt + 1) * per_tile <= vb1;
     return true;
   }
-  const long long vb0 = tail_begin(p, G, c), vb1 = tail_begin(p, G, c + 1);
-  const long long v = vb0 + (k - (long long)p.waves * B);
-  if (v >= vb1) return false;
-  const long long per_tile = (long long)B * p.ksplit;
-  const int tt = (int)(v / per_tile);
-  const int rem = (int)(v % per_tile);
-  it.tile = p.waves * G + tt;
-  it.i = rem / p.ksplit;
-  const int ch = rem % p.ksplit;
-  it.kb0 = ch * p.kb_per_chunk;
-  it.kb1 = min(it.kb0 + p.kb_per_chunk, p.tblocks);
-  it.seg_first = v == vb0 || rem == 0;
-  it.seg_last = v == vb1 - 1 || rem == per_tile - 1;
-  it.whole = (long long)tt * per_tile >= vb0 && (long long)(tt + 1) * per_tile <= vb1;
+  const long long kw = k - (vb1 - vb0);
+  if (kw >= (long long)p.waves * B) return false;
+  it.tile = c + (int)(kw / B) * G;
+  it.i = (int)(kw % B);
+  it.kb0 = 0;
+  it.kb1 = p.tblocks;
+  it.seg_first = it.i == 0;
+  it.seg_last = it.i == B - 1;
+  it.whole = true;
   return true;
 }
 
-// Adds sigma C z to the running sum of one thread's 128 columns of row r and
-// stores them (columns beyond p are skipped; p is a multiple of 8).
-__device__ __forceinline__ void store_with_noise(const GemmDpParams& p, int r, int cb,
-                                                 const float (&tot)[128]) {
-  if (r >= p.d) return;
+// Finishes the warp's 32 x 128 block of the gradient: lane l holds, in tot,
+// columns cb .. cb+127 of row r0 + l.  Per 16-column chunk the rows go
+// through the staging tile; lane l then takes row 8g + l / 4 (g = 0..3) and
+// the 16-byte block l % 4 of the chunk, adds sigma C z from that block's
+// Philox draw (the gradient's row-major blocks of four: (r p + c) / 4), and
+// writes it (rows beyond d and columns beyond p skipped; p is a multiple of
+// 8), with the fused update theta -= (lr / L) g when asked.  The loop over
+// rows stays rolled, so one copy of the generator serves every block.
+__device__ __forceinline__ void store_block(const GemmDpParams& p, int r0, int cb,
+                                            const float (&tot)[128], float4* tb) {
+  const int lane = threadIdx.x & 31;
   const float nscale = p.sigma * p.C;
-  float* rowp = p.grad ? p.grad + (size_t)r * p.p : nullptr;
-  float* wrow = p.upd_param ? p.upd_param + (size_t)r * p.p : nullptr;
+  const int nrows = min(32, p.d - r0);
+  const int swz = (lane >> 1) & 3;
+#pragma unroll 1
+  for (int ch = 0; ch < 8; ++ch) {
+    __syncwarp();
 #pragma unroll
-  for (int jb = 0; jb < 32; ++jb) {
-    const int c = cb + 4 * jb;
-    if (c < p.p) {
-      float4 o = make_float4(tot[4 * jb], tot[4 * jb + 1], tot[4 * jb + 2], tot[4 * jb + 3]);
-      if (nscale != 0.f) {
-        float4 z;
-        noise4(p.seed, p.offset, (uint32_t)(((size_t)r * p.p + c) >> 2), &z);
-        o.x = fmaf(nscale, z.x, o.x);
-        o.y = fmaf(nscale, z.y, o.y);
-        o.z = fmaf(nscale, z.z, o.z);
-        o.w = fmaf(nscale, z.w, o.w);
+    for (int q8 = 0; q8 < 8; ++q8) {
+      if (q8 == ch) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          tb[lane * 4 + (q ^ swz)] = make_float4(tot[16 * q8 + 4 * q], tot[16 * q8 + 4 * q + 1],
+                                                 tot[16 * q8 + 4 * q + 2], tot[16 * q8 + 4 * q + 3]);
       }
-      if (rowp) *reinterpret_cast<float4*>(rowp + c) = o;
-      if (wrow) {
-        // the fused parameter update: theta -= (lr / L) g
-        float4 w = *reinterpret_cast<const float4*>(wrow + c);
-        w.x = fmaf(-p.upd_scale, o.x, w.x);
-        w.y = fmaf(-p.upd_scale, o.y, w.y);
-        w.z = fmaf(-p.upd_scale, o.z, w.z);
-        w.w = fmaf(-p.upd_scale, o.w, w.w);
-        *reinterpret_cast<float4*>(wrow + c) = w;
+    }
+    __syncwarp();
+    const int c = cb + 16 * ch + 4 * (lane & 3);
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      const int rl = 8 * g + (lane >> 2);
+      float4 v = tb[rl * 4 + ((lane & 3) ^ ((rl >> 1) & 3))];
+      if (rl < nrows && c < p.p) {
+        const size_t e = (size_t)(r0 + rl) * p.p + c;
+        if (nscale != 0.f) {
+          float z[4];
+          philox_normal4_fast(p.seed, 3u, p.offset, (uint32_t)(e >> 2), z);
+          v.x = fmaf(nscale, z[0], v.x);
+          v.y = fmaf(nscale, z[1], v.y);
+          v.z = fmaf(nscale, z[2], v.z);
+          v.w = fmaf(nscale, z[3], v.w);
+        }
+        if (p.grad) *reinterpret_cast<float4*>(p.grad + e) = v;
+        if (p.upd_param) {
+          float4 w = *reinterpret_cast<const float4*>(p.upd_param + e);
+          w.x = fmaf(-p.upd_scale, v.x, w.x);
+          w.y = fmaf(-p.upd_scale, v.y, w.y);
+          w.z = fmaf(-p.upd_scale, v.z, w.z);
+          w.w = fmaf(-p.upd_scale, v.w, w.w);
+          *reinterpret_cast<float4*>(p.upd_param + e) = w;
+        }
       }
     }
   }
@@ -460,7 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
             }
           }
         }
-        if (do_store) store_with_noise(p, row0 + quad * 32 + lane, col0 + half * 128, tot);
+        if (do_store && row0 + quad * 32 < p.d)
+          store_block(p, row0 + quad * 32, col0 + half * 128, tot,
+                      reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(ctl) + sizeof(Ctl)) +
+                          (size_t)ew * (kGradTileFloats / 4));
       } else {
         float ss = 0.f;
         if (p.pstore) {
@@ -603,7 +634,7 @@ cudaError_t launch_gemm_dp(const GemmDpParams& params, bool grad_mode, cudaStrea
   cudaError_t e;
   auto kernel = grad_mode ? gemm_dp_kernel<true> : gemm_dp_kernel<false>;
   if ((e = check_regs(kernel)) != cudaSuccess) return e;
-  const size_t smem = (!grad_mode && p.pstore) ? kSmemBytesStore : kSmemBytes;
+  const size_t smem = grad_mode ? kSmemBytesGrad : (p.pstore ? kSmemBytesStore : kSmemBytes);
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
       cudaSuccess)
     return e;

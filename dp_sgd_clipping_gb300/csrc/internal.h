@@ -215,6 +215,8 @@ cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t ro
                                bool bf16, uint64_t seed, uint32_t stream_id, uint64_t offset,
                                cudaStream_t s, uint32_t* zero = nullptr, int zero_words = 0,
                                int kind = 0);
+// Zeroes n control words after the stream's previous kernel (programmatic launch).
+cudaError_t launch_clear_words(uint32_t* w, int n, cudaStream_t s);
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
                                cudaStream_t s);
 // sq[i] = scale * sum_{u < nunits, w < nw} part[(u * su + i * si) * nw + w]
