@@ -41,7 +41,8 @@ EXTRA_ROWS = ("hutch_rademacher", "hutchpp_rademacher", "exact_direct_stored",
               "stored_clipped_noisy_grad", "bias_grads", "clipped_noisy_grad_sgd",
               "fiber_step", "clipped_noisy_grad_fiber")
 # kernels each ABI call launches for bf16 inputs (memsets of the control block excluded)
-LAUNCHES = {"hutch": 3, "hutchpp": 9, "exact_direct": 1, "exact_ghost": 1, "clipped_noisy_grad": 1}
+# kernels per call: the exact and gradient calls start with one that clears their control words
+LAUNCHES = {"hutch": 3, "hutchpp": 9, "exact_direct": 2, "exact_ghost": 2, "clipped_noisy_grad": 2}
 
 
 def algorithmic_work(wl):
@@ -514,6 +515,13 @@ def main():
         ms = extra_ms["exact_direct_stored"] + extra_ms["stored_clipped_noisy_grad"]
         extra["layer_exact_stored_total"] = {"ms": round(ms, 4),
                                              "tokens_per_s": B * T / (ms * 1e-3)}
+    # per-layer totals: one norm method, then clip + clipped noisy gradient
+    layer_totals = {}
+    if "clipped_noisy_grad" in row_ms:
+        for r in ("hutch", "hutchpp", "exact_direct", "exact_ghost"):
+            if r in row_ms:
+                ms = row_ms[r] + row_ms["clipped_noisy_grad"]
+                layer_totals[r + "+grad"] = {"ms": round(ms, 4), "tokens_per_s": B * T / (ms * 1e-3)}
     dom = max(rows, key=lambda r: row_ms[r])
     traffic = _traffic_from_profiles(dom)
     roof = dict(breakdown[dom])
@@ -527,7 +535,8 @@ def main():
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(wl), "gpu_launches": args.steps * sum(LAUNCHES[r] for r in rows),
-            "roofline": roofline, "breakdown": breakdown, "extra_rows": extra, "clocks": clk,
+            "roofline": roofline, "breakdown": breakdown, "layer_totals": layer_totals,
+            "extra_rows": extra, "clocks": clk,
             "e2e": e2e}
     if world == 1 and not args.no_cpu_baseline:
         v, t, threads, desc = cpu_baseline(wl, 1024, wl.p)
