@@ -57,6 +57,8 @@
 // move from the first warpgroup to the epilogue warpgroups (setmaxnreg: 40
 // and 232 per thread, which adds up to the 168 per thread the block is
 // launched with; the host checks the compiled count before every launch).
+#include <atomic>
+
 #include "common.cuh"
 
 namespace dpclip {
@@ -653,13 +655,15 @@ cudaError_t launch_gemm_dp(const GemmDpParams& params, bool grad_mode, cudaStrea
 }
 
 // Pairs (clusters of two CTAs, one per SM) of a kernel variant that can be
-// resident at once, per device; `slot` names the variant for the cache.
+// resident at once, per device; `slot` names the variant for the cache
+// (atomics: calls may come from several host threads).
 int max_resident_pairs(const void* kernel, int threads, size_t smem, int slot) {
-  static int cache[16][kPairSlots] = {};
+  static std::atomic<int> cache[16][kPairSlots];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
   if (slot < 0 || slot >= kPairSlots) return 0;
-  if (cache[dev][slot] > 0) return cache[dev][slot];
+  const int cached = cache[dev][slot].load(std::memory_order_relaxed);
+  if (cached > 0) return cached;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * kMaxPersistentGrid);
   cfg.blockDim = dim3(threads);
@@ -676,7 +680,7 @@ int max_resident_pairs(const void* kernel, int threads, size_t smem, int slot) {
     (void)cudaGetLastError();
     return 0;
   }
-  cache[dev][slot] = n;
+  cache[dev][slot].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -44,6 +44,8 @@
 
 #include <algorithm>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace dpclip {
@@ -447,9 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_consta
 
 // Largest cluster this kernel can be launched with on the current device:
 // 16 CTAs (a non-portable size) where the device has room for one, else 8.
+// Cached per device and shared-memory size (atomics: calls may come from
+// several host threads).
 int cluster_cap(size_t smem) {
-  static int cap = 0;
-  if (cap) return cap;
+  static std::atomic<int> cap[16];
+  static std::atomic<size_t> cap_smem[16];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) dev = 0;
+  const int cached = cap[dev].load(std::memory_order_acquire);
+  if (cached && cap_smem[dev].load(std::memory_order_relaxed) == smem) return cached;
   int c = 8;
   if (cudaFuncSetAttribute(hpp_qr_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
       cudaSuccess) {
@@ -468,8 +476,9 @@ int cluster_cap(size_t smem) {
     if (cudaOccupancyMaxActiveClusters(&n, hpp_qr_kernel, &cfg) == cudaSuccess && n > 0) c = 16;
   }
   (void)cudaGetLastError();
-  cap = c;
-  return cap;
+  cap_smem[dev].store(smem, std::memory_order_relaxed);
+  cap[dev].store(c, std::memory_order_release);
+  return c;
 }
 
 }  // namespace

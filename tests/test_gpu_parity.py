@@ -383,6 +383,31 @@ def test_empty_poisson_lot(api):
     np.testing.assert_allclose(host(beta), -lr / L * Db_ref, atol=1e-5)
 
 
+def test_gradient_noise_is_the_oracle_stream(api):
+    # With A = 0 (G = 0 for the bias) the clipped sum vanishes and each path
+    # returns sigma C z, z the Philox normals of its stream at element r p + c
+    # (stream 3) or c (stream 4).  The kernels draw them with the SFU's log2,
+    # sine and cosine: every value within 2e-5 of the fp64 transform.
+    C, sigma, seed, off = 2.0, 1.5, 0x5EED, 11
+    tol = 2e-5 * sigma * C
+    for dtype, (B, T, d, p) in ((torch.bfloat16, (3, 70, 200, 328)),
+                                (torch.float32, (2, 9, 24, 40))):
+        A = torch.zeros(B, T, d, dtype=dtype, device="cuda")
+        G = torch.randn(B, T, p, device="cuda").to(dtype)
+        q = torch.ones(B, device="cuda")
+        z = O.philox_normals(d * p, seed, 3, off).reshape(d, p)
+        g, _, _ = api.clipped_noisy_grad(A, G, q, C, sigma, seed, off)
+        assert np.max(np.abs(host(g) - sigma * C * z)) < tol, dtype
+        q2, stored = api.norms_direct_store(A, G)
+        gs, _, _ = api.stored_clipped_noisy_grad(stored, q, C, sigma, seed, off)
+        assert np.max(np.abs(host(gs) - sigma * C * z)) < tol, dtype
+    p = 520
+    zb = O.philox_normals(p, seed, 4, off)
+    _, bg = api.bias_grads(torch.zeros(2, 33, p, dtype=torch.bfloat16, device="cuda"))
+    gb = api.clipped_noisy_bias_grad(bg, torch.ones(2, device="cuda"), C, sigma, seed, off)
+    assert np.max(np.abs(host(gb) - sigma * C * zb)) < tol
+
+
 FIBER_HP = dict(lr=0.05, beta1=0.9, beta2=0.99, eps=1e-6, eps_v=1e-10, weight_decay=0.01,
                 omega=0.4)
 
