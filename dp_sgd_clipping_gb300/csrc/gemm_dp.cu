@@ -148,12 +148,15 @@ struct PairPos {
   int c, G;   // cluster index, number of clusters
 };
 
-// Stream-K range of the tail: sub-units [vb(c), vb(c+1)).
+// Stream-K range of the tail: sub-units [vb(c), vb(c+1)).  With tail_whole
+// (the tail is a partial wave of whole tiles) pair c < tail takes tile c.
 __device__ __forceinline__ long long tail_begin(const GemmDpParams& p, int G, int c) {
+  if (p.tail_whole) return (long long)min(c, (int)(p.vtotal / p.B)) * p.B;
   return (long long)c * p.vtotal / G;
 }
 // Pair whose tail range holds sub-unit v.
 __device__ __forceinline__ int tail_owner(const GemmDpParams& p, int G, long long v) {
+  if (p.tail_whole) return (int)(v / p.B);
   return (int)(((v + 1) * G + p.vtotal - 1) / p.vtotal - 1);
 }
 __device__ __forceinline__ bool tail_nonempty(const GemmDpParams& p, int G, int c) {
@@ -596,11 +599,16 @@ size_t gemm_dp_smem() { return kSmemBytes; }
 
 size_t gemm_dp_slot_bytes(int max_grid) { return (size_t)2 * max_grid * 32 * kEpiThreads * 16; }
 
-// Grad-mode schedule over `grid` pairs: full waves of whole pair tiles, then
-// the K-split of the remaining tiles (1, 2 or 4 chunks per sample) that best
-// evens out the per-pair work.
+// Grad-mode schedule over `grid` pairs: full waves of whole pair tiles, and
+// the remaining tiles either K-split (1, 2 or 4 chunks per sample, the split
+// that best evens out the per-pair work) or dealt whole, one per pair, as a
+// partial wave (tail_whole).  In a wave every pair works on the same sample
+// at the same time, so pairs that share A and G slabs find them in L2; the
+// sub-units of the split run on different samples and stream from HBM,
+// about twice as slowly per K-block (timestamps per unit).  The cheaper of
+// the two, with that factor, is taken.
 void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ksplit,
-                        int& kb_per_chunk, long long& vtotal) {
+                        int& kb_per_chunk, long long& vtotal, int& tail_whole) {
   waves = ntiles / grid;
   const int tail = ntiles - waves * grid;
   ksplit = 1;
@@ -610,12 +618,15 @@ void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, in
     const int ks = (tblocks + kbc - 1) / kbc;   // chunks actually used: none is empty
     const long long v = (long long)tail * B * ks;
     // the busiest pair's work in K-blocks
-    const double span = (double)waves * B * tblocks + (double)((v + grid - 1) / grid) * kbc;
+    const double span = (double)((v + grid - 1) / grid) * kbc;
     if (span < best - 1e-9) {
       best = span;
       ksplit = ks;
     }
   }
+  constexpr double kSplitSlowdown = 2.0;
+  tail_whole = tail > 0 && (double)B * tblocks <= kSplitSlowdown * best ? 1 : 0;
+  if (tail_whole) ksplit = 1;
   kb_per_chunk = (tblocks + ksplit - 1) / ksplit;
   vtotal = (long long)tail * B * ksplit;
 }
@@ -650,7 +661,8 @@ cudaError_t launch_gemm_dp(const GemmDpParams& params, bool grad_mode, cudaStrea
   pairs_ll = std::max(1LL, std::min(pairs_ll, work));
   const int pairs = (int)pairs_ll;
   if (grad_mode)
-    plan_grad_schedule(ntiles, p.B, p.tblocks, pairs, p.waves, p.ksplit, p.kb_per_chunk, p.vtotal);
+    plan_grad_schedule(ntiles, p.B, p.tblocks, pairs, p.waves, p.ksplit, p.kb_per_chunk, p.vtotal,
+                       p.tail_whole);
   return launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, 2, p);
 }
 

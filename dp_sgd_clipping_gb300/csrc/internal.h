@@ -117,6 +117,7 @@ struct GemmDpParams {
   // grad-mode schedule (set by launch_gemm_dp)
   int waves, ksplit, kb_per_chunk;
   long long vtotal;
+  int tail_whole;        // the tail is a partial wave of whole tiles (one per pair)
   float* slots;          // 2 per CTA of the grid: partial CTA tiles of 128 x 256 fp32
   uint32_t* tickets;     // [mtiles * ntiles] (CTA tiles), zero at launch
   const float* sqnorms;
@@ -265,7 +266,7 @@ size_t feat_gemm_smem(int NP);
 size_t gemm_dp_smem();
 size_t gemm_dp_slot_bytes(int max_grid);
 void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ksplit,
-                        int& kb_per_chunk, long long& vtotal);
+                        int& kb_per_chunk, long long& vtotal, int& tail_whole);
 constexpr int kMaxPersistentGrid = 160;   // CTAs of the persistent kernels (<= SMs)
 size_t ghost_smem();
 // Tail split of the ghost units for a grid: sets nfull, tail_split, pb_per_split.
