@@ -308,6 +308,18 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mas
       : "memory");
 }
 
+// Register reallocation between warpgroups (all threads of a warpgroup
+// execute it): dec gives registers back, inc takes them, up to the block's
+// launch allocation.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose
 // 1024-byte swizzle atoms start on 1024-byte boundaries.
 //   K-major operand (rows of 64 bf16 along K): lbo unused, sbo = byte step

@@ -270,15 +270,6 @@ __device__ __forceinline__ void store_block(const GemmDpParams& p, int r0, int c
   }
 }
 
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 template <bool kGrad>
 __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_constant__ GemmDpParams p) {
   extern __shared__ uint8_t smem_raw[];
