@@ -1,0 +1,69 @@
+"""The bench's output contract: one JSON line with the keys a driver reads.
+
+The reference arm (the fp64 oracle on a bounded sample) runs on the CPU in a
+few seconds; the library's arm needs a GPU.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(args, timeout):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, r.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+BASE_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+             "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e")
+
+
+def _check_common(line, steps, warmup):
+    for k in BASE_KEYS:
+        assert k in line, k
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["steps"] == steps and line["warmup"] == warmup and line["n_gpus"] == 1
+    assert line["scaling"] == "weak" and line["data"] == "synthetic"
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["config"]["workload"] == "up_proj_bf16_B4_T4096_d2048_p8192"
+    e2e = line["e2e"]
+    assert e2e["unit"] == "tokens/s" and e2e["value"] > 0
+    assert e2e["h2d_bytes_per_step"] >= 0 and e2e["d2h_bytes_per_step"] >= 0
+
+
+def test_reference_arm_line():
+    line = _run(["--impl", "reference", "--steps", "1", "--warmup", "3"], timeout=600)
+    _check_common(line, 1, 3)
+    assert line["impl"] == "reference" and line["dtype"] == "f64"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert "sample" in cb and cb["unit"] == "tokens/s"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.gpu
+def test_library_arm_line():
+    line = _run(["--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--no-extra"], timeout=900)
+    _check_common(line, 3, 3)
+    assert "impl" not in line or line["impl"] != "reference"
+    assert line["dtype"] == "bf16" and line["gpu_launches"] == 3 * 18
+    roof = line["roofline"]
+    assert roof["bound"] in ("hbm", "tensor") and roof["unit"] in ("GB/s", "TFLOP/s")
+    assert roof["achieved"] > 0 and roof["peak"] > 0
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
+    assert set(line["breakdown"]) == {"hutch", "hutchpp", "exact_direct", "exact_ghost",
+                                      "clipped_noisy_grad"}
+    assert set(line["layer_totals"]) == {"hutch+grad", "hutchpp+grad", "exact_direct+grad",
+                                         "exact_ghost+grad"}
+    assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
+    # the end-to-end leg moves the inputs in and the results out every step
+    assert line["e2e"]["h2d_bytes_per_step"] == 2 * 4 * 4096 * (2048 + 8192)
+    assert line["e2e"]["d2h_bytes_per_step"] >= 4 * 2048 * 8192
