@@ -549,9 +549,16 @@ def main():
 
 
 def _sha256(path):
+    """Digest of a source file's code: comments and whitespace are dropped, so
+    that a capture stays valid across comment edits but not code edits."""
     import hashlib
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    import re
+    with open(path, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = re.sub(r"\s+", " ", text).strip()
+    return hashlib.sha256(text.encode("utf-8")).hexdigest()
 
 
 def _traffic_from_profiles(row):

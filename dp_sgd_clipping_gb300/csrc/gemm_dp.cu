@@ -43,7 +43,11 @@
 //     order), adds the noise and stores.  No CTA ever waits on another pair.
 //     Each pair runs its range of sub-units first: the partial tiles are then
 //     combined while the tensor cores work through the waves, and the kernel
-//     ends on whole tiles.
+//     ends on whole tiles.  Where splitting would cost more than dealing the
+//     remaining tiles whole (tail_whole: pair c < tail takes tile c, all
+//     samples), the tail is that partial wave instead (plan_grad_schedule).
+//     The finished block leaves through a per-warp staging tile; the noise is
+//     drawn there, one Philox block of four columns per lane (store_block).
 //
 // Pipeline: the leader's `full` barrier of a stage counts the bytes of both
 // CTAs' loads; the MMA's completion is multicast to the `empty` barriers of
