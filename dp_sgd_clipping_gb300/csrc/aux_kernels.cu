@@ -17,8 +17,11 @@ template <bool kBf16>
 __global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
                                    uint64_t seed, uint32_t stream_id, uint64_t offset,
                                    uint32_t* zero, int zero_words, int kind) {
-  pdl_trigger();
+  // the first kernel of a Hutch / Hutch++ call: its dependents may read the
+  // call's inputs before their own wait, so they start only once everything
+  // before the call has completed
   pdl_wait();
+  pdl_trigger();
   if (zero)
     for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < zero_words; w += gridDim.x * blockDim.x)
       zero[w] = 0u;

@@ -130,19 +130,33 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_wait();   // inputs of this call may come from the previous kernel
+  // X (G or A) is an input of the call, and the call's first kernel starts
+  // its dependents only once everything before the call has completed: the
+  // first stages of X are requested before waiting for the previous kernel,
+  // whose output (W) they do not need.
+  const int nearly = min(kStages, nkb);
+  const uint32_t bytes = kXTileBytes + kWBytes * (p.has_lo ? 2u : 1u);
+  if (warp == 0 && lane == 0) {
+    for (int it = 0; it < nearly; ++it) {
+      mbar_arrive_expect_tx(&ctl->full[it], bytes);
+      tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it], (kb0 + it) * kBlockK,
+                  mt * kTokTileM, i);
+    }
+  }
+  pdl_wait();   // W may come from the previous kernel
   const uint32_t tmem = ctl->tmem;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
 
   if (warp == 0 && lane == 0) {
-    const uint32_t bytes = kXTileBytes + kWBytes * (p.has_lo ? 2u : 1u);
     const int wz = p.w_per_sample ? i : 0;
     for (int it = 0; it < nkb; ++it) {
       const int s = it % kStages;
-      if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
-      mbar_arrive_expect_tx(&ctl->full[s], bytes);
       const int f0 = (kb0 + it) * kBlockK;
-      tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, mt * kTokTileM, i);
+      if (it >= nearly) {
+        if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&ctl->full[s], bytes);
+        tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, mt * kTokTileM, i);
+      }
       tma_load_3d(sWhi + s * kWBytes, &p.map_whi, &ctl->full[s], f0, 0, wz);
       if (p.has_lo) tma_load_3d(sWlo + s * kWBytes, &p.map_wlo, &ctl->full[s], f0, 0, wz);
       ctl->issued = it + 1;
@@ -269,20 +283,34 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  pdl_wait();   // inputs of this call may come from the previous kernel
+  // X (A or G) is an input of the call: its first stages are requested
+  // before waiting for the previous kernel, whose output (Y) they do not
+  // need (see tok_gemm_kernel).
+  const int nearly = min(kStages, ntb);
+  const uint32_t bytes = kXTileBytes + 2 * kYBytes;
+  const int f0 = ft * kFeatTileM;
+  if (warp == 0 && lane == 0) {
+    for (int it = 0; it < nearly; ++it) {
+      const int t0 = (tb0 + it) * kBlockK;
+      mbar_arrive_expect_tx(&ctl->full[it], bytes);
+      tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it], f0, t0, i);
+      tma_load_3d(sX + it * kXTileBytes + kHalf, &p.map_x, &ctl->full[it], f0 + 64, t0, i);
+    }
+  }
+  pdl_wait();   // Y may come from the previous kernel
   const uint32_t tmem = ctl->tmem;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
 
   if (warp == 0 && lane == 0) {
-    const uint32_t bytes = kXTileBytes + 2 * kYBytes;
     for (int it = 0; it < ntb; ++it) {
       const int s = it % kStages;
-      if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
-      mbar_arrive_expect_tx(&ctl->full[s], bytes);
       const int t0 = (tb0 + it) * kBlockK;
-      const int f0 = ft * kFeatTileM;
-      tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, t0, i);
-      tma_load_3d(sX + s * kXTileBytes + kHalf, &p.map_x, &ctl->full[s], f0 + 64, t0, i);
+      if (it >= nearly) {
+        if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&ctl->full[s], bytes);
+        tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, t0, i);
+        tma_load_3d(sX + s * kXTileBytes + kHalf, &p.map_x, &ctl->full[s], f0 + 64, t0, i);
+      }
       tma_load_3d(sYhi + s * kYBytes, &p.map_yhi, &ctl->full[s], t0, 0, i);
       tma_load_3d(sYlo + s * kYBytes, &p.map_ylo, &ctl->full[s], t0, 0, i);
       ctl->issued = it + 1;
