@@ -12,10 +12,50 @@ namespace {
 // rows_valid rows (element e = j * cols + c uses Philox block e / 4, lane
 // e % 4), zeros below.  kind 0: standard normals (Box-Muller); kind 1:
 // Rademacher values, +1 / -1 by the top bit of the lane's word.  One thread
-// per Philox block of four elements.
+// per Philox block of four elements; one launch fills up to two such
+// matrices (jobs), the blocks of the second following those of the first.
+struct FillJob {
+  void* out;
+  int64_t rows, cols, rows_valid;
+  uint32_t stream_id;
+};
+struct FillJobs {
+  FillJob job[2];
+  int njobs;
+};
+
 template <bool kBf16>
-__global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_t rows_valid,
-                                   uint64_t seed, uint32_t stream_id, uint64_t offset,
+__device__ __forceinline__ void fill_block(const FillJob& j, int64_t b, uint64_t seed,
+                                           uint64_t offset, int kind) {
+  const int64_t nvalid = j.rows_valid * j.cols, ntotal = j.rows * j.cols;
+  float z[4] = {0.f, 0.f, 0.f, 0.f};
+  if (4 * b < nvalid) {
+    if (kind == 1) {
+      const U4 x = philox4x32_10(U4{(uint32_t)b, j.stream_id, (uint32_t)offset,
+                                    (uint32_t)(offset >> 32)},
+                                 (uint32_t)seed, (uint32_t)(seed >> 32));
+      z[0] = (x.x >> 31) ? -1.f : 1.f;
+      z[1] = (x.y >> 31) ? -1.f : 1.f;
+      z[2] = (x.z >> 31) ? -1.f : 1.f;
+      z[3] = (x.w >> 31) ? -1.f : 1.f;
+    } else {
+      philox_normal4(seed, j.stream_id, offset, (uint32_t)b, z);
+    }
+  }
+#pragma unroll
+  for (int l = 0; l < 4; ++l) {
+    const int64_t e = 4 * b + l;
+    if (e >= ntotal) break;
+    const float v = e < nvalid ? z[l] : 0.f;
+    if (kBf16)
+      static_cast<__nv_bfloat16*>(j.out)[e] = __float2bfloat16_rn(v);
+    else
+      static_cast<float*>(j.out)[e] = v;
+  }
+}
+
+template <bool kBf16>
+__global__ void philox_fill_kernel(const FillJobs jobs, uint64_t seed, uint64_t offset,
                                    uint32_t* zero, int zero_words, int kind) {
   // the first kernel of a Hutch / Hutch++ call: its dependents may read the
   // call's inputs before their own wait, so they start only once everything
@@ -25,34 +65,14 @@ __global__ void philox_fill_kernel(void* out, int64_t rows, int64_t cols, int64_
   if (zero)
     for (int w = blockIdx.x * blockDim.x + threadIdx.x; w < zero_words; w += gridDim.x * blockDim.x)
       zero[w] = 0u;
-  const int64_t nvalid = rows_valid * cols, ntotal = rows * cols;
-  const int64_t nblk = (ntotal + 3) / 4;
-  for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblk;
+  const int64_t nblk0 = (jobs.job[0].rows * jobs.job[0].cols + 3) / 4;
+  const int64_t nblk1 = jobs.njobs > 1 ? (jobs.job[1].rows * jobs.job[1].cols + 3) / 4 : 0;
+  for (int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; b < nblk0 + nblk1;
        b += (int64_t)gridDim.x * blockDim.x) {
-    float z[4] = {0.f, 0.f, 0.f, 0.f};
-    if (4 * b < nvalid) {
-      if (kind == 1) {
-        const U4 x = philox4x32_10(U4{(uint32_t)b, stream_id, (uint32_t)offset,
-                                      (uint32_t)(offset >> 32)},
-                                   (uint32_t)seed, (uint32_t)(seed >> 32));
-        z[0] = (x.x >> 31) ? -1.f : 1.f;
-        z[1] = (x.y >> 31) ? -1.f : 1.f;
-        z[2] = (x.z >> 31) ? -1.f : 1.f;
-        z[3] = (x.w >> 31) ? -1.f : 1.f;
-      } else {
-        philox_normal4(seed, stream_id, offset, (uint32_t)b, z);
-      }
-    }
-#pragma unroll
-    for (int l = 0; l < 4; ++l) {
-      const int64_t e = 4 * b + l;
-      if (e >= ntotal) break;
-      const float v = e < nvalid ? z[l] : 0.f;
-      if (kBf16)
-        static_cast<__nv_bfloat16*>(out)[e] = __float2bfloat16_rn(v);
-      else
-        static_cast<float*>(out)[e] = v;
-    }
+    if (b < nblk0)
+      fill_block<kBf16>(jobs.job[0], b, seed, offset, kind);
+    else
+      fill_block<kBf16>(jobs.job[1], b - nblk0, seed, offset, kind);
   }
 }
 
@@ -288,18 +308,40 @@ __global__ void wait_selftest_kernel(uint32_t* err, uint64_t limit_ns) {
 
 }  // namespace
 
-cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid, bool bf16,
-                               uint64_t seed, uint32_t stream_id, uint64_t offset, cudaStream_t s,
-                               uint32_t* zero, int zero_words, int kind) {
-  const int64_t nblk = (rows * cols + 3) / 4;
+namespace {
+cudaError_t launch_fill_jobs(const FillJobs& jobs, bool bf16, uint64_t seed, uint64_t offset,
+                             cudaStream_t s, uint32_t* zero, int zero_words, int kind) {
+  int64_t nblk = 0;
+  for (int j = 0; j < jobs.njobs; ++j) nblk += (jobs.job[j].rows * jobs.job[j].cols + 3) / 4;
   const int threads = 256;
   const int grid = (int)std::max<int64_t>(
       1, std::min<int64_t>((nblk + threads - 1) / threads, 152 * 16));
   if (bf16)
-    return launch_pdl(philox_fill_kernel<true>, dim3(grid), dim3(threads), 0, s, 0, out, rows,
-                      cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
-  return launch_pdl(philox_fill_kernel<false>, dim3(grid), dim3(threads), 0, s, 0, out, rows,
-                    cols, rows_valid, seed, stream_id, offset, zero, zero_words, kind);
+    return launch_pdl(philox_fill_kernel<true>, dim3(grid), dim3(threads), 0, s, 0, jobs, seed,
+                      offset, zero, zero_words, kind);
+  return launch_pdl(philox_fill_kernel<false>, dim3(grid), dim3(threads), 0, s, 0, jobs, seed,
+                    offset, zero, zero_words, kind);
+}
+}  // namespace
+
+cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t rows_valid, bool bf16,
+                               uint64_t seed, uint32_t stream_id, uint64_t offset, cudaStream_t s,
+                               uint32_t* zero, int zero_words, int kind) {
+  FillJobs jobs{};
+  jobs.job[0] = FillJob{out, rows, cols, rows_valid, stream_id};
+  jobs.njobs = 1;
+  return launch_fill_jobs(jobs, bf16, seed, offset, s, zero, zero_words, kind);
+}
+
+cudaError_t launch_philox_fill2(void* out0, int64_t rows0, int64_t valid0, uint32_t stream0,
+                                void* out1, int64_t rows1, int64_t valid1, uint32_t stream1,
+                                int64_t cols, bool bf16, uint64_t seed, uint64_t offset,
+                                cudaStream_t s, uint32_t* zero, int zero_words, int kind) {
+  FillJobs jobs{};
+  jobs.job[0] = FillJob{out0, rows0, cols, valid0, stream0};
+  jobs.job[1] = FillJob{out1, rows1, cols, valid1, stream1};
+  jobs.njobs = 2;
+  return launch_fill_jobs(jobs, bf16, seed, offset, s, zero, zero_words, kind);
 }
 
 cudaError_t launch_clear_words(uint32_t* w, int n, cudaStream_t s) {

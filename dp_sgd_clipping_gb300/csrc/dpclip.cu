@@ -654,8 +654,8 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
   if (dtype == DPCLIP_BF16) {
     void* S = at<void>(ws, pl.off[kS]);
     void* Gp = at<void>(ws, pl.off[kGp]);
-    DPCLIP_CUDA(launch_philox_fill(S, 16, p, r, true, seed, 1u, offset, s, ctrl, ctrl_words, probe));
-    DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, true, seed, 2u, offset, s, nullptr, 0, probe));
+    DPCLIP_CUDA(launch_philox_fill2(S, 16, r, 1u, Gp, m, m, 2u, p, true, seed, offset, s, ctrl,
+                                    ctrl_words, probe));
     void *Y1h = at<void>(ws, pl.off[kY1hi]), *Y1l = at<void>(ws, pl.off[kY1lo]);
     void *Z1h = at<void>(ws, pl.off[kZ1hi]), *Z1l = at<void>(ws, pl.off[kZ1lo]);
     void *Uh = at<void>(ws, pl.off[kUhi]), *Ul = at<void>(ws, pl.off[kUlo]);
@@ -702,8 +702,8 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
   float* V = at<float>(ws, pl.off[kFV]);
   float* QW = at<float>(ws, pl.off[kFQW]);
   float* Y3 = at<float>(ws, pl.off[kFY3]);
-  DPCLIP_CUDA(launch_philox_fill(S, r, p, r, false, seed, 1u, offset, s, ctrl, ctrl_words, probe));
-  DPCLIP_CUDA(launch_philox_fill(Gp, m, p, m, false, seed, 2u, offset, s, nullptr, 0, probe));
+  DPCLIP_CUDA(launch_philox_fill2(S, r, r, 1u, Gp, m, m, 2u, p, false, seed, offset, s, ctrl,
+                                  ctrl_words, probe));
   int nb = 0;
   SimtParams sp = simt_base();
   // Y1 = G S

@@ -216,6 +216,11 @@ cudaError_t launch_philox_fill(void* out, int64_t rows, int64_t cols, int64_t ro
                                bool bf16, uint64_t seed, uint32_t stream_id, uint64_t offset,
                                cudaStream_t s, uint32_t* zero = nullptr, int zero_words = 0,
                                int kind = 0);
+// Two fills (same columns, seed, offset and kind) in one launch.
+cudaError_t launch_philox_fill2(void* out0, int64_t rows0, int64_t valid0, uint32_t stream0,
+                                void* out1, int64_t rows1, int64_t valid1, uint32_t stream1,
+                                int64_t cols, bool bf16, uint64_t seed, uint64_t offset,
+                                cudaStream_t s, uint32_t* zero, int zero_words, int kind);
 // Zeroes n control words after the stream's previous kernel (programmatic launch).
 cudaError_t launch_clear_words(uint32_t* w, int n, cudaStream_t s);
 cudaError_t launch_clip_scales(const float* sq, int B, float C, float* scales, uint8_t* clipped,
