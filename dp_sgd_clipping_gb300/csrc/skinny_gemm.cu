@@ -136,11 +136,14 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
   // whose output (W) they do not need.
   const int nearly = min(kStages, nkb);
   const uint32_t bytes = kXTileBytes + kWBytes * (p.has_lo ? 2u : 1u);
+  // each tile walks its K-blocks from its own starting point, so that the
+  // CTAs in flight spread their row segments over the memory channels
+  const int rot = nkb > 0 ? (int)(((unsigned)tile * 5u) % (unsigned)nkb) : 0;
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < nearly; ++it) {
       mbar_arrive_expect_tx(&ctl->full[it], bytes);
-      tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it], (kb0 + it) * kBlockK,
-                  mt * kTokTileM, i);
+      tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it],
+                  (kb0 + (it + rot) % nkb) * kBlockK, mt * kTokTileM, i);
     }
   }
   pdl_wait();   // W may come from the previous kernel
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
     const int wz = p.w_per_sample ? i : 0;
     for (int it = 0; it < nkb; ++it) {
       const int s = it % kStages;
-      const int f0 = (kb0 + it) * kBlockK;
+      const int f0 = (kb0 + (it + rot) % nkb) * kBlockK;
       if (it >= nearly) {
         if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(&ctl->full[s], bytes);
@@ -287,11 +290,14 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   // before waiting for the previous kernel, whose output (Y) they do not
   // need (see tok_gemm_kernel).
   const int nearly = min(kStages, ntb);
+  // each tile walks its token blocks from its own starting point (see
+  // tok_gemm_kernel)
+  const int rot = ntb > 0 ? (int)(((unsigned)(ft + i * 3) * 5u) % (unsigned)ntb) : 0;
   const uint32_t bytes = kXTileBytes + 2 * kYBytes;
   const int f0 = ft * kFeatTileM;
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < nearly; ++it) {
-      const int t0 = (tb0 + it) * kBlockK;
+      const int t0 = (tb0 + (it + rot) % ntb) * kBlockK;
       mbar_arrive_expect_tx(&ctl->full[it], bytes);
       tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it], f0, t0, i);
       tma_load_3d(sX + it * kXTileBytes + kHalf, &p.map_x, &ctl->full[it], f0 + 64, t0, i);
@@ -304,7 +310,7 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < ntb; ++it) {
       const int s = it % kStages;
-      const int t0 = (tb0 + it) * kBlockK;
+      const int t0 = (tb0 + (it + rot) % ntb) * kBlockK;
       if (it >= nearly) {
         if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(&ctl->full[s], bytes);
