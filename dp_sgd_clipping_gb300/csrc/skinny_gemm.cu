@@ -290,14 +290,12 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   // before waiting for the previous kernel, whose output (Y) they do not
   // need (see tok_gemm_kernel).
   const int nearly = min(kStages, ntb);
-  // each tile walks its token blocks from its own starting point (see
-  // tok_gemm_kernel)
-  const int rot = ntb > 0 ? (int)(((unsigned)(ft + i * 3) * 5u) % (unsigned)ntb) : 0;
+
   const uint32_t bytes = kXTileBytes + 2 * kYBytes;
   const int f0 = ft * kFeatTileM;
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < nearly; ++it) {
-      const int t0 = (tb0 + (it + rot) % ntb) * kBlockK;
+      const int t0 = (tb0 + it) * kBlockK;
       mbar_arrive_expect_tx(&ctl->full[it], bytes);
       tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it], f0, t0, i);
       tma_load_3d(sX + it * kXTileBytes + kHalf, &p.map_x, &ctl->full[it], f0 + 64, t0, i);
@@ -310,7 +308,7 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < ntb; ++it) {
       const int s = it % kStages;
-      const int t0 = (tb0 + (it + rot) % ntb) * kBlockK;
+      const int t0 = (tb0 + it) * kBlockK;
       if (it >= nearly) {
         if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(&ctl->full[s], bytes);
