@@ -92,6 +92,8 @@ SIGNATURES = {
     "dpclip_philox_normal": (_i, [_vp, _i64, _i, _u64, _u32, _u64, _vp]),
     "dpclip_workspace_status": (_i, [_vp, _vp]),
     "dpclip_selftest_wait_timeout": (_i, [_vp, _sz, _i, _vp]),
+    "dpclip_grad_tail_schedule": (_i, [_i, _i, _i, _i, _c.POINTER(_i), _c.POINTER(_i), _vp, _i,
+                                       _c.POINTER(_i), _vp, _i, _c.POINTER(_i)]),
     "dpclip_status_string": (_c.c_char_p, [_i]),
     "dpclip_version": (_c.c_char_p, []),
 }
@@ -122,6 +124,27 @@ def _load():
 
 
 lib = _load()
+
+
+def grad_tail_schedule(pairs: int, ntiles: int, B: int, tblocks: int):
+    """The gradient's tail schedule (host only): (waves, ntail, segments,
+    contributions), segments as rows (pair, tail tile, t0, t1, slot) and
+    contributions as rows (tail tile, slot)."""
+    import numpy as np
+    waves, ntail, ns, nc = _c.c_int(), _c.c_int(), _c.c_int(), _c.c_int()
+    seg_cap = contrib_cap = 0
+    while True:
+        segs = np.zeros((max(seg_cap, 1), 5), dtype=np.int64)
+        contrib = np.zeros((max(contrib_cap, 1), 2), dtype=np.int64)
+        st = lib.dpclip_grad_tail_schedule(pairs, ntiles, B, tblocks, _c.byref(waves),
+                                           _c.byref(ntail), segs.ctypes.data, seg_cap,
+                                           _c.byref(ns), contrib.ctypes.data, contrib_cap,
+                                           _c.byref(nc))
+        if st != 0:
+            raise DpclipError("dpclip_grad_tail_schedule", st, status_string(st))
+        if ns.value <= seg_cap and nc.value <= contrib_cap:
+            return waves.value, ntail.value, segs[:ns.value], contrib[:nc.value]
+        seg_cap, contrib_cap = ns.value, nc.value
 
 
 def status_string(status: int) -> str:

@@ -1136,6 +1136,20 @@ int dpclip_workspace_status(const void* ws, dpclip_stream_t stream) {
   return (int)word;
 }
 
+int dpclip_grad_tail_schedule(int pairs, int ntiles, int B, int tblocks, int* waves, int* ntail,
+                              int64_t* segs, int seg_cap, int* nsegs, int64_t* contrib,
+                              int contrib_cap, int* ncontrib) {
+  if (pairs < 1 || pairs > kMaxPersistentGrid / 2 || ntiles < 1 || B < 1 || tblocks < 1 ||
+      !waves || !ntail || !nsegs || !ncontrib || seg_cap < 0 || contrib_cap < 0 ||
+      (seg_cap > 0 && !segs) || (contrib_cap > 0 && !contrib))
+    return DPCLIP_ERR_INVALID_ARG;
+  uint32_t cover = 0;
+  plan_grad_schedule(ntiles, B, tblocks, pairs, *waves, *ntail, cover);
+  grad_tail_dump(pairs, *ntail, (long long)B * tblocks, cover, segs, seg_cap, nsegs, contrib,
+                 contrib_cap, ncontrib);
+  return DPCLIP_OK;
+}
+
 int dpclip_selftest_wait_timeout(void* ws, size_t ws_bytes, int timeout_us, dpclip_stream_t stream) {
   if (timeout_us < 1 || timeout_us > 1000000) return DPCLIP_ERR_INVALID_ARG;
   DPCLIP_TRY(check_ws(ws, ws_bytes, kAlign));

@@ -33,19 +33,17 @@
 //     so the pairs running together share one sample's A and G slabs in L2.
 //   grad mode: `waves` full waves of whole tiles (pair c owns tiles c,
 //     c + G, ...: all B samples of a tile, folded into a register running
-//     sum s_0 acc_0 + s_1 acc_1 + ... in fp32), and the remaining tiles cut
-//     into (tile, sample, K-chunk) sub-units dealt in contiguous ranges, one
-//     range per pair, so that every pair gets the same amount of work.  A
-//     range covers whole tiles (finished directly) plus at most one partial
-//     tile at each end; a CTA writes each partial half-tile to its own
-//     workspace slot, takes an integer ticket on its CTA tile, and the last
-//     CTA to arrive adds the slots of the CTA tile in pair order (a fixed
-//     order), adds the noise and stores.  No CTA ever waits on another pair.
-//     Each pair runs its range of sub-units first: the partial tiles are then
-//     combined while the tensor cores work through the waves, and the kernel
-//     ends on whole tiles.  Where splitting would cost more than dealing the
-//     remaining tiles whole (tail_whole: pair c < tail takes tile c, all
-//     samples), the tail is that partial wave instead (plan_grad_schedule).
+//     sum s_0 acc_0 + s_1 acc_1 + ... in fp32), and the `ntail` remaining
+//     tiles cut into lockstep bands of their time lines (the samples'
+//     K-blocks one after another; grad_tail.cuh): each pair holds a few
+//     segments (tile, K-block range), cut into items where a segment passes
+//     from one sample to the next.  A CTA writes each partial half-tile to
+//     the workspace slot of its segment, takes an integer ticket on its CTA
+//     tile, and the last CTA to arrive adds the slots of the CTA tile in the
+//     schedule's order (a fixed order), adds the noise and stores.  No CTA
+//     ever waits on another pair.  Each pair runs its segments first: the
+//     partial tiles are then combined while the tensor cores work through
+//     the waves, and the kernel ends on whole tiles.
 //     The finished block leaves through a per-warp staging tile; the noise is
 //     drawn there, one Philox block of four columns per lane (store_block).
 //
@@ -64,6 +62,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "grad_tail.cuh"
 
 namespace dpclip {
 namespace {
@@ -83,6 +82,12 @@ constexpr int kRegsAtLaunch = 168;               // needed: 128*40 + 256*232 <= 
 static_assert(128 * kRegsProducer + kEpiThreads * kRegsEpilogue <= kThreads * kRegsAtLaunch,
               "register split exceeds the block's allocation");
 
+// A tail segment of this pair as its items see it: samples i0..i1, the
+// first item from K-block kb0, the last up to kb1.
+struct PairSeg {
+  int tile, slot, i0, i1, kb0, kb1, whole, pad;
+};
+
 struct Ctl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -95,6 +100,8 @@ struct Ctl {
   int mma_units;     // items whose MMAs were committed to tfull
   int is_last;
   int combine;
+  int nseg;          // grad mode: this pair's tail segments
+  PairSeg seg[kTailMaxSegs];
   float red[kThreads / 32];
 };
 
@@ -142,6 +149,7 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 
 struct Item {
   int tile, i, kb0, kb1;   // tile: pair tile
+  int slot;         // tail segment: its workspace slot (pair level)
   bool seg_first;   // first item of this pair's part of the tile: reset the sum
   bool seg_last;    // last item of this pair's part of the tile: finish it
   bool whole;       // this pair holds every item of the tile
@@ -152,70 +160,53 @@ struct PairPos {
   int c, G;   // cluster index, number of clusters
 };
 
-// Stream-K range of the tail: sub-units [vb(c), vb(c+1)).  With tail_whole
-// (the tail is a partial wave of whole tiles) pair c < tail takes tile c.
-__device__ __forceinline__ long long tail_begin(const GemmDpParams& p, int G, int c) {
-  if (p.tail_whole) return (long long)min(c, (int)(p.vtotal / p.B)) * p.B;
-  return (long long)c * p.vtotal / G;
-}
-// Pair whose tail range holds sub-unit v.
-__device__ __forceinline__ int tail_owner(const GemmDpParams& p, int G, long long v) {
-  if (p.tail_whole) return (int)(v / p.B);
-  return (int)(((v + 1) * G + p.vtotal - 1) / p.vtotal - 1);
-}
-__device__ __forceinline__ bool tail_nonempty(const GemmDpParams& p, int G, int c) {
-  return tail_begin(p, G, c) < tail_begin(p, G, c + 1);
-}
-// Workspace slot of pair c's partial of tail tile tt (its first or last
-// tile), half `rank`.
-__device__ __forceinline__ int tail_slot(const GemmDpParams& p, int G, int c, int tt, int rank) {
-  const long long per_tile = (long long)p.B * p.ksplit;
-  return 2 * (2 * c + ((int)(tail_begin(p, G, c) / per_tile) == tt ? 0 : 1)) + rank;
-}
-
-// The k-th item of this pair; false past the end.
+// The k-th item of this pair; false past the end.  `seg` holds the pair's
+// tail segments (grad mode), found once at the start of the kernel.
 template <bool kGrad>
-__device__ __forceinline__ bool item_at(const GemmDpParams& p, const PairPos& pp, int k, Item& it) {
+__device__ __forceinline__ bool item_at(const GemmDpParams& p, const PairPos& pp,
+                                        const PairSeg* seg, int nseg, int k, Item& it) {
   const int G = pp.G, c = pp.c, B = p.B;
   const int ntiles = (p.mtiles >> 1) * p.ntiles;
-  if (!kGrad) {
+  if constexpr (!kGrad) {
     const long long u = (long long)c + (long long)k * G;
     if (u >= (long long)ntiles * B) return false;
     it.i = (int)(u / ntiles);
     it.tile = (int)(u % ntiles);
     it.kb0 = 0;
     it.kb1 = p.tblocks;
+    it.slot = -1;
     it.seg_first = it.seg_last = it.whole = true;
     return true;
-  }
-  // first this pair's range of the tail sub-units, so that the partial tiles
-  // are combined while the tensor cores run the full waves; then the waves
-  const long long vb0 = tail_begin(p, G, c), vb1 = tail_begin(p, G, c + 1);
-  if (k < vb1 - vb0) {
-    const long long v = vb0 + k;
-    const long long per_tile = (long long)B * p.ksplit;
-    const int tt = (int)(v / per_tile);
-    const int rem = (int)(v % per_tile);
-    it.tile = p.waves * G + tt;
-    it.i = rem / p.ksplit;
-    const int ch = rem % p.ksplit;
-    it.kb0 = ch * p.kb_per_chunk;
-    it.kb1 = min(it.kb0 + p.kb_per_chunk, p.tblocks);
-    it.seg_first = v == vb0 || rem == 0;
-    it.seg_last = v == vb1 - 1 || rem == per_tile - 1;
-    it.whole = (long long)tt * per_tile >= vb0 && (long long)(tt + 1) * per_tile <= vb1;
+  } else {
+    // first this pair's segments of the tail tiles (each cut where the time
+    // line passes from one sample to the next), so that the partial tiles are
+    // combined while the tensor cores run the full waves; then the waves
+    for (int j = 0; j < nseg; ++j) {
+      const PairSeg sg = seg[j];
+      if (k <= sg.i1 - sg.i0) {
+        it.tile = p.waves * G + sg.tile;
+        it.i = sg.i0 + k;
+        it.kb0 = k == 0 ? sg.kb0 : 0;
+        it.kb1 = it.i == sg.i1 ? sg.kb1 : p.tblocks;
+        it.slot = sg.slot;
+        it.seg_first = k == 0;
+        it.seg_last = it.i == sg.i1;
+        it.whole = sg.whole != 0;
+        return true;
+      }
+      k -= sg.i1 - sg.i0 + 1;
+    }
+    if (k >= p.waves * B) return false;
+    it.tile = c + (k / B) * G;
+    it.i = k % B;
+    it.kb0 = 0;
+    it.kb1 = p.tblocks;
+    it.slot = -1;
+    it.seg_first = it.i == 0;
+    it.seg_last = it.i == B - 1;
+    it.whole = true;
     return true;
   }
-  const long long kw = k - (vb1 - vb0);
-  if (kw >= (long long)p.waves * B) return false;
-  it.tile = c + (int)(kw / B) * G;
-  it.i = (int)(kw % B);
-  it.kb0 = 0;
-  it.kb1 = p.tblocks;
-  it.seg_first = it.i == 0;
-  it.seg_last = it.i == B - 1;
-  it.whole = true;
-  return true;
 }
 
 // Finishes the warp's 32 x 128 block of the gradient: lane l holds, in tot,
@@ -315,6 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     tma_prefetch_map(&p.map_g);
   }
   if (warp == 1) tmem_alloc_pair(&ctl->tmem, 512);
+  if (kGrad && threadIdx.x == 64) {
+    // this pair's tail segments (the host keeps them within kTailMaxSegs)
+    TailSeg sgs[kTailMaxSegs];
+    const int ns = tail_pair_segs(pp.G, p.ntail, (long long)p.B * p.tblocks, p.tail_cover, pp.c, sgs);
+    for (int j = 0; j < ns; ++j) {
+      const TailSeg& sg = sgs[j];
+      PairSeg& q = ctl->seg[j];
+      q.tile = sg.tile;
+      q.slot = sg.slot;
+      q.i0 = (int)(sg.t0 / p.tblocks);
+      q.i1 = (int)((sg.t1 - 1) / p.tblocks);
+      q.kb0 = (int)(sg.t0 - (long long)q.i0 * p.tblocks);
+      q.kb1 = (int)(sg.t1 - (long long)q.i1 * p.tblocks);
+      q.whole = sg.t0 == 0 && sg.t1 == (long long)p.B * p.tblocks;
+    }
+    ctl->nseg = ns;
+  }
   tc_fence_before();
   cluster_sync_all();   // both CTAs' barriers exist before either uses the other's
   tc_fence_after();
@@ -327,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
     }
   }
   const uint32_t tmem = ctl->tmem;
+  const int nseg = kGrad ? ctl->nseg : 0;
   const WaitCtx wc{&ctl->abort_flag, p.err, kWaitLimitNs};
   if (warp < kEpiWarp0) {
     regs_dec<kRegsProducer>();
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
       int it = 0;
       Item itm;
       bool run = true;
-      for (int k = 0; run && item_at<kGrad>(p, pp, k, itm); ++k) {
+      for (int k = 0; run && item_at<kGrad>(p, pp, ctl->seg, nseg, k, itm); ++k) {
         const int d0 = (2 * (itm.tile % mp) + rank) * kDpTileM;
         const int p0 = (itm.tile / mp) * kDpTileN + rank * (kDpTileN / 2);
         for (int kb = itm.kb0; kb < itm.kb1; ++kb, ++it) {
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
       int it = 0, u = 0;
       Item itm;
       bool run = true;
-      for (; run && item_at<kGrad>(p, pp, u, itm); ++u) {
+      for (; run && item_at<kGrad>(p, pp, ctl->seg, nseg, u, itm); ++u) {
         const int acc = u & 1;
         if (!mbar_wait_cluster(&ctl->tempty[acc], ((u >> 1) & 1) ^ 1, wc)) break;
         tc_fence_after();
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 #pragma unroll
     for (int j = 0; j < 128; ++j) tot[j] = 0.f;
     Item itm;
-    for (int u = 0; item_at<kGrad>(p, pp, u, itm); ++u) {
+    for (int u = 0; item_at<kGrad>(p, pp, ctl->seg, nseg, u, itm); ++u) {
       const int acc = u & 1;
       if (!epi_all(mbar_wait(&ctl->tfull[acc], (u >> 1) & 1, wc))) break;
       tc_fence_after();
@@ -444,25 +453,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
           do_store = itm.whole;
           if (!itm.whole) {
             // partial tile: publish this CTA's part; the last CTA to arrive
-            // on the CTA tile adds every participant's part, in pair order,
-            // and stores
+            // on the CTA tile adds every participant's part, in the order of
+            // the schedule, and stores
             const int tt = itm.tile - p.waves * pp.G;
+            const long long L = (long long)p.B * p.tblocks;
             float4* slot = reinterpret_cast<float4*>(p.slots) +
-                           (size_t)tail_slot(p, pp.G, pp.c, tt, rank) * (32 * kEpiThreads);
+                           (size_t)(2 * itm.slot + rank) * (32 * kEpiThreads);
 #pragma unroll
             for (int jb = 0; jb < 32; ++jb)
               __stcg(slot + jb * kEpiThreads + etid,
                      make_float4(tot[4 * jb], tot[4 * jb + 1], tot[4 * jb + 2], tot[4 * jb + 3]));
             __threadfence();
             epi_sync();
-            // participants: the pairs from the owner of the tile's first
-            // sub-unit to the owner of its last, skipping empty ranges
-            const long long per_tile = (long long)p.B * p.ksplit;
-            const int c_lo = tail_owner(p, pp.G, (long long)tt * per_tile);
-            const int c_hi = tail_owner(p, pp.G, (long long)(tt + 1) * per_tile - 1);
             if (etid == 0) {
               int parts = 0;
-              for (int cc = c_lo; cc <= c_hi; ++cc) parts += tail_nonempty(p, pp.G, cc) ? 1 : 0;
+              tail_tile_slots(pp.G, p.ntail, L, p.tail_cover, tt, [&](int) { ++parts; });
               const uint32_t prev = atomicAdd(&p.tickets[ctile], 1u);
               ctl->combine = prev == (uint32_t)(parts - 1);
             }
@@ -471,10 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
               __threadfence();
 #pragma unroll
               for (int j = 0; j < 128; ++j) tot[j] = 0.f;
-              for (int cc = c_lo; cc <= c_hi; ++cc) {
-                if (!tail_nonempty(p, pp.G, cc)) continue;
+              tail_tile_slots(pp.G, p.ntail, L, p.tail_cover, tt, [&](int sl) {
                 const float4* src = reinterpret_cast<const float4*>(p.slots) +
-                                    (size_t)tail_slot(p, pp.G, cc, tt, rank) * (32 * kEpiThreads);
+                                    (size_t)(2 * sl + rank) * (32 * kEpiThreads);
 #pragma unroll
                 for (int jb = 0; jb < 32; ++jb) {
                   const float4 v = __ldcg(src + jb * kEpiThreads + etid);
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
                   tot[4 * jb + 2] += v.z;
                   tot[4 * jb + 3] += v.w;
                 }
-              }
+              });
               do_store = true;
             }
           }
@@ -592,38 +596,116 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_dp_kernel(const __grid_const
 
 size_t gemm_dp_smem() { return kSmemBytes; }
 
-size_t gemm_dp_slot_bytes(int max_grid) { return (size_t)2 * max_grid * 32 * kEpiThreads * 16; }
+size_t gemm_dp_slot_bytes(int max_grid) {
+  // kTailMaxSegs contributions per pair, one half-tile slot per CTA each
+  return (size_t)kTailMaxSegs * max_grid * 32 * kEpiThreads * 16;
+}
 
-// Grad-mode schedule over `grid` pairs: full waves of whole pair tiles, and
-// the remaining tiles either K-split (1, 2 or 4 chunks per sample, the split
-// that best evens out the per-pair work) or dealt whole, one per pair, as a
-// partial wave (tail_whole).  In a wave every pair works on the same sample
-// at the same time, so pairs that share A and G slabs find them in L2; the
-// sub-units of the split run on different samples and stream from HBM,
-// about twice as slowly per K-block (timestamps per unit).  The cheaper of
-// the two, with that factor, is taken.
-void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ksplit,
-                        int& kb_per_chunk, long long& vtotal, int& tail_whole) {
-  waves = ntiles / grid;
-  const int tail = ntiles - waves * grid;
-  ksplit = 1;
-  double best = 1e30;
-  for (int want : {1, 2, 4}) {
-    const int kbc = (tblocks + want - 1) / want;
-    const int ks = (tblocks + kbc - 1) / kbc;   // chunks actually used: none is empty
-    const long long v = (long long)tail * B * ks;
-    // the busiest pair's work in K-blocks
-    const double span = (double)((v + grid - 1) / grid) * kbc;
-    if (span < best - 1e-9) {
-      best = span;
-      ksplit = ks;
+TailStats grad_tail_stats(int G, int ntail, long long L, uint32_t cover) {
+  TailStats st{};
+  if (G < 1 || G > kMaxPersistentGrid / 2) return st;
+  long long work[kMaxPersistentGrid / 2] = {};
+  int segs[kMaxPersistentGrid / 2] = {};
+  bool covered = false;
+  TailWalk w;
+  w.start(G, ntail, L, cover);
+  while (!w.done) {
+    ++st.levels;
+    for (int c = w.p0; c < w.p0 + w.n; ++c) {
+      TailSeg sg;
+      if (tail_seg_of(w, c, sg) > 0 && sg.t1 > sg.t0) {
+        work[c] += sg.t1 - sg.t0;
+        ++segs[c];
+        ++st.nsegs;
+        st.nslots = std::max(st.nslots, sg.slot + 1);
+      }
+    }
+    if (w.band() && w.cover) covered = true;
+    w.advance(cover);
+  }
+  st.complete = covered || w.m == 0 || w.t1 <= w.t0;
+  for (int c = 0; c < G; ++c) {
+    st.max_work = std::max(st.max_work, work[c]);
+    st.max_segs = std::max(st.max_segs, segs[c]);
+  }
+  return st;
+}
+
+void grad_tail_dump(int G, int ntail, long long L, uint32_t cover, int64_t* segs, int seg_cap,
+                    int* nsegs, int64_t* contrib, int contrib_cap, int* ncontrib) {
+  int ns = 0, nc = 0;
+  for (int c = 0; c < G && ntail > 0; ++c) {
+    // the segments of the kernel's prologue, for pair c
+    TailSeg sgs[kTailMaxSegs];
+    const int n = tail_pair_segs(G, ntail, L, cover, c, sgs);
+    for (int j = 0; j < n; ++j, ++ns) {
+      if (ns < seg_cap) {
+        int64_t* o = segs + 5 * (size_t)ns;
+        o[0] = c;
+        o[1] = sgs[j].tile;
+        o[2] = sgs[j].t0;
+        o[3] = sgs[j].t1;
+        o[4] = sgs[j].slot;
+      }
     }
   }
-  constexpr double kSplitSlowdown = 2.0;
-  tail_whole = tail > 0 && (double)B * tblocks <= kSplitSlowdown * best ? 1 : 0;
-  if (tail_whole) ksplit = 1;
-  kb_per_chunk = (tblocks + ksplit - 1) / ksplit;
-  vtotal = (long long)tail * B * ksplit;
+  struct Emit {
+    int64_t* out;
+    int cap, tt;
+    int* n;
+    __host__ __device__ void operator()(int sl) const {
+      if (*n < cap) {
+        out[2 * (size_t)*n] = tt;
+        out[2 * (size_t)*n + 1] = sl;
+      }
+      ++*n;
+    }
+  };
+  for (int tt = 0; tt < ntail; ++tt)
+    tail_tile_slots(G, ntail, L, cover, tt, Emit{contrib, contrib_cap, tt, &nc});
+  *nsegs = ns;
+  *ncontrib = nc;
+}
+
+// Grad-mode schedule over `grid` pairs: full waves of whole pair tiles (every
+// pair works on the same sample at the same time, so pairs that share A and
+// G slabs find them in L2), and the remaining tiles cut into lockstep bands
+// (grad_tail.cuh).  Of the schedules that make the first k band levels exact
+// and the next one cover, the one with the least work on its busiest pair
+// is taken (then the fewest partial tiles), among those that keep every pair
+// within kTailMaxSegs partial tiles; k = 0 (one cover level: q bands of the
+// whole time line, the remaining pairs idle in the tail) always qualifies.
+void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ntail,
+                        uint32_t& cover) {
+  waves = ntiles / grid;
+  ntail = ntiles - waves * grid;
+  cover = ~0u;
+  if (ntail == 0) return;
+  // the last plan of this host thread (a training loop repeats its shapes)
+  thread_local int key[4] = {-1, -1, -1, -1};
+  thread_local uint32_t key_cover = ~0u;
+  if (key[0] == ntiles && key[1] == B && key[2] == tblocks && key[3] == grid) {
+    cover = key_cover;
+    return;
+  }
+  const long long L = (long long)B * tblocks;
+  long long best = -1, best_segs = 0;
+  for (int k = 0; k < kTailMaxLevels; ++k) {
+    const uint32_t mask = ~0u << k;
+    const TailStats st = grad_tail_stats(grid, ntail, L, mask);
+    if (st.complete && st.max_segs <= kTailMaxSegs && st.nslots <= kTailMaxSegs * grid &&
+        (best < 0 || st.max_work < best || (st.max_work == best && st.nsegs < best_segs))) {
+      best = st.max_work;
+      best_segs = st.nsegs;
+      cover = mask;
+    }
+    if (st.levels <= k) break;   // the walk ended before level k: larger k change nothing
+  }
+  key[0] = ntiles;
+  key[1] = B;
+  key[2] = tblocks;
+  key[3] = grid;
+  key_cover = cover;
 }
 
 // The register split above is only safe when the compiled kernel is launched
@@ -656,8 +738,7 @@ cudaError_t launch_gemm_dp(const GemmDpParams& params, bool grad_mode, cudaStrea
   pairs_ll = std::max(1LL, std::min(pairs_ll, work));
   const int pairs = (int)pairs_ll;
   if (grad_mode)
-    plan_grad_schedule(ntiles, p.B, p.tblocks, pairs, p.waves, p.ksplit, p.kb_per_chunk, p.vtotal,
-                       p.tail_whole);
+    plan_grad_schedule(ntiles, p.B, p.tblocks, pairs, p.waves, p.ntail, p.tail_cover);
   return launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, s, 2, p);
 }
 

@@ -115,10 +115,9 @@ struct GemmDpParams {
   int B, T, d, p;
   int mtiles, ntiles, tblocks;   // mtiles: 128-row CTA tiles along d (even: pairs of them)
   // grad-mode schedule (set by launch_gemm_dp)
-  int waves, ksplit, kb_per_chunk;
-  long long vtotal;
-  int tail_whole;        // the tail is a partial wave of whole tiles (one per pair)
-  float* slots;          // 2 per CTA of the grid: partial CTA tiles of 128 x 256 fp32
+  int waves, ntail;      // full waves of whole pair tiles; pair tiles left after them
+  uint32_t tail_cover;   // band levels of the tail schedule that cover (bit per level)
+  float* slots;          // partial CTA tiles of 128 x 256 fp32, 2 per tail contribution
   uint32_t* tickets;     // [mtiles * ntiles] (CTA tiles), zero at launch
   const float* sqnorms;
   float C, sigma;
@@ -270,8 +269,22 @@ size_t tok_gemm_smem(int NP);
 size_t feat_gemm_smem(int NP);
 size_t gemm_dp_smem();
 size_t gemm_dp_slot_bytes(int max_grid);
-void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ksplit,
-                        int& kb_per_chunk, long long& vtotal, int& tail_whole);
+void plan_grad_schedule(int ntiles, int B, int tblocks, int grid, int& waves, int& ntail,
+                        uint32_t& cover);
+// Summary of a tail schedule (host walk of grad_tail.cuh).
+struct TailStats {
+  long long max_work;   // K-blocks of the busiest pair
+  int max_segs;         // most partial tiles held by one pair
+  int nslots;           // slots used (pair level)
+  long long nsegs;      // segments in all
+  bool complete;        // every (tile, K-block) of the tail is assigned
+  int levels;           // levels walked
+};
+TailStats grad_tail_stats(int G, int ntail, long long L, uint32_t cover);
+// Writes the tail schedule's segments and contributions (see
+// dpclip_grad_tail_schedule).
+void grad_tail_dump(int G, int ntail, long long L, uint32_t cover, int64_t* segs, int seg_cap,
+                    int* nsegs, int64_t* contrib, int contrib_cap, int* ncontrib);
 constexpr int kMaxPersistentGrid = 160;   // CTAs of the persistent kernels (<= SMs)
 size_t ghost_smem();
 // Tail split of the ghost units for a grid: sets nfull, tail_split, pb_per_split.

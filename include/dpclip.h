@@ -335,6 +335,22 @@ int dpclip_workspace_status(const void* ws, dpclip_stream_t stream);
 int dpclip_selftest_wait_timeout(void* ws, size_t ws_bytes, int timeout_us,
                                  dpclip_stream_t stream);
 
+/* Host-only diagnostic (no device work): the schedule that
+ * dpclip_clipped_noisy_grad gives the tiles left after the full waves, for
+ * `pairs` CTA pairs, `ntiles` pair tiles of 256 x 256, B samples of `tblocks`
+ * 64-token blocks.  Writes *waves (full waves of whole tiles) and *ntail
+ * (tiles left).  Each segment is 5 int64 at segs[5 j]: pair, tail tile,
+ * first and end K-block of the tile's time line (sample i's block kb is
+ * i * tblocks + kb) and the workspace slot; pairs appear in index order and
+ * a pair's segments in the order it runs them.  Each contribution is 2 int64
+ * at contrib[2 j]: tail tile and slot, per tile in the order the partial
+ * sums are added.  *nsegs and *ncontrib receive the full counts; records
+ * beyond seg_cap or contrib_cap are not written.  DPCLIP_ERR_INVALID_ARG for
+ * pairs outside 1..80 or non-positive sizes. */
+int dpclip_grad_tail_schedule(int pairs, int ntiles, int B, int tblocks, int* waves, int* ntail,
+                              int64_t* segs, int seg_cap, int* nsegs, int64_t* contrib,
+                              int contrib_cap, int* ncontrib);
+
 /* Human-readable name of a status code. */
 const char* dpclip_status_string(int status);
 

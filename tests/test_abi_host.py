@@ -45,10 +45,10 @@ def test_workspace_sizes(L):
     # O(BkT + kp) memory of the randomized estimator: far below one d x p gradient
     assert n1 < 2048 * 8192 * 4 / 4
     assert ws(L.OP_NORMS_HUTCHPP, 4, 4096, 2048, 8192, L.BF16, 32) > n1
-    # gradient: tile tickets plus two partial 128x256 fp32 tiles per CTA of the
-    # balanced tail (at most 160 CTAs)
+    # gradient: tile tickets plus three partial 128x256 fp32 tiles per CTA (the
+    # segments of the tail schedule; at most 160 CTAs)
     g = ws(L.OP_CLIPPED_NOISY_GRAD, 4, 4096, 2048, 8192, L.BF16, 0)
-    assert 2 * 160 * 128 * 256 * 4 <= g <= 2 * 160 * 128 * 256 * 4 + 4096
+    assert 3 * 160 * 128 * 256 * 4 <= g <= 3 * 160 * 128 * 256 * 4 + 4096
     assert ws(L.OP_CLIPPED_NOISY_GRAD, 4, 64, 32, 48, L.F32, 0) == 256
     direct = ws(L.OP_NORMS_EXACT, 8, 512, 768, 768, L.BF16, L.EXACT_DIRECT)
     ghost = ws(L.OP_NORMS_EXACT, 8, 512, 768, 768, L.BF16, L.EXACT_GHOST)
@@ -180,3 +180,84 @@ def test_product_path_does_not_import_oracle():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 assert not pat.search(open(os.path.join(dirpath, f)).read()), f
+
+
+# ----------------------------------------------------------------------------- gradient tail schedule
+
+def _tail_cases():
+    # (pairs, pair tiles, samples, 64-token blocks per sample)
+    cases = [(76, 256, 4, 64), (76, 64, 4, 64), (76, 64, 1, 128), (74, 256, 4, 64),
+             (76, 8 * 32, 1, 1), (80, 79, 1, 1), (80, 79, 4, 64), (76, 75, 2, 3),
+             (3, 5, 2, 1), (1, 1, 1, 1), (76, 152, 8, 16), (76, 1, 33, 1)]
+    for pairs in (2, 5, 13, 37, 64, 76, 80):
+        for ntiles in (1, pairs - 1, pairs + 1, 2 * pairs + pairs // 3, 3 * pairs + 7):
+            for B, tb in ((1, 1), (2, 5), (4, 64), (3, 100)):
+                if ntiles >= 1:
+                    cases.append((pairs, ntiles, B, tb))
+    return cases
+
+
+def test_grad_tail_schedule_covers_once(L):
+    """Every (tile, K-block) of the tiles left after the full waves belongs
+    to exactly one segment; each pair holds at most three partial tiles;
+    slots are unique and below 3 per pair; the contributions of a tile are
+    exactly the slots of its segments, added in slot order; and the busiest
+    pair carries no more than a whole tile's time line."""
+    import numpy as np
+    for pairs, ntiles, B, tb in _tail_cases():
+        waves, ntail, segs, contrib = L.grad_tail_schedule(pairs, ntiles, B, tb)
+        assert waves == ntiles // pairs and ntail == ntiles % pairs
+        Lt = B * tb
+        if ntail == 0:
+            assert len(segs) == 0 and len(contrib) == 0
+            continue
+        cover = np.zeros((ntail, Lt), dtype=np.int32)
+        work = np.zeros(pairs, dtype=np.int64)
+        count = np.zeros(pairs, dtype=np.int64)
+        for c, t, t0, t1, sl in segs:
+            assert 0 <= c < pairs and 0 <= t < ntail and 0 <= t0 < t1 <= Lt
+            cover[t, t0:t1] += 1
+            work[c] += t1 - t0
+            count[c] += 1
+        assert (cover == 1).all(), (pairs, ntiles, B, tb)
+        assert count.max() <= 3
+        slots = segs[:, 4]
+        assert len(set(slots.tolist())) == len(slots) and slots.min() >= 0
+        assert slots.max() < 3 * pairs
+        assert list(segs[:, 0]) == sorted(segs[:, 0])
+        for t in range(ntail):
+            mine = sorted(segs[segs[:, 1] == t][:, 4].tolist())
+            listed = contrib[contrib[:, 0] == t][:, 1].tolist()
+            assert listed == mine, (pairs, ntiles, B, tb, t)
+        assert work.max() <= Lt
+
+
+def test_grad_tail_schedule_balance(L):
+    """Where the time line is long, the busiest pair of the tail stays near
+    the fair share ntail * L / pairs; on the up_proj shape (256 pair tiles,
+    76 pairs, 4 samples of 64 blocks) it is within two K-blocks of it, and
+    most pairs hold a single segment."""
+    import numpy as np
+    _, ntail, segs, _ = L.grad_tail_schedule(76, 256, 4, 64)
+    assert ntail == 28
+    work = np.bincount(segs[:, 0], weights=segs[:, 3] - segs[:, 2], minlength=76)
+    fair = 28 * 256 / 76
+    assert work.max() <= fair + 2
+    assert np.sum(np.bincount(segs[:, 0], minlength=76) == 1) >= 50
+    for pairs, ntiles, B, tb in _tail_cases():
+        if B * tb < 64:
+            continue
+        _, ntail, segs, _ = L.grad_tail_schedule(pairs, ntiles, B, tb)
+        if ntail == 0:
+            continue
+        work = np.bincount(segs[:, 0], weights=segs[:, 3] - segs[:, 2], minlength=pairs)
+        assert work.max() <= 1.35 * ntail * B * tb / pairs + 1, (pairs, ntiles, B, tb)
+
+
+def test_grad_tail_schedule_rejects(L):
+    import ctypes as C
+    w, n, ns, nc = C.c_int(), C.c_int(), C.c_int(), C.c_int()
+    for args in ((0, 4, 1, 1), (81, 4, 1, 1), (4, 0, 1, 1), (4, 4, 0, 1), (4, 4, 1, 0)):
+        st = L.lib.dpclip_grad_tail_schedule(*args, C.byref(w), C.byref(n), None, 0, C.byref(ns),
+                                             None, 0, C.byref(nc))
+        assert st == L.ERR_INVALID_ARG

@@ -524,6 +524,22 @@ def test_grad_tail_split_over_k(api):
     check_grad(api, inp, A, G, q, float(np.sqrt(q).min()), 0.0, Ms)
 
 
+def test_grad_tail_bands(api):
+    # 104 pair tiles: on 76 pairs one full wave and 28 tiles cut into bands
+    # over three levels (pairs with up to three segments, tiles summed from
+    # up to four partial sums); ragged T, d and p
+    from dp_sgd_clipping_gb300 import _lib
+    _, ntail, segs, contrib = _lib.grad_tail_schedule(76, 104, 2, 20)
+    assert ntail == 28 and np.bincount(segs[:, 0]).max() == 2
+    assert np.bincount(contrib[:, 0]).max() == 4
+    wl = W.Workload(174, "tail_bands", 2, 1270, 248, 26616, "bf16", 1e-3, 0.5, 0.8, 8, ())
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    Ms = list(O.per_sample_grads(inp.A, inp.G))
+    q = np.array([np.sum(M * M) for M in Ms])
+    check_grad(api, inp, A, G, q, float(np.sqrt(q).min()), wl.sigma, Ms)
+
+
 # ----------------------------------------------------------------------------- Rademacher probes
 
 def test_rademacher_fill_is_exact(api):
