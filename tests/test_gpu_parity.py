@@ -540,6 +540,22 @@ def test_grad_tail_bands(api):
     check_grad(api, inp, A, G, q, float(np.sqrt(q).min()), wl.sigma, Ms)
 
 
+def test_grad_tail_three_segments(api):
+    # 180 pair tiles: on 76 pairs two full waves and 28 tiles whose bands go
+    # three levels deep (pairs with three segments, run shortest first; tiles
+    # summed from up to five partial sums); ragged T, d and p
+    from dp_sgd_clipping_gb300 import _lib
+    _, ntail, segs, contrib = _lib.grad_tail_schedule(76, 180, 2, 16)
+    assert ntail == 28 and np.bincount(segs[:, 0]).max() == 3
+    assert np.bincount(contrib[:, 0]).max() == 5
+    wl = W.Workload(175, "tail_three_segments", 2, 1000, 248, 46072, "bf16", 1e-3, 0.5, 0.8, 8, ())
+    inp = W.make_inputs(wl)
+    A, G = to_dev(inp)
+    Ms = list(O.per_sample_grads(inp.A, inp.G))
+    q = np.array([np.sum(M * M) for M in Ms])
+    check_grad(api, inp, A, G, q, float(np.sqrt(q).min()), wl.sigma, Ms)
+
+
 # ----------------------------------------------------------------------------- Rademacher probes
 
 def test_rademacher_fill_is_exact(api):
