@@ -745,6 +745,7 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
   hq.m = m;
   hq.out_f32 = QW;
   hq.err = at<uint32_t>(ws, pl.ctrl);
+  hq.gram_f64 = 1;
   DPCLIP_CUDA(launch_hpp_qr(hq, s));
   // Y3 = G [Q | W]  (T x (r+m))
   sp = simt_base();

@@ -10,14 +10,25 @@
 // gives the same result as a Householder QR.
 //
 // CholeskyQR2: Gram H = V^T V, Cholesky H = R^T R, Q1 = V R^-1, then once more
-// on Q1 (whose Gram is close to the identity).  Everything runs in fp32: this
-// GPU's fp64 pipe is a small fraction of its fp32 rate.  A Cholesky pivot
-// below 1e-5 of the largest diagonal entry (a singular-value ratio of ~3e-3)
-// marks its column as dependent on the earlier ones: that column of Q is set
-// to zero, so Q spans the rest and the tail estimates what is left (T < r
-// makes rank(O_i) < r, for instance).  With those columns dropped the kept
-// Gram has condition number below ~1e5, within fp32 Cholesky's reach, and the
-// second pass restores orthogonality to fp32 level.
+// on Q1 (whose Gram is close to the identity).  For bf16 inputs everything
+// runs in fp32 (this GPU's fp64 pipe is a small fraction of its fp32 rate,
+// and V itself carries only ~16 bits).  A Cholesky pivot below 1e-5 of the
+// largest diagonal entry (a singular-value ratio of ~3e-3) marks its column
+// as dependent on the earlier ones: that column of Q is set to zero, so Q
+// spans the rest and the tail estimates what is left (T < r makes
+// rank(O_i) < r, for instance).  With those columns dropped the kept Gram has
+// condition number below ~1e5, within fp32 Cholesky's reach, and the second
+// pass restores orthogonality to fp32 level.
+//
+// For fp32 inputs the first pass's Gram, its Cholesky factor and R^-1 are
+// formed in fp64 (the fp32 products are exact in fp64), and only pivots
+// below 1e-12 of the largest are dropped: the squared singular values of
+// O_i S fall as the fourth power of those of A_i^T G_i, so on a decaying
+// spectrum the fp32 rule would hand most of the head's directions to the
+// tail, whose estimate then differs from an exact QR's by far more than
+// fp32 rounding.  Q1 = V R^-1 is still formed in fp32; its loss of
+// orthogonality (about the fp32 unit roundoff times the condition number of
+// V) is what the second, fp32 pass removes.
 //
 // Parallel layout: one thread-block cluster per sample (up to 16 CTAs where
 // the device allows clusters that large, else 8; fewer for short p).  CTA j
@@ -62,6 +73,7 @@ constexpr int kMaxR = 16;            // r = floor(k/3) <= 16 for k <= 48
 constexpr int kMaxM = 18;            // m = k - 2r <= 18 for k <= 48
 constexpr int kPub = kMaxR * kMaxNP; // one CTA's partial: r x (r + m) <= 16 x 32
 constexpr float kDropTol = 1e-5f;
+constexpr double kDropTol64 = 1e-12;
 
 struct Smem {
   float xs[kCols][kLdc];           // staged columns: V (then Q1, then Q) | G'
@@ -78,6 +90,19 @@ struct Smem {
   float M1[kMaxR][kMaxR];          // R^-1 as the forward substitution applies it
   float M2[kMaxR][kMaxR];          // (zero outside the leading r x r block)
 };
+
+// The fp64 first pass of fp32 inputs: partials, cluster sum and factor.
+// Placed after Smem in dynamic shared memory, only by that instantiation.
+struct Smem64 {
+  double red[kThreads * 16];
+  double pub[kMaxR * kMaxR];
+  double sum[kMaxR * kMaxR];
+  double R[kMaxR][kMaxR + 1];
+  double rd[kMaxR];
+};
+
+__device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
+__device__ __forceinline__ double rsqrt_t(double x) { return 1.0 / sqrt(x); }
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
@@ -105,20 +130,21 @@ __device__ __forceinline__ void copy_f32(float* dst, const float* src, int n, bo
 // column b (rdiag[b] = 0) is a zero column of M.  Entries outside the
 // leading r x r block are zero.  Not inlined: the two factorisations and
 // the instruction-cache warm-up below run the same code.
-__device__ __noinline__ void invert_factor(const float (*R)[kMaxR + 1], const float* rdiag,
-                                              int r, float (*M)[kMaxR]) {
+template <typename T>
+__device__ __noinline__ void invert_factor(const T (*R)[kMaxR + 1], const T* rdiag, int r,
+                                           float (*M)[kMaxR]) {
   const int a = threadIdx.x & 31;
   if (a >= kMaxR) return;
-  float q[kMaxR];
+  T q[kMaxR];
 #pragma unroll
   for (int b = 0; b < kMaxR; ++b) {
-    float s = (a == b && b < r) ? 1.f : 0.f;
+    T s = (a == b && b < r) ? T(1) : T(0);
 #pragma unroll
-    for (int c = 0; c < b; ++c) s = fmaf(-q[c], R[c][b], s);
-    q[b] = b < r ? s * rdiag[b] : 0.f;
+    for (int c = 0; c < b; ++c) s = fma(-q[c], R[c][b], s);
+    q[b] = b < r ? s * rdiag[b] : T(0);
   }
 #pragma unroll
-  for (int b = 0; b < kMaxR; ++b) M[a][b] = a < r ? q[b] : 0.f;
+  for (int b = 0; b < kMaxR; ++b) M[a][b] = a < r ? (float)q[b] : 0.f;
 }
 
 // Stages rows [base, base + nvalid) of V (columns < r) and G' (m columns) as
@@ -137,7 +163,7 @@ __device__ __forceinline__ void stage_tile(Smem& sm, const HppQrParams& p, int i
     // pass) inverse on the second factor's scratch, which pass 1 overwrites:
     // that fetches its code into the instruction cache before the first real
     // use, where the fetch would otherwise sit on the critical path.
-    invert_factor(sm.R2, sm.rd2, r, sm.M2);
+    invert_factor<float>(sm.R2, sm.rd2, r, sm.M2);
   }
   if (p.gp_bf16) {
     // p % 8 == 0 on this path: base and nvalid are multiples of 8
@@ -176,8 +202,9 @@ struct Blocking {
 
 // acc += this thread's share of X^T Y over staged rows [0, nrows): block
 // (a0.., b0..) over the row groups 4 (s + k slices) .. + 3.
+template <typename T>
 __device__ __forceinline__ void accumulate(const Smem& sm, const Blocking& bk, int nrows,
-                                           float (&acc)[4][4]) {
+                                           T (&acc)[4][4]) {
   const int blk = (int)threadIdx.x % bk.nblk, s = (int)threadIdx.x / bk.nblk;
   if (s >= bk.slices) return;
   const int a0 = (blk / bk.nbb) * 4, b0 = (blk % bk.nbb) * 4;
@@ -193,70 +220,74 @@ __device__ __forceinline__ void accumulate(const Smem& sm, const Blocking& bk, i
     for (int u = 0; u < 4; ++u)
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        float a = acc[u][w];
-        a = fmaf(x[u].x, y[w].x, a);
-        a = fmaf(x[u].y, y[w].y, a);
-        a = fmaf(x[u].z, y[w].z, a);
-        a = fmaf(x[u].w, y[w].w, a);
+        T a = acc[u][w];
+        a = fma((T)x[u].x, (T)y[w].x, a);
+        a = fma((T)x[u].y, (T)y[w].y, a);
+        a = fma((T)x[u].z, (T)y[w].z, a);
+        a = fma((T)x[u].w, (T)y[w].w, a);
         acc[u][w] = a;
       }
   }
 }
 
-// sm.pub[pass][a * nb + b] = this CTA's sum of X^T Y, the slices added in
-// slice order (deterministic).
-__device__ __forceinline__ void stash_acc(Smem& sm, const float (&acc)[4][4]) {
+// pub[a * nb + b] = this CTA's sum of X^T Y, the slices added in slice order
+// (deterministic); red holds each thread's 4 x 4 block.
+template <typename T>
+__device__ __forceinline__ void stash_acc(T* red, const T (&acc)[4][4]) {
 #pragma unroll
   for (int u = 0; u < 4; ++u)
 #pragma unroll
-    for (int w = 0; w < 4; ++w) sm.red[threadIdx.x * 16 + u * 4 + w] = acc[u][w];
+    for (int w = 0; w < 4; ++w) red[threadIdx.x * 16 + u * 4 + w] = acc[u][w];
   __syncthreads();
 }
-__device__ __forceinline__ void publish(Smem& sm, int nbb, int nblk, int slices, int pass, int na,
-                                     int nb) {
+template <typename T>
+__device__ __forceinline__ void publish(const T* red, T* pub, int nbb, int nblk, int slices, int na,
+                                        int nb) {
   for (int e = threadIdx.x; e < na * nb; e += kThreads) {
     const int a = e / nb, b = e % nb;
     const int blk = (a / 4) * nbb + b / 4, q = (a % 4) * 4 + b % 4;
-    float s = 0.f;
-    for (int sl = 0; sl < slices; ++sl) s += sm.red[(sl * nblk + blk) * 16 + q];
-    sm.pub[pass][e] = s;
+    T s = 0;
+    for (int sl = 0; sl < slices; ++sl) s += red[(sl * nblk + blk) * 16 + q];
+    pub[e] = s;
   }
 }
 
-// sm.sum[e] = sum over the cluster's ranks, in rank order, of pub[pass][e].
-__device__ __forceinline__ void cluster_sum(Smem& sm, cg::cluster_group& cluster, int pass, int ne, int cs) {
+// sum[e] = sum over the cluster's ranks, in rank order, of their pub[e].
+template <typename T>
+__device__ __forceinline__ void cluster_sum(T* pub, T* sum, cg::cluster_group& cluster, int ne,
+                                            int cs) {
   cluster.sync();   // every rank has published
   for (int e = threadIdx.x; e < ne; e += kThreads) {
-    float v[16];
+    T v[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
-      v[q] = q < cs ? cluster.map_shared_rank(&sm.pub[pass][0], q)[e] : 0.f;
-    float s = 0.f;
+    for (int q = 0; q < 16; ++q) v[q] = q < cs ? cluster.map_shared_rank(pub, q)[e] : T(0);
+    T s = 0;
 #pragma unroll
     for (int q = 0; q < 16; ++q) s += v[q];
-    sm.sum[e] = s;
+    sum[e] = s;
   }
   __syncthreads();
 }
 
 // Warp 0: Cholesky A = R^T R in place on the n x n Gram in A (upper
 // triangle read, R written over it), lane j owning column j.  A pivot below
-// kDropTol times the largest diagonal entry marks its column as dependent on
+// droptol times the largest diagonal entry marks its column as dependent on
 // the earlier ones: its row of R and its entry of rdiag (= 1 / R[k][k]) are
 // zero, so the matching column of Q comes out zero and drops out of both the
-// head and the tail projection.  1 / R[k][k] is the hardware reciprocal
-// square root (within 2 ulp); the second CholeskyQR pass absorbs that.
-// Short rolled loops: this runs once per CTA, where the fetch of unrolled
-// straight-line code would cost more than the arithmetic.
-__device__ __forceinline__ void cholesky(float (*A)[kMaxR + 1], int n, float* rdiag) {
+// head and the tail projection.  In fp32, 1 / R[k][k] is the hardware
+// reciprocal square root (within 2 ulp); the second CholeskyQR pass absorbs
+// that.  Short rolled loops: this runs once per CTA, where the fetch of
+// unrolled straight-line code would cost more than the arithmetic.
+template <typename T>
+__device__ __forceinline__ void cholesky(T (*A)[kMaxR + 1], int n, T* rdiag, T droptol) {
   const int j = threadIdx.x & 31;
-  float dmax = 0.f;
-  for (int a = 0; a < n; ++a) dmax = fmaxf(dmax, A[a][a]);
-  const float tol = kDropTol * dmax;
+  T dmax = 0;
+  for (int a = 0; a < n; ++a) dmax = fmax(dmax, A[a][a]);
+  const T tol = droptol * dmax;
   for (int k = 0; k < n; ++k) {
-    const float piv = A[k][k];
-    const bool keep = piv > tol && dmax > 0.f;
-    const float inv = keep ? rsqrtf(piv) : 0.f;
+    const T piv = A[k][k];
+    const bool keep = piv > tol && dmax > T(0);
+    const T inv = keep ? rsqrt_t(piv) : T(0);
     __syncwarp();
     if (j == k) {
       A[k][k] = piv * inv;
@@ -266,8 +297,8 @@ __device__ __forceinline__ void cholesky(float (*A)[kMaxR + 1], int n, float* rd
     }
     __syncwarp();
     if (j > k && j < n) {
-      const float rkj = A[k][j];
-      for (int i2 = k + 1; i2 <= j; ++i2) A[i2][j] = fmaf(-A[k][i2], rkj, A[i2][j]);
+      const T rkj = A[k][j];
+      for (int i2 = k + 1; i2 <= j; ++i2) A[i2][j] = fma(-A[k][i2], rkj, A[i2][j]);
     }
     __syncwarp();
   }
@@ -360,16 +391,21 @@ __device__ __forceinline__ void write_rows(const Smem& sm, const HppQrParams& p,
   }
 }
 
-__device__ __forceinline__ void zero_acc(float (&acc)[4][4]) {
+template <typename T>
+__device__ __forceinline__ void zero_acc(T (&acc)[4][4]) {
 #pragma unroll
   for (int u = 0; u < 4; ++u)
 #pragma unroll
-    for (int w = 0; w < 4; ++w) acc[u][w] = 0.f;
+    for (int w = 0; w < 4; ++w) acc[u][w] = T(0);
 }
 
+// kF64: the first pass's Gram, Cholesky factor and inverse in fp64 (fp32
+// inputs); its shared memory follows Smem.
+template <bool kF64>
 __global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_constant__ HppQrParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  Smem64& s64 = *reinterpret_cast<Smem64*>(smem_raw + ((sizeof(Smem) + 15) & ~size_t(15)));
   cg::cluster_group cluster = cg::this_cluster();
   pdl_trigger();
   pdl_wait();
@@ -392,8 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_consta
   for (int pass = 0; pass < 3; ++pass) {
     const int nb = pass == 0 ? r : r + m;
     const Blocking bk(r, nb);
+    const bool f64 = kF64 && pass == 0;
     float acc[4][4];
+    double acc64[4][4];
     zero_acc(acc);
+    if (kF64) zero_acc(acc64);
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
       const int base = row0 + t * kTileRows;
@@ -406,7 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_consta
         apply_matrix(sm, f == 1 ? sm.M1 : sm.M2, r, nv);
         __syncthreads();
       }
-      if (pass < 2) {
+      if (f64) {
+        accumulate(sm, bk, nv, acc64);
+      } else if (pass < 2) {
         accumulate(sm, bk, nv, acc);
       } else {
         tail_rows(sm, r, m, nv);
@@ -416,9 +457,21 @@ __global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_consta
       if (!resident) __syncthreads();
     }
     if (pass == 2) break;
-    stash_acc(sm, acc);
-    publish(sm, bk.nbb, bk.nblk, bk.slices, pass, r, nb);
-    cluster_sum(sm, cluster, pass, r * nb, cs);
+    if (f64) {
+      stash_acc(s64.red, acc64);
+      publish(s64.red, s64.pub, bk.nbb, bk.nblk, bk.slices, r, nb);
+      cluster_sum(s64.pub, s64.sum, cluster, r * nb, cs);
+      for (int e = threadIdx.x; e < r * r; e += kThreads) s64.R[e / r][e % r] = s64.sum[e];
+      __syncthreads();
+      if (threadIdx.x < 32) cholesky(s64.R, r, s64.rd, kDropTol64);
+      __syncthreads();
+      if (threadIdx.x < 32) invert_factor(s64.R, s64.rd, r, sm.M1);
+      __syncthreads();
+      continue;
+    }
+    stash_acc(sm.red, acc);
+    publish(sm.red, sm.pub[pass], bk.nbb, bk.nblk, bk.slices, r, nb);
+    cluster_sum(sm.pub[pass], sm.sum, cluster, r * nb, cs);
     float (*R)[kMaxR + 1] = pass == 0 ? sm.R1 : sm.R2;
     for (int e = threadIdx.x; e < r * nb; e += kThreads) {
       const int a = e / nb, b = e % nb;
@@ -427,9 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_consta
     }
     __syncthreads();
     float* rd = pass == 0 ? sm.rd1 : sm.rd2;
-    if (threadIdx.x < 32) cholesky(R, r, rd);
+    if (threadIdx.x < 32) cholesky(R, r, rd, kDropTol);
     __syncthreads();
-    if (threadIdx.x < 32) invert_factor(R, rd, r, pass == 0 ? sm.M1 : sm.M2);
+    if (threadIdx.x < 32) invert_factor<float>(R, rd, r, pass == 0 ? sm.M1 : sm.M2);
     __syncthreads();
     if (pass == 1) {
       // Cm = R2^-T K = M2^T K, stored transposed; one entry per thread
@@ -451,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) hpp_qr_kernel(const __grid_consta
 // 16 CTAs (a non-portable size) where the device has room for one, else 8.
 // Cached per device and shared-memory size (atomics: calls may come from
 // several host threads).
+template <bool kF64>
 int cluster_cap(size_t smem) {
   static std::atomic<int> cap[16];
   static std::atomic<size_t> cap_smem[16];
@@ -459,8 +513,8 @@ int cluster_cap(size_t smem) {
   const int cached = cap[dev].load(std::memory_order_acquire);
   if (cached && cap_smem[dev].load(std::memory_order_relaxed) == smem) return cached;
   int c = 8;
-  if (cudaFuncSetAttribute(hpp_qr_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-      cudaSuccess) {
+  if (cudaFuncSetAttribute(hpp_qr_kernel<kF64>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           1) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16);
     cfg.blockDim = dim3(kThreads);
@@ -473,7 +527,8 @@ int cluster_cap(size_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, hpp_qr_kernel, &cfg) == cudaSuccess && n > 0) c = 16;
+    if (cudaOccupancyMaxActiveClusters(&n, hpp_qr_kernel<kF64>, &cfg) == cudaSuccess && n > 0)
+      c = 16;
   }
   (void)cudaGetLastError();
   cap_smem[dev].store(smem, std::memory_order_relaxed);
@@ -481,18 +536,23 @@ int cluster_cap(size_t smem) {
   return c;
 }
 
+template <bool kF64>
+cudaError_t launch_qr(const HppQrParams& p_in, cudaStream_t s) {
+  const size_t smem = kF64 ? ((sizeof(Smem) + 15) & ~size_t(15)) + sizeof(Smem64) : sizeof(Smem);
+  cudaError_t e = cudaFuncSetAttribute(hpp_qr_kernel<kF64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  HppQrParams p = p_in;
+  p.cs = std::min(cluster_cap<kF64>(smem), std::max(1, (p.p + kRowsTarget - 1) / kRowsTarget));
+  return launch_pdl(hpp_qr_kernel<kF64>, dim3(p.B * p.cs), dim3(kThreads), smem, s, p.cs, p);
+}
+
 }  // namespace
 
 cudaError_t launch_hpp_qr(const HppQrParams& p_in, cudaStream_t s) {
   if (p_in.r < 1 || p_in.r > kMaxR || p_in.m > kMaxM || p_in.r + p_in.m > kMaxNP)
     return cudaErrorInvalidValue;
-  const size_t smem = sizeof(Smem);
-  cudaError_t e =
-      cudaFuncSetAttribute(hpp_qr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  HppQrParams p = p_in;
-  p.cs = std::min(cluster_cap(smem), std::max(1, (p.p + kRowsTarget - 1) / kRowsTarget));
-  return launch_pdl(hpp_qr_kernel, dim3(p.B * p.cs), dim3(kThreads), smem, s, p.cs, p);
+  return p_in.gram_f64 ? launch_qr<true>(p_in, s) : launch_qr<false>(p_in, s);
 }
 
 }  // namespace dpclip

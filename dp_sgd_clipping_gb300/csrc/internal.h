@@ -165,6 +165,7 @@ struct HppQrParams {
   __nv_bfloat16* out_lo;
   float* out_f32;        // fp32 output [B][32][p]
   uint32_t* err;
+  int gram_f64;          // first pass's Gram, Cholesky and inverse in fp64 (fp32 inputs)
 };
 
 // Generic fp32 SIMT GEMM over a batch:  acc[b](m,n) = sum_k X[b](m,k) Y[b](k,n)

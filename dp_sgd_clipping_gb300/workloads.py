@@ -22,7 +22,7 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "Inputs",
+__all__ = ["Workload", "WORKLOADS", "get", "make_inputs", "make_decaying_inputs", "Inputs",
            "f32_to_bf16_bits", "bf16_bits_to_f32"]
 
 
@@ -117,4 +117,42 @@ def make_inputs(wl: Workload, seed: int | None = None) -> Inputs:
         A_dev, G_dev = A, G
     else:
         raise ValueError(f"unknown dtype {wl.dtype!r}")
+    return Inputs(wl, A, G, A_dev, G_dev, ln)
+
+
+def make_decaying_inputs(wl: Workload, n_dirs: int = 12, ratio: float = 0.5,
+                         floor: float = 1e-2) -> Inputs:
+    """Inputs whose per-sample gradient A_i^T G_i has `n_dirs` singular values
+    decaying geometrically by `ratio`, over a flat floor of i.i.d. noise.
+
+    Per sample, with orthonormal columns E (T x n), X (d x n), Y (p x n) drawn
+    at random:  A_i = sqrt(T d / n) E X^T + floor N(0, 1) and
+    G_i = g_scale L_i (sqrt(T p / n) E diag(ratio^j) Y^T + floor N(0, 1)),
+    so that A_i^T G_i is close to a multiple of X diag(ratio^j) Y^T (entries
+    of A and G stay of order 1 and g_scale L_i).  The stream is numpy's
+    PCG64(3000 + workload id); rounding to bfloat16 as in make_inputs."""
+    rng = np.random.Generator(np.random.PCG64(3000 + wl.wid))
+    B, T, d, p, n = wl.B, wl.T, wl.d, wl.p, n_dirs
+    if min(T, d, p) < n:
+        raise ValueError("T, d and p must be at least n_dirs")
+    A = np.empty((B, T, d), dtype=np.float32)
+    G = np.empty((B, T, p), dtype=np.float32)
+    ln = np.exp(rng.standard_normal(B)).astype(np.float32)
+    decay = ratio ** np.arange(n)
+    for i in range(B):
+        E = np.linalg.qr(rng.standard_normal((T, n)))[0]
+        X = np.linalg.qr(rng.standard_normal((d, n)))[0]
+        Y = np.linalg.qr(rng.standard_normal((p, n)))[0]
+        A[i] = np.sqrt(T * d / n) * (E @ X.T) + floor * rng.standard_normal((T, d))
+        Gi = np.sqrt(T * p / n) * ((E * decay) @ Y.T) + floor * rng.standard_normal((T, p))
+        G[i] = wl.g_scale * ln[i] * Gi
+    if wl.dtype == "bf16":
+        A_dev = f32_to_bf16_bits(A)
+        G_dev = f32_to_bf16_bits(G)
+        A = bf16_bits_to_f32(A_dev).reshape(B, T, d)
+        G = bf16_bits_to_f32(G_dev).reshape(B, T, p)
+        A_dev = A_dev.reshape(B, T, d)
+        G_dev = G_dev.reshape(B, T, p)
+    else:
+        A_dev, G_dev = A, G
     return Inputs(wl, A, G, A_dev, G_dev, ln)

@@ -11,7 +11,8 @@ import torch
 
 import oracle as O
 from dp_sgd_clipping_gb300 import workloads as W
-from gpu_util import TOL, assert_flags, assert_grad, assert_rel, grad_magnitude, host, to_dev
+from gpu_util import (NOISE_TOL, TOL, assert_flags, assert_grad, assert_rel, grad_magnitude, host,
+                      to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,22 +38,39 @@ def oracle_all(inp, k=None, want=("direct", "hutch", "hutchpp")):
     return out
 
 
+def oracle_grad_parts(inp, q32, C, sigma, Ms, offset):
+    """The oracle's clipped sum S = sum_i s_i M_i, its noise sigma C z (None at
+    sigma = 0), the scales, and mag = sum_i s_i |A_i|^T |G_i| for the bound."""
+    wl = inp.wl
+    S, s_ref, _ = O.clipped_noisy_grad(None, None, q32, C, 0.0, wl.seed, offset, Ms=Ms)
+    noise = sigma * C * O.noise_matrix(wl.d, wl.p, wl.seed, offset) if sigma != 0.0 else None
+    return S, noise, s_ref, grad_magnitude(inp.A, inp.G, s_ref)
+
+
 def check_grad(api, inp, A, G, q, C, sigma, Ms, offset=0, stored=None):
-    # stored: the StoredGradients of norms_direct_store; then the gradient comes
-    # from the stored per-sample tiles instead of a second GEMM
+    """The clipped noisy gradient at sigma and, when sigma > 0, again at
+    sigma = 0, each compared with the oracle's clipped sum after taking the
+    oracle's noise away (gpu_util.assert_grad).  stored: the StoredGradients
+    of norms_direct_store; then the gradient comes from the stored per-sample
+    tiles instead of a second GEMM."""
     wl = inp.wl
     tol = TOL[wl.dtype]
     qd = torch.tensor(q, dtype=torch.float32, device="cuda")
-    if stored is None:
-        grad, scales, clipped = api.clipped_noisy_grad(A, G, qd, C, sigma, wl.seed, offset)
-    else:
-        grad, scales, clipped = api.stored_clipped_noisy_grad(stored, qd, C, sigma, wl.seed, offset)
-    torch.cuda.synchronize()
     q32 = qd.double().cpu().numpy()          # the sqnorms the GPU saw
-    D, s_ref, _ = O.clipped_noisy_grad(None, None, q32, C, sigma, wl.seed, offset, Ms=Ms)
-    assert_rel(host(scales), s_ref, 1e-6, "scales")
-    assert_flags(host(clipped), np.sqrt(q32), C, tol)
-    assert_grad(host(grad), D, tol, sigma * C, mag=grad_magnitude(inp.A, inp.G, s_ref))
+    S, noise, s_ref, mag = oracle_grad_parts(inp, q32, C, sigma, Ms, offset)
+    K = wl.B * wl.T
+    grad = None
+    for sg in ((sigma, 0.0) if sigma != 0.0 else (0.0,)):
+        if stored is None:
+            g, scales, clipped = api.clipped_noisy_grad(A, G, qd, C, sg, wl.seed, offset)
+        else:
+            g, scales, clipped = api.stored_clipped_noisy_grad(stored, qd, C, sg, wl.seed, offset)
+        torch.cuda.synchronize()
+        assert_rel(host(scales), s_ref, 1e-6, "scales")
+        assert_flags(host(clipped), np.sqrt(q32), C, tol)
+        assert_grad(host(g), S, tol, K, mag, noise if sg != 0.0 else None, sg * C,
+                    what=f"grad (sigma={sg}, {'stored' if stored is not None else 'gemm'})")
+        grad = g if grad is None else grad
     return grad
 
 
@@ -140,6 +158,29 @@ def test_hutchpp_exact_when_rank_deficient(api):
     A, G = to_dev(inp)
     q = host(api.norms_hutchpp(A, G, 32, wl.seed, 0))
     assert_rel(q, O.sqnorms_direct(inp.A, inp.G), 2e-2, "hutch++ rank-deficient")
+
+
+@pytest.mark.parametrize("case", ["bf16", "f32"])
+def test_hutchpp_decaying_spectrum(api, case):
+    # A_i^T G_i with 12 singular values decaying by 1/2 over a flat floor, the
+    # inputs Hutch++ is meant for: the sketch O_i S spans directions whose
+    # squared singular values fall by 1/4 each, so the Gram of the QR's first
+    # pass has pivots down to ~1e-11 of the largest, and a head that keeps only
+    # the well-conditioned ones leaves the rest to the tail estimate
+    wl = W.Workload(185 if case == "bf16" else 186, f"decay_{case}", 2, 300, 200, 328, case, 1e-2,
+                    1.0, 1.0, 32, ())
+    inp = W.make_decaying_inputs(wl)
+    A, G = to_dev(inp)
+    Ms = list(O.per_sample_grads(inp.A, inp.G))
+    sv = np.linalg.svd(Ms[0], compute_uv=False)
+    assert 0.4 < sv[9] / sv[8] < 0.8 and sv[5] / sv[0] < 0.04     # the spectrum decays
+    S, Gp = O.hutchpp_probes(wl.p, wl.k, wl.seed, 0, wl.dtype)
+    ref = O.sqnorms_hutchpp(None, None, S, Gp, Ms=Ms)
+    assert_rel(host(api.norms_hutchpp(A, G, wl.k, wl.seed, 0)), ref, TOL[wl.dtype],
+               "hutch++ decaying spectrum")
+    P = O.hutch_probe(wl.p, wl.k, wl.seed, 0, wl.dtype)
+    assert_rel(host(api.norms_hutch(A, G, wl.k, wl.seed, 0)),
+               O.sqnorms_hutch(None, None, P, Ms=Ms), TOL[wl.dtype], "hutch decaying spectrum")
 
 
 def test_zero_gradients(api):
@@ -304,23 +345,39 @@ def test_bias_grads(api, wid):
     assert_rel(host(q_tot), q_ref, tol, "weights + bias sqnorms")
     C = float(np.median(np.sqrt(q_ref)))
     q32 = host(q_tot).astype(np.float64)
-    Db = host(api.clipped_noisy_bias_grad(bg, q_tot, C, wl.sigma, wl.seed, 11))
-    Db_ref, s_ref, _ = O.clipped_noisy_bias_grad(None, q32, C, wl.sigma, wl.seed, 11, bs=b_ref)
-    mag = np.abs(Db_ref) + wl.sigma * C + np.sum(s_ref[:, None] * np.abs(b_ref), axis=0)
-    assert np.all(np.abs(Db - Db_ref) <= tol * mag)
+    Sb, nb, s_ref, bmag = bias_parts(inp, b_ref, q32, C, wl.sigma, 11)
+    for sg in (wl.sigma, 0.0):
+        Db = host(api.clipped_noisy_bias_grad(bg, q_tot, C, sg, wl.seed, 11))
+        assert_grad(Db, Sb, tol, wl.B * wl.T, bmag, nb if sg else None, sg * C,
+                    what=f"bias grad (sigma={sg})")
 
 
-def _check_update(theta0, theta1, D_ref, scale, tol, mag):
-    # theta1 = theta0 - scale * g, g within tolerance of the oracle's D
-    want = theta0.astype(np.float64) - scale * D_ref
-    slack = tol * scale * (np.abs(D_ref) + mag) + 4 * np.spacing(np.abs(theta0).astype(np.float32))
-    assert np.all(np.abs(theta1 - want) <= slack)
+def bias_parts(inp, b_ref, q32, C, sigma, offset):
+    """The oracle's clipped bias sum sum_i s_i b_i, its noise (stream 4), the
+    scales and mag = sum_i s_i sum_t |G_i[t, :]| for the bound."""
+    wl = inp.wl
+    Sb, s_ref, _ = O.clipped_noisy_bias_grad(None, q32, C, 0.0, wl.seed, offset, bs=b_ref)
+    noise = (sigma * C * O.philox_normals(wl.p, wl.seed, O.STREAM_BIAS_NOISE, offset)
+             if sigma != 0.0 else None)
+    absb = np.abs(inp.G).astype(np.float64).sum(axis=1)
+    return Sb, noise, s_ref, np.sum(s_ref[:, None] * absb, axis=0)
+
+
+def _check_update(theta0, theta1, scale, S, noise, tol, K, mag, sigmaC, what):
+    """theta1 = theta0 - scale * g: the step taken, divided by scale, is the
+    gradient the kernel applied, compared with the oracle's clipped sum after
+    taking its noise away.  The parameters are rounded to fp32 once more,
+    hence a slack of two of their ulps (in gradient units)."""
+    g_eff = (theta0.astype(np.float64) - theta1) / scale
+    slack = 2.0 * np.spacing(np.abs(theta1).astype(np.float32)).astype(np.float64) / scale
+    assert_grad(g_eff, S, tol, K, mag, noise, sigmaC, slack=slack, what=what)
 
 
 @pytest.mark.parametrize("path", ["gemm_bf16", "gemm_f32", "stored_bf16"])
 def test_fused_sgd_update(api, path):
     # weights and bias updated in place by the gradient calls, with and
-    # without the gradient itself being stored
+    # without the gradient itself being stored; the parameters start at the
+    # size of one step so that their rounding does not hide the clipped sum
     if path == "gemm_f32":
         wl = W.Workload(170, "f32_odd", 3, 37, 29, 50, "f32", 1.0, 1.0, 1.0, 7, ())
     else:
@@ -328,17 +385,18 @@ def test_fused_sgd_update(api, path):
     inp = W.make_inputs(wl)
     A, G = to_dev(inp)
     tol = TOL[wl.dtype]
+    K = wl.B * wl.T
     Ms = list(O.per_sample_grads(inp.A, inp.G))
     q_ref = O.sqnorms_direct(inp.A, inp.G) + O.bias_sqnorms(inp.G)
     C = float(np.median(np.sqrt(q_ref)))
     qd = torch.tensor(q_ref, dtype=torch.float32, device="cuda")
     q32 = host(qd).astype(np.float64)
-    D_ref, s_ref, _ = O.clipped_noisy_grad(None, None, q32, C, wl.sigma, wl.seed, 5, Ms=Ms)
-    mag = grad_magnitude(inp.A, inp.G, s_ref) + wl.sigma * C
+    S, noise, s_ref, mag = oracle_grad_parts(inp, q32, C, wl.sigma, Ms, 5)
     lr, L = 0.3, 7.0
+    scale = lr / L
     rng = np.random.default_rng(3)
     for store in (True, False):
-        theta0 = rng.standard_normal((wl.d, wl.p)).astype(np.float32)
+        theta0 = (scale * np.abs(S).max() * rng.standard_normal((wl.d, wl.p))).astype(np.float32)
         theta = torch.tensor(theta0, device="cuda")
         upd = api.SGDUpdate(theta, lr, L, store_grad=store)
         if path == "stored_bf16":
@@ -346,21 +404,21 @@ def test_fused_sgd_update(api, path):
             g, _, _ = api.stored_clipped_noisy_grad(stored, qd, C, wl.sigma, wl.seed, 5, update=upd)
         else:
             g, _, _ = api.clipped_noisy_grad(A, G, qd, C, wl.sigma, wl.seed, 5, update=upd)
-        _check_update(theta0, host(theta), D_ref, lr / L, tol, mag)
+        _check_update(theta0, host(theta), scale, S, noise, tol, K, mag, wl.sigma * C,
+                      f"{path} update (grad stored: {store})")
         if store:
-            assert_grad(host(g), D_ref, tol, wl.sigma * C, mag=grad_magnitude(inp.A, inp.G, s_ref))
+            assert_grad(host(g), S, tol, K, mag, noise, wl.sigma * C, what=f"{path} grad")
         elif path != "gemm_f32":
             assert g is None
     # the bias
     q_b, bg = api.bias_grads(G)
     b_ref = O.per_sample_bias_grads(inp.G)
-    Db_ref, _, _ = O.clipped_noisy_bias_grad(None, q32, C, wl.sigma, wl.seed, 5, bs=b_ref)
-    beta0 = rng.standard_normal(wl.p).astype(np.float32)
+    Sb, nb, _, bmag = bias_parts(inp, b_ref, q32, C, wl.sigma, 5)
+    beta0 = (scale * np.abs(Sb).max() * rng.standard_normal(wl.p)).astype(np.float32)
     beta = torch.tensor(beta0, device="cuda")
     api.clipped_noisy_bias_grad(bg, qd, C, wl.sigma, wl.seed, 5,
                                 update=api.SGDUpdate(beta, lr, L, store_grad=False))
-    bmag = np.abs(Db_ref) + wl.sigma * C + np.sum(s_ref[:, None] * np.abs(b_ref), axis=0)
-    _check_update(beta0, host(beta), Db_ref, lr / L, tol, bmag)
+    _check_update(beta0, host(beta), scale, Sb, nb, tol, K, bmag, wl.sigma * C, f"{path} bias update")
 
 
 def test_empty_poisson_lot(api):
@@ -387,25 +445,32 @@ def test_gradient_noise_is_the_oracle_stream(api):
     # With A = 0 (G = 0 for the bias) the clipped sum vanishes and each path
     # returns sigma C z, z the Philox normals of its stream at element r p + c
     # (stream 3) or c (stream 4).  The kernels draw them with the SFU's log2,
-    # sine and cosine: every value within 2e-5 of the fp64 transform.
+    # sine and cosine (and a series for the log near 1): every value within
+    # NOISE_TOL of the fp64 transform.
+    # The bf16 GEMM case draws a whole up_proj gradient (2048 x 8192 normals),
+    # the size at which NOISE_TOL is used by the gradient checks.
     C, sigma, seed, off = 2.0, 1.5, 0x5EED, 11
-    tol = 2e-5 * sigma * C
+    tol = NOISE_TOL * sigma * C
     for dtype, (B, T, d, p) in ((torch.bfloat16, (3, 70, 200, 328)),
+                                (torch.bfloat16, (1, 16, 2048, 8192)),
                                 (torch.float32, (2, 9, 24, 40))):
         A = torch.zeros(B, T, d, dtype=dtype, device="cuda")
         G = torch.randn(B, T, p, device="cuda").to(dtype)
         q = torch.ones(B, device="cuda")
         z = O.philox_normals(d * p, seed, 3, off).reshape(d, p)
         g, _, _ = api.clipped_noisy_grad(A, G, q, C, sigma, seed, off)
-        assert np.max(np.abs(host(g) - sigma * C * z)) < tol, dtype
+        err = np.max(np.abs(host(g) - sigma * C * z))
+        assert err < tol, f"{dtype} {d}x{p} gemm: {err / (sigma * C):.2e} sigma C"
         q2, stored = api.norms_direct_store(A, G)
         gs, _, _ = api.stored_clipped_noisy_grad(stored, q, C, sigma, seed, off)
-        assert np.max(np.abs(host(gs) - sigma * C * z)) < tol, dtype
+        err = np.max(np.abs(host(gs) - sigma * C * z))
+        assert err < tol, f"{dtype} {d}x{p} stored: {err / (sigma * C):.2e} sigma C"
     p = 520
     zb = O.philox_normals(p, seed, 4, off)
     _, bg = api.bias_grads(torch.zeros(2, 33, p, dtype=torch.bfloat16, device="cuda"))
     gb = api.clipped_noisy_bias_grad(bg, torch.ones(2, device="cuda"), C, sigma, seed, off)
-    assert np.max(np.abs(host(gb) - sigma * C * zb)) < tol
+    err = np.max(np.abs(host(gb) - sigma * C * zb))
+    assert err < tol, f"bias: {err / (sigma * C):.2e} sigma C"
 
 
 FIBER_HP = dict(lr=0.05, beta1=0.9, beta2=0.99, eps=1e-6, eps_v=1e-10, weight_decay=0.01,
@@ -473,6 +538,9 @@ def test_fiber_fused(api, path):
         _, stored = api.norms_direct_store(A, G)
     if path == "bias":
         _, bg = api.bias_grads(G)
+    q32 = host(q)
+    tol, K = TOL[wl.dtype], wl.B * wl.T
+    Ms = list(O.per_sample_grads(inp.A, inp.G)) if path not in ("bias", "empty") else None
     for step in range(2):
         if path == "stored_bf16":
             g, _, _ = api.stored_clipped_noisy_grad(stored, q, C, wl.sigma, wl.seed, step, fiber=opt)
@@ -482,6 +550,14 @@ def test_fiber_fused(api, path):
             g, _, _ = api.clipped_noisy_grad(A, G, q[:A.shape[0]], C, wl.sigma, wl.seed, step,
                                              fiber=opt)
         grads.append(host(g).copy())
+        # the gradient the step was fed, against the oracle's clipped sum
+        if path == "bias":
+            Sb, nb, _, bmag = bias_parts(inp, O.per_sample_bias_grads(inp.G), q32, C, wl.sigma,
+                                         step)
+            assert_grad(grads[-1], Sb, tol, K, bmag, nb, wl.sigma * C, what="fiber bias grad")
+        elif path != "empty":
+            S, noise, _, mag = oracle_grad_parts(inp, q32, C, wl.sigma, Ms, step)
+            assert_grad(grads[-1], S, tol, K, mag, noise, wl.sigma * C, what=f"fiber {path} grad")
         ref = _fiber_oracle_steps(theta0, grads, denom, nv, FIBER_HP)[-1]
         _check_fiber(opt, ref, theta0)
 
@@ -515,7 +591,8 @@ def test_long_sequence_narrow_layer(api):
 
 
 def test_grad_tail_split_over_k(api):
-    # several full waves of tiles plus a remainder split by sample and K
+    # 64 pair tiles on 76 CTA pairs: no full wave, every tile is cut into
+    # bands over its samples and K-blocks and summed from partial tiles
     wl = W.Workload(173, "waves", 2, 1100, 1024, 4096, "bf16", 1e-3, 0.5, 0.0, 8, ())
     inp = W.make_inputs(wl)
     A, G = to_dev(inp)
