@@ -89,6 +89,7 @@ SIGNATURES = {
     "dpclip_stored_clipped_noisy_grad": (_i, [_i, _i, _i, _vp, _f, _f, _u64, _u64, _vp, _vp, _vp,
                                               _vp, _sz, _vp]),
     "dpclip_norms_hutch_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _u64, _u64, _vp, _vp]),
+    "dpclip_noalloc_status": (_i, [_vp]),
     "dpclip_philox_normal": (_i, [_vp, _i64, _i, _u64, _u32, _u64, _vp]),
     "dpclip_workspace_status": (_i, [_vp, _vp]),
     "dpclip_selftest_wait_timeout": (_i, [_vp, _sz, _i, _vp]),

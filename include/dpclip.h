@@ -310,13 +310,26 @@ int dpclip_philox_normal(void* out, int64_t n, int dtype, uint64_t seed, uint32_
  * workspace (dpclip_workspace_size) exceeds it return DPCLIP_ERR_WORKSPACE
  * before anything is enqueued.  The first call on a device looks up the
  * array's device address with that device current; make that first call
- * before any stream capture.  Every call shares the array and it keeps the
- * last call's contents (each call clears what must start at zero): calls that
- * can overlap on the GPU race on it, so issue them on one stream.  Never calls
- * cudaMalloc, cudaFree or any allocating routine. */
+ * before any stream capture.  The address is kept per device and context: a
+ * device reset (cudaDeviceReset) destroys the array, and the first call in
+ * the new context looks the address up again.  Every call shares the array
+ * and it keeps the last call's contents (each call clears what must start at
+ * zero): calls that can overlap on the GPU race on it, so issue them on one
+ * stream.  Never calls cudaMalloc, cudaFree or any allocating routine.  A
+ * bounded wait that expires on the device is not reported by the return
+ * value (the call returns once its kernels are enqueued): read it with
+ * dpclip_noalloc_status. */
 int dpclip_norms_hutch_noalloc(const void* A, const void* G, int B, int T, int d, int p,
                                int dtype, int k, uint64_t seed, uint64_t offset, float* sqnorms,
                                dpclip_stream_t stream);
+
+/* Synchronises `stream`, then returns DPCLIP_OK or the error that the device
+ * recorded in the scratch array of dpclip_norms_hutch_noalloc on the current
+ * device (DPCLIP_ERR_TIMEOUT: a bounded wait expired and the norms of that
+ * call are not valid), or DPCLIP_ERR_CUDA if the synchronisation or the read
+ * failed.  The array is shared, so this is the status of the last call that
+ * ran on it.  Allocates nothing. */
+int dpclip_noalloc_status(dpclip_stream_t stream);
 
 /* The n Rademacher values of one Philox stream (see dpclip_probe), written as
  * float or bfloat16 into `out` (device, 4-byte aligned). */
