@@ -1,7 +1,7 @@
 """The bench's output contract: one JSON line with the keys a driver reads.
 
-The reference arm (the fp64 oracle on a bounded sample) runs on the CPU in a
-few seconds; the library's arm needs a GPU.
+The reference arm (the fp64 oracle over all of one sample) runs on the CPU in
+well under a minute per step; the library's arm needs a GPU.
 """
 import json
 import os
@@ -40,8 +40,8 @@ def _check_common(line, steps, warmup):
 
 
 def test_reference_arm_line():
-    line = _run(["--impl", "reference", "--steps", "1", "--warmup", "3"], timeout=600)
-    _check_common(line, 1, 3)
+    line = _run(["--impl", "reference", "--steps", "1", "--warmup", "1"], timeout=600)
+    _check_common(line, 1, 1)
     assert line["impl"] == "reference" and line["dtype"] == "f64"
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
@@ -67,3 +67,14 @@ def test_library_arm_line():
     # the end-to-end leg moves the inputs in and the results out every step
     assert line["e2e"]["h2d_bytes_per_step"] == 2 * 4 * 4096 * (2048 + 8192)
     assert line["e2e"]["d2h_bytes_per_step"] >= 4 * 2048 * 8192
+    # the other standard workloads, each with the rows it names
+    cf = line["configs"]
+    assert set(cf) == {"tiny_f32_B4_T64_d32_p48", "exact_bf16_B8_T512_d768_p768",
+                       "q_proj_bf16_B4_T4096_d2048_p2048", "long_ctx_bf16_B2_T16384_d2048_p2048"}
+    assert set(cf["long_ctx_bf16_B2_T16384_d2048_p2048"]["rows"]) == {
+        "hutch", "hutchpp", "exact_direct", "clipped_noisy_grad"}
+    for name, c in cf.items():
+        for r, e in c["rows"].items():
+            assert e["ms"] > 0, (name, r)
+            if e["bound"] != "latency":
+                assert 0 < e["frac"] < 1.5, (name, r)
