@@ -220,6 +220,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
+// 16 bytes into the shared memory of a CTA of the cluster (address from
+// mapa_shared, 16-byte aligned).  A posted store: a later cluster barrier
+// (release / acquire) makes it visible to that CTA.
+__device__ __forceinline__ void st_dsmem_v4(uint32_t caddr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 // All threads of all CTAs of the cluster (release / acquire at cluster scope).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile(

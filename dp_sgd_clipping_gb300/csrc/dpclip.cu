@@ -40,10 +40,12 @@ struct Carve {
 };
 
 // K-split factor of a skinny GEMM: enough CTAs to keep ~two per SM resident,
-// at least 4 K-blocks per split, no empty split.
+// at least 4 K-blocks per split, no empty split, at most kMaxSplits (the
+// splits of a tile form one cluster).
 void choose_splits(int ntiles, int kblocks, int& splits, int& per) {
   int s = std::max(1, kTargetCtas / std::max(1, ntiles));
   s = std::min(s, std::max(1, kblocks / 4));
+  s = std::min(s, kMaxSplits);
   per = cdiv(kblocks, s);
   splits = cdiv(kblocks, per);
 }
@@ -126,9 +128,9 @@ struct Plan {
 };
 
 enum {
-  kP = 0, kYhi, kYlo, kPart, kPart2, kQpart,                 // hutch
+  kP = 0, kYhi, kYlo, kQpart,                                // hutch
   kS = 0, kGp, kY1hi, kY1lo, kZ1hi, kZ1lo, kUhi, kUlo,       // hutch++ ...
-  kV, kQWhi, kQWlo, kY3hi, kY3lo, kHPart, kHQpart,
+  kV, kQWhi, kQWlo, kY3hi, kY3lo, kHQpart,
 };
 
 int np_for(int n) { return n <= 16 ? 16 : 32; }
@@ -139,20 +141,14 @@ Plan plan_hutch_bf16(int B, int T, int d, int p, int k) {
   pl.mtiles = cdiv(T, kTokTileM);
   pl.Tp = pl.mtiles * kTokTileM;
   pl.tblocks = cdiv(T, kBlockK);
-  int s1, per1, s2, per2;
-  choose_splits(B * pl.mtiles, cdiv(p, kBlockK), s1, per1);
   const int ftiles = cdiv(d, kFeatTileM);
-  choose_splits(B * ftiles, pl.tblocks, s2, per2);
   Carve c;
-  const size_t ncnt = std::max<size_t>((size_t)B * pl.mtiles, (size_t)B * ftiles + B);
-  pl.ctrl_bytes = align_up(4 * (1 + ncnt), kAlign);
+  pl.ctrl_bytes = align_up(4 * (1 + (size_t)B), kAlign);   // error word, per-sample tickets
   pl.ctrl = c.take(pl.ctrl_bytes);
   pl.off[kP] = c.take((size_t)NP * p * 2);
   pl.off[kYhi] = c.take((size_t)B * NP * pl.Tp * 2);
   pl.off[kYlo] = c.take((size_t)B * NP * pl.Tp * 2);
-  pl.off[kPart] = c.take(s1 > 1 ? (size_t)s1 * B * NP * pl.Tp * 4 : 0);
-  pl.off[kPart2] = c.take(s2 > 1 ? (size_t)s2 * B * NP * ftiles * kFeatTileM * 4 : 0);
-  pl.off[kQpart] = c.take((size_t)B * ftiles * 4);
+  pl.off[kQpart] = c.take((size_t)B * ftiles * kMaxSplits * 4);
   pl.total = c.total();
   return pl;
 }
@@ -165,21 +161,8 @@ Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
   pl.Tp = pl.mtiles * kTokTileM;
   pl.tblocks = cdiv(T, kBlockK);
   const int fd = cdiv(d, kFeatTileM), fp = cdiv(p, kFeatTileM);
-  size_t part = 0;
-  for (int F : {p, d}) {   // tok_gemm over features F (NP up to 32)
-    int s, per;
-    choose_splits(B * pl.mtiles, cdiv(F, kBlockK), s, per);
-    if (s > 1) part = std::max(part, (size_t)s * B * 32 * pl.Tp * 4);
-  }
-  for (int ft : {fd, fp}) {  // feat_gemm over tokens
-    int s, per;
-    choose_splits(B * ft, pl.tblocks, s, per);
-    if (s > 1) part = std::max(part, (size_t)s * B * 32 * ft * kFeatTileM * 4);
-  }
   Carve c;
-  const size_t ncnt =
-      std::max<size_t>((size_t)B * pl.mtiles, (size_t)B * std::max(fd, fp) + B);
-  pl.ctrl_bytes = align_up(4 * (1 + ncnt), kAlign);
+  pl.ctrl_bytes = align_up(4 * (1 + (size_t)B), kAlign);   // error word, per-sample tickets
   pl.ctrl = c.take(pl.ctrl_bytes);
   pl.off[kS] = c.take((size_t)16 * p * 2);
   pl.off[kGp] = c.take((size_t)32 * p * 2);
@@ -194,8 +177,7 @@ Plan plan_hutchpp_bf16(int B, int T, int d, int p, int k) {
   pl.off[kQWlo] = c.take((size_t)B * 32 * p * 2);
   pl.off[kY3hi] = c.take((size_t)B * 32 * pl.Tp * 2);
   pl.off[kY3lo] = c.take((size_t)B * 32 * pl.Tp * 2);
-  pl.off[kHPart] = c.take(part);
-  pl.off[kHQpart] = c.take((size_t)B * std::max(fd, fp) * 4);
+  pl.off[kHQpart] = c.take((size_t)B * std::max(fd, fp) * kMaxSplits * 4);
   pl.total = c.total();
   return pl;
 }
@@ -371,7 +353,7 @@ T* at(void* ws, size_t off) {
 
 // ------------------------------------------------------------------ skinny launches
 int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo, int NP,
-            bool per_sample, const Plan& pl, void* ws, size_t part_off, void* out_hi, void* out_lo,
+            bool per_sample, const Plan& pl, void* ws, void* out_hi, void* out_lo,
             cudaStream_t s) {
   TokGemmParams tp;
   std::memset(&tp, 0, sizeof(tp));
@@ -395,15 +377,13 @@ int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo
   tp.Tp = pl.Tp;
   tp.out_hi = static_cast<__nv_bfloat16*>(out_hi);
   tp.out_lo = static_cast<__nv_bfloat16*>(out_lo);
-  tp.part = at<float>(ws, part_off);
-  tp.counters = at<uint32_t>(ws, pl.ctrl + 4);
   tp.err = at<uint32_t>(ws, pl.ctrl);
   DPCLIP_CUDA(launch_tok_gemm(tp, s));
   return DPCLIP_OK;
 }
 
 int run_feat(const void* X, int B, int T, int F, const void* Yhi, const void* Ylo, int NP, int mode,
-             const float* w, const Plan& pl, void* ws, size_t part_off, size_t qpart_off,
+             const float* w, const Plan& pl, void* ws, size_t qpart_off,
              float* out_f32, void* out_hi, void* out_lo, float* sq, cudaStream_t s) {
   FeatGemmParams fp;
   std::memset(&fp, 0, sizeof(fp));
@@ -424,7 +404,6 @@ int run_feat(const void* X, int B, int T, int F, const void* Yhi, const void* Yl
   fp.out_hi = static_cast<__nv_bfloat16*>(out_hi);
   fp.out_lo = static_cast<__nv_bfloat16*>(out_lo);
   fp.sq = sq;
-  fp.part = at<float>(ws, part_off);
   fp.qpart = at<float>(ws, qpart_off);
   fp.counters = at<uint32_t>(ws, pl.ctrl + 4);
   fp.err = at<uint32_t>(ws, pl.ctrl);
@@ -606,10 +585,10 @@ int dpclip_norms_hutch_ex(const void* A, const void* G, int B, int T, int d, int
     DPCLIP_CUDA(launch_philox_fill(P, NP, p, k, true, seed, 0u, offset, s, ctrl, ctrl_words, probe));
     void* Yhi = at<void>(ws, pl.off[kYhi]);
     void* Ylo = at<void>(ws, pl.off[kYlo]);
-    DPCLIP_TRY(run_tok(G, B, T, p, P, nullptr, NP, false, pl, ws, pl.off[kPart], Yhi, Ylo, s));
+    DPCLIP_TRY(run_tok(G, B, T, p, P, nullptr, NP, false, pl, ws, Yhi, Ylo, s));
     float w[kMaxNP];
     for (int j = 0; j < kMaxNP; ++j) w[j] = j < k ? 1.f / (float)k : 0.f;
-    DPCLIP_TRY(run_feat(A, B, T, d, Yhi, Ylo, NP, kFeatSqNorm, w, pl, ws, pl.off[kPart2],
+    DPCLIP_TRY(run_feat(A, B, T, d, Yhi, Ylo, NP, kFeatSqNorm, w, pl, ws,
                         pl.off[kQpart], nullptr, nullptr, nullptr, sqnorms, s));
     return DPCLIP_OK;
   }
@@ -662,14 +641,14 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
     float* V = at<float>(ws, pl.off[kV]);
     void *QWh = at<void>(ws, pl.off[kQWhi]), *QWl = at<void>(ws, pl.off[kQWlo]);
     void *Y3h = at<void>(ws, pl.off[kY3hi]), *Y3l = at<void>(ws, pl.off[kY3lo]);
-    const size_t part = pl.off[kHPart], qpart = pl.off[kHQpart];
+    const size_t qpart = pl.off[kHQpart];
     // sweep 1: Y1 = G S, Z1 = A^T Y1
-    DPCLIP_TRY(run_tok(G, B, T, p, S, nullptr, 16, false, pl, ws, part, Y1h, Y1l, s));
-    DPCLIP_TRY(run_feat(A, B, T, d, Y1h, Y1l, 16, kFeatOutHiLo, nullptr, pl, ws, part, qpart,
+    DPCLIP_TRY(run_tok(G, B, T, p, S, nullptr, 16, false, pl, ws, Y1h, Y1l, s));
+    DPCLIP_TRY(run_feat(A, B, T, d, Y1h, Y1l, 16, kFeatOutHiLo, nullptr, pl, ws, qpart,
                         nullptr, Z1h, Z1l, nullptr, s));
     // sweep 2: U = A Z1, V = G^T U  (= O S)
-    DPCLIP_TRY(run_tok(A, B, T, d, Z1h, Z1l, 16, true, pl, ws, part, Uh, Ul, s));
-    DPCLIP_TRY(run_feat(G, B, T, p, Uh, Ul, 16, kFeatOutF32, nullptr, pl, ws, part, qpart, V,
+    DPCLIP_TRY(run_tok(A, B, T, d, Z1h, Z1l, 16, true, pl, ws, Uh, Ul, s));
+    DPCLIP_TRY(run_feat(G, B, T, p, Uh, Ul, 16, kFeatOutF32, nullptr, pl, ws, qpart, V,
                         nullptr, nullptr, nullptr, s));
     // Q, W
     HppQrParams hq;
@@ -687,8 +666,8 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
     hq.err = at<uint32_t>(ws, pl.ctrl);
     DPCLIP_CUDA(launch_hpp_qr(hq, s));
     // sweep 3: Y3 = G [Q | W], head + tail / m from A^T Y3
-    DPCLIP_TRY(run_tok(G, B, T, p, QWh, QWl, 32, true, pl, ws, part, Y3h, Y3l, s));
-    DPCLIP_TRY(run_feat(A, B, T, d, Y3h, Y3l, 32, kFeatSqNorm, w, pl, ws, part, qpart, nullptr,
+    DPCLIP_TRY(run_tok(G, B, T, p, QWh, QWl, 32, true, pl, ws, Y3h, Y3l, s));
+    DPCLIP_TRY(run_feat(A, B, T, d, Y3h, Y3l, 32, kFeatSqNorm, w, pl, ws, qpart, nullptr,
                         nullptr, nullptr, sqnorms, s));
     return DPCLIP_OK;
   }

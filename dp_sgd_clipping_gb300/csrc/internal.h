@@ -17,11 +17,12 @@ namespace dpclip {
 
 // Launches `kernel` with programmatic stream serialisation, so that its
 // prologue overlaps the tail of the previous kernel in the stream (the kernel
-// itself waits for that kernel before touching global memory).  cluster_x > 0
-// groups consecutive CTAs along x into thread-block clusters of that size.
+// itself waits for that kernel before touching global memory).  A cluster
+// with cluster.x > 0 groups CTAs into thread-block clusters of those
+// dimensions; cluster.x == 0 launches without a cluster attribute.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t s, int cluster_x, Args&&... args) {
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t s, dim3 cluster, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -31,12 +32,22 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = (unsigned)(cluster_x > 0 ? cluster_x : 1);
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  attr[1].val.clusterDim.x = cluster.x;
+  attr[1].val.clusterDim.y = cluster.y;
+  attr[1].val.clusterDim.z = cluster.z;
   cfg.attrs = attr;
-  cfg.numAttrs = cluster_x > 0 ? 2 : 1;
+  cfg.numAttrs = cluster.x > 0 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The same with clusters of cluster_x consecutive CTAs along x (none when
+// cluster_x <= 0).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, int cluster_x, Args&&... args) {
+  return launch_pdl_cluster(kernel, grid, block, smem, s,
+                            cluster_x > 0 ? dim3((unsigned)cluster_x, 1, 1) : dim3(0, 0, 0),
+                            std::forward<Args>(args)...);
 }
 
 // ----------------------------------------------------------------------------
@@ -50,6 +61,7 @@ constexpr int kDpTileN = 256;      // p columns per gradient / direct-norm tile
 constexpr int kGhostTile = 128;    // tokens per CTA of a ghost Gram pair tile (256 x 256)
 constexpr int kEpiWarps = 8;       // epilogue warps of the persistent kernels
 constexpr int kMaxNP = 32;         // widest skinny operand (probe columns)
+constexpr int kMaxSplits = 8;      // K-splits of a skinny tile (one portable cluster)
 
 // Skinny-GEMM epilogue modes of feat_gemm.
 enum FeatMode { kFeatOutF32 = 0, kFeatOutHiLo = 1, kFeatSqNorm = 2 };
@@ -66,8 +78,6 @@ struct TokGemmParams {
   int mtiles, kblocks, splits, kb_per_split, Tp;
   __nv_bfloat16* out_hi;
   __nv_bfloat16* out_lo;
-  float* part;           // [splits][B][NP][Tp] when splits > 1
-  uint32_t* counters;    // [B * mtiles]
   uint32_t* err;
 };
 
@@ -86,9 +96,8 @@ struct FeatGemmParams {
   __nv_bfloat16* out_hi;
   __nv_bfloat16* out_lo;
   float* sq;             // [B] output of the sqnorm mode
-  float* part;           // [splits][B][NP][Fp] when splits > 1
-  float* qpart;          // [B][ftiles]
-  uint32_t* counters;    // [B * ftiles] then [B]
+  float* qpart;          // [B][ftiles][splits]: each CTA's share of the square sum
+  uint32_t* counters;    // [B]: CTAs of the sample done (sqnorm mode)
   uint32_t* err;
 };
 

@@ -15,9 +15,15 @@
 //
 // Skinny operands are bf16 hi + lo pairs (two MMAs into one fp32 TMEM
 // accumulator), so a fp32 intermediate keeps ~16 significant bits.  A split
-// of the K range over several CTAs is reduced deterministically: partials go
-// to the workspace and the last CTA of a tile (found with an integer ticket)
-// adds them in split order.
+// of the K range over several CTAs is reduced deterministically inside a
+// thread-block cluster: the splits of a tile are the CTAs of one cluster
+// (along y).  CTA q of the cluster finishes the rows r with r % splits == q:
+// every CTA stores its partial of those rows into CTA q's shared memory
+// (posted stores), and after a cluster barrier CTA q adds them, in split
+// order, from its own shared memory.  The former global round trip per
+// partial (store, fence, ticket, reload by the last CTA) cost about 5 us of
+// dependent latency at the end of every feature-side sweep, and pulling the
+// partials over the cluster with remote loads about 3 us.
 //
 // Warp roles (128 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
 // tcgen05.mma, then all four warps drain TMEM (warp w owns TMEM lanes
@@ -71,21 +77,44 @@ __device__ void drain_after_abort(SmemCtl* ctl) {
     if (globaltimer_ns() - t0 > lim) break;
 }
 
-// Sum over the K-splits of one tile row: acc[j] = sum_s base[s*split_stride + j*ld].
-// Each split's NP loads are issued together (one L2 round trip per split,
-// not per element); splits are added in index order (deterministic).
+// Sum of one tile's K-split partials over the cluster that holds them (see
+// the header).  z: this thread's row of this CTA's partial (row = thread);
+// zs: this CTA's idle pipeline stages, which receive [splits][rows owned]
+// rows of NP + 4 floats.  Returns true for the rows this CTA finishes
+// (row % splits == rank), with their sums in z.  Every CTA of the cluster
+// calls it (it holds two cluster barriers).
 template <int NP>
-__device__ __forceinline__ void sum_split_partials(const float* base, size_t split_stride, int ld,
-                                                   int splits, float (&acc)[NP]) {
+__device__ __forceinline__ bool cluster_reduce_rows(float* zs, SmemCtl* ctl, float (&z)[32],
+                                                    int row, int rank, int splits) {
+  constexpr int ld = NP + 4;   // 16-byte rows, 4-bank stagger between rows
+  const int rmax = (kTokTileM + splits - 1) / splits;
+  __syncthreads();
+  // no copy may still land in the stages that zs reuses
+  if (ctl->abort_flag && threadIdx.x == 0) drain_after_abort(ctl);
+  cluster_sync_all();   // every CTA's stages are idle: they may receive rows
+  const int owner = row % splits, k = row / splits;
+  const uint32_t dst = mapa_shared(smem_u32(zs + ((size_t)rank * rmax + k) * ld), (uint32_t)owner);
 #pragma unroll
-  for (int j = 0; j < NP; ++j) acc[j] = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    float v[NP];
+  for (int c = 0; c < NP / 4; ++c)
+    st_dsmem_v4(dst + 16u * c, z[4 * c], z[4 * c + 1], z[4 * c + 2], z[4 * c + 3]);
+  cluster_sync_all();   // every row has been delivered
+  const bool mine = owner == rank;
+  if (mine) {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) v[j] = __ldcg(base + (size_t)s * split_stride + (size_t)j * ld);
+    for (int j = 0; j < NP; ++j) z[j] = 0.f;
+    for (int q = 0; q < splits; ++q) {
+      const float* src = zs + ((size_t)q * rmax + k) * ld;
 #pragma unroll
-    for (int j = 0; j < NP; ++j) acc[j] += v[j];
+      for (int c = 0; c < NP / 4; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(src + 4 * c);
+        z[4 * c] += v.x;
+        z[4 * c + 1] += v.y;
+        z[4 * c + 2] += v.z;
+        z[4 * c + 3] += v.w;
+      }
+    }
   }
+  return mine;
 }
 
 // ---------------------------------------------------------------------------
@@ -192,44 +221,24 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
   const size_t plane = (size_t)NP * p.Tp;
   // tcgen05.ld is warp-collective: decide per warp
   const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->done, 0, wc));
+  float y[32];
   if (ok) {
     tc_fence_after();
-    float y[32];
     tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), y);
-    if (p.splits == 1) {
+  } else {
 #pragma unroll
-      for (int j = 0; j < NP; ++j) {
-        __nv_bfloat16 hi, lo;
-        split_hilo(y[j], hi, lo);
-        p.out_hi[(size_t)i * plane + (size_t)j * p.Tp + t] = hi;
-        p.out_lo[(size_t)i * plane + (size_t)j * p.Tp + t] = lo;
-      }
-    } else {
-      float* part = p.part + ((size_t)split * p.B + i) * plane;
-#pragma unroll
-      for (int j = 0; j < NP; ++j) part[(size_t)j * p.Tp + t] = y[j];
-      __threadfence();
-    }
+    for (int j = 0; j < 32; ++j) y[j] = 0.f;
   }
-  if (p.splits > 1) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t prev = atomicAdd(&p.counters[tile], 1u);
-      ctl->is_last = (prev == (uint32_t)p.splits - 1u);
-    }
-    __syncthreads();
-    if (ctl->is_last) {
-      __threadfence();
-      float acc[NP];
-      sum_split_partials<NP>(p.part + (size_t)i * plane + t, (size_t)p.B * plane, p.Tp, p.splits, acc);
+  bool mine = true;
+  if (p.splits > 1)
+    mine = cluster_reduce_rows<NP>(reinterpret_cast<float*>(sX), ctl, y, row, split, p.splits);
+  if (mine) {
 #pragma unroll
-      for (int j = 0; j < NP; ++j) {
-        __nv_bfloat16 hi, lo;
-        split_hilo(acc[j], hi, lo);
-        p.out_hi[(size_t)i * plane + (size_t)j * p.Tp + t] = hi;
-        p.out_lo[(size_t)i * plane + (size_t)j * p.Tp + t] = lo;
-      }
-      if (threadIdx.x == 0) p.counters[tile] = 0u;
+    for (int j = 0; j < NP; ++j) {
+      __nv_bfloat16 hi, lo;
+      split_hilo(y[j], hi, lo);
+      p.out_hi[(size_t)i * plane + (size_t)j * p.Tp + t] = hi;
+      p.out_lo[(size_t)i * plane + (size_t)j * p.Tp + t] = lo;
     }
   }
 
@@ -357,73 +366,56 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
     for (int j = 0; j < 32; ++j) z[j] = 0.f;
   }
   bool have_final = true;
-  if (p.splits > 1) {
-    float* part = p.part + ((size_t)split * p.B + i) * plane;
+  if (p.splits > 1)
+    have_final = cluster_reduce_rows<NP>(reinterpret_cast<float*>(sX), ctl, z, row, split, p.splits);
+  if (MODE == kFeatOutF32) {
+    if (have_final && f < p.F) {
 #pragma unroll
-    for (int j = 0; j < NP; ++j) part[(size_t)j * p.Fp + f] = z[j];
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t prev = atomicAdd(&p.counters[tile], 1u);
-      ctl->is_last = (prev == (uint32_t)p.splits - 1u);
+      for (int j = 0; j < NP; ++j) p.out_f32[((size_t)i * NP + j) * p.F + f] = z[j];
     }
-    __syncthreads();
-    have_final = ctl->is_last != 0;
+  } else if (MODE == kFeatOutHiLo) {
+    if (have_final && f < p.F) {
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        __nv_bfloat16 hi, lo;
+        split_hilo(z[j], hi, lo);
+        p.out_hi[((size_t)i * NP + j) * p.F + f] = hi;
+        p.out_lo[((size_t)i * NP + j) * p.F + f] = lo;
+      }
+    }
+  } else {
+    // this CTA's share of the tile's weighted square sum: its finished rows
+    float v = 0.f;
     if (have_final) {
-      __threadfence();
-      float acc[NP];
-      sum_split_partials<NP>(p.part + (size_t)i * plane + f, (size_t)p.B * plane, p.Fp, p.splits, acc);
-#pragma unroll
-      for (int j = 0; j < NP; ++j) z[j] = acc[j];
-      if (threadIdx.x == 0) p.counters[tile] = 0u;
-    }
-  }
-  if (have_final) {
-    if (MODE == kFeatOutF32) {
-      if (f < p.F) {
-#pragma unroll
-        for (int j = 0; j < NP; ++j) p.out_f32[((size_t)i * NP + j) * p.F + f] = z[j];
-      }
-    } else if (MODE == kFeatOutHiLo) {
-      if (f < p.F) {
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-          __nv_bfloat16 hi, lo;
-          split_hilo(z[j], hi, lo);
-          p.out_hi[((size_t)i * NP + j) * p.F + f] = hi;
-          p.out_lo[((size_t)i * NP + j) * p.F + f] = lo;
-        }
-      }
-    } else {
-      float v = 0.f;
 #pragma unroll
       for (int j = 0; j < NP; ++j) v += p.w[j] * z[j] * z[j];
-      v = warp_sum(v);
-      if (lane == 0) ctl->red[warp] = v;
-      __syncthreads();
-      uint32_t* cnt = p.counters + (size_t)p.B * p.ftiles + i;
-      if (threadIdx.x == 0) {
-        const float tile_sum = ((ctl->red[0] + ctl->red[1]) + ctl->red[2]) + ctl->red[3];
-        p.qpart[(size_t)i * p.ftiles + ft] = tile_sum;
-        __threadfence();
-        const uint32_t prev = atomicAdd(cnt, 1u);
-        ctl->is_last = (prev == (uint32_t)p.ftiles - 1u);
+    }
+    v = warp_sum(v);
+    if (lane == 0) ctl->red[warp] = v;
+    __syncthreads();
+    const int nparts = p.ftiles * p.splits;
+    uint32_t* cnt = p.counters + i;
+    if (threadIdx.x == 0) {
+      const float cta_sum = ((ctl->red[0] + ctl->red[1]) + ctl->red[2]) + ctl->red[3];
+      p.qpart[(size_t)i * nparts + (size_t)ft * p.splits + split] = cta_sum;
+      __threadfence();
+      const uint32_t prev = atomicAdd(cnt, 1u);
+      ctl->is_last = (prev == (uint32_t)nparts - 1u);
+    }
+    __syncthreads();
+    if (ctl->is_last && warp == 0) {
+      // the last CTA of the sample adds the per-CTA sums: lane-parallel
+      // loads, then a fixed shuffle tree (deterministic)
+      __threadfence();
+      float q = 0.f;
+      for (int u0 = 0; u0 < nparts; u0 += 32) {
+        const int u = u0 + lane;
+        q += u < nparts ? __ldcg(p.qpart + (size_t)i * nparts + u) : 0.f;
       }
-      __syncthreads();
-      if (ctl->is_last && warp == 0) {
-        // the last tile of the sample adds the per-tile sums: lane-parallel
-        // loads, then a fixed shuffle tree (deterministic)
-        __threadfence();
-        float q = 0.f;
-        for (int u0 = 0; u0 < p.ftiles; u0 += 32) {
-          const int u = u0 + lane;
-          q += u < p.ftiles ? __ldcg(p.qpart + (size_t)i * p.ftiles + u) : 0.f;
-        }
-        q = warp_sum(q);
-        if (lane == 0) {
-          p.sq[i] = q;
-          *cnt = 0u;
-        }
+      q = warp_sum(q);
+      if (lane == 0) {
+        p.sq[i] = q;
+        *cnt = 0u;
       }
     }
   }
@@ -450,17 +442,25 @@ size_t tok_gemm_smem(int NP) {
 }
 size_t feat_gemm_smem(int NP) { return tok_gemm_smem(NP); }
 
+// The K-splits of a tile form one cluster along y.
+static dim3 split_cluster(int splits) {
+  return splits > 1 ? dim3(1, (unsigned)splits, 1) : dim3(0, 0, 0);
+}
+
 cudaError_t launch_tok_gemm(const TokGemmParams& p, cudaStream_t s) {
+  if (p.splits < 1 || p.splits > kMaxSplits) return cudaErrorInvalidValue;
   const dim3 grid(p.B * p.mtiles, p.splits);
   cudaError_t e;
   if (p.NP == 16) {
     const size_t sm = skinny_smem_bytes<16>();
     if ((e = set_smem(tok_gemm_kernel<16>, sm)) != cudaSuccess) return e;
-    return launch_pdl(tok_gemm_kernel<16>, grid, dim3(128), sm, s, 0, p);
+    return launch_pdl_cluster(tok_gemm_kernel<16>, grid, dim3(128), sm, s,
+                              split_cluster(p.splits), p);
   } else if (p.NP == 32) {
     const size_t sm = skinny_smem_bytes<32>();
     if ((e = set_smem(tok_gemm_kernel<32>, sm)) != cudaSuccess) return e;
-    return launch_pdl(tok_gemm_kernel<32>, grid, dim3(128), sm, s, 0, p);
+    return launch_pdl_cluster(tok_gemm_kernel<32>, grid, dim3(128), sm, s,
+                              split_cluster(p.splits), p);
   }
   return cudaErrorInvalidValue;
 }
@@ -471,10 +471,12 @@ static cudaError_t launch_feat_t(const FeatGemmParams& p, cudaStream_t s) {
   const size_t sm = skinny_smem_bytes<NP>();
   cudaError_t e = set_smem(feat_gemm_kernel<NP, MODE>, sm);
   if (e != cudaSuccess) return e;
-  return launch_pdl(feat_gemm_kernel<NP, MODE>, grid, dim3(128), sm, s, 0, p);
+  return launch_pdl_cluster(feat_gemm_kernel<NP, MODE>, grid, dim3(128), sm, s,
+                            split_cluster(p.splits), p);
 }
 
 cudaError_t launch_feat_gemm(const FeatGemmParams& p, int mode, cudaStream_t s) {
+  if (p.splits < 1 || p.splits > kMaxSplits) return cudaErrorInvalidValue;
   if (p.NP == 16) {
     if (mode == kFeatOutF32) return launch_feat_t<16, kFeatOutF32>(p, s);
     if (mode == kFeatOutHiLo) return launch_feat_t<16, kFeatOutHiLo>(p, s);

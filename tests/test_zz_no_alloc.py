@@ -56,7 +56,7 @@ def test_noalloc_matches_workspace_entry_point(L, case):
     elif case == "f32":
         wl = W.get(1)
     else:
-        wl = W.get(4)          # the largest standard Hutch workload (10.5 MiB of scratch)
+        wl = W.get(4)          # the up_proj workload (2.5 MiB of scratch)
     A, G = to_dev(W.make_inputs(wl))
     dt = L.BF16 if wl.dtype == "bf16" else L.F32
     stream = torch.cuda.current_stream().cuda_stream
