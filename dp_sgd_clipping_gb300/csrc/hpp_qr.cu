@@ -47,10 +47,10 @@
 //
 // Latency, not arithmetic, sets this kernel's time: every phase runs once
 // per CTA, so the first fetch of each phase's instructions is on the
-// critical path.  The factorisation is a short rolled loop; the unrolled
-// inverse is one (non-inlined) function that a spare warp runs once on
-// scratch while the first tile's copies are in flight; every function has a
-// single call site.
+// critical path.  The factorisation (lane-parallel, in registers) and the
+// unrolled inverse are non-inlined functions that a spare warp runs once on
+// scratch while the first tile's copies are in flight; every other function
+// has a single call site.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -147,6 +147,9 @@ __device__ __noinline__ void invert_factor(const T (*R)[kMaxR + 1], const T* rdi
   for (int b = 0; b < kMaxR; ++b) M[a][b] = a < r ? (float)q[b] : 0.f;
 }
 
+template <typename T>
+__device__ __noinline__ void cholesky(T (*A)[kMaxR + 1], int n, T* rdiag, T droptol);
+
 // Stages rows [base, base + nvalid) of V (columns < r) and G' (m columns) as
 // xs[col][c], col < r + m; rows nvalid .. (nvalid rounded up to 4) are zero,
 // nothing else past nvalid is read later.  Asynchronous copies throughout
@@ -158,13 +161,6 @@ __device__ __forceinline__ void stage_tile(Smem& sm, const HppQrParams& p, int i
   const bool vec = (p.p % 4) == 0;   // then base, nvalid and every column start are 16-byte aligned
   for (int col = 0; col < r; ++col)
     copy_f32(sm.xs[col], p.V + ((size_t)i * p.ldv + col) * p.p + base, nvalid, vec);
-  if (warm && threadIdx.x >= 32 && threadIdx.x < 64) {
-    // While the copies are in flight, warp 1 runs the (unrolled, once-per-
-    // pass) inverse on the second factor's scratch, which pass 1 overwrites:
-    // that fetches its code into the instruction cache before the first real
-    // use, where the fetch would otherwise sit on the critical path.
-    invert_factor<float>(sm.R2, sm.rd2, r, sm.M2);
-  }
   if (p.gp_bf16) {
     // p % 8 == 0 on this path: base and nvalid are multiples of 8
     for (int l = 0; l < m; ++l) {
@@ -172,15 +168,25 @@ __device__ __forceinline__ void stage_tile(Smem& sm, const HppQrParams& p, int i
       for (int q = threadIdx.x; q < nvalid / 8; q += kThreads)
         cp_async16(&sm.gtmp[l][8 * q], src + 8 * q);
     }
-    cp_async_wait_all();
+  } else {
+    for (int l = 0; l < m; ++l)
+      copy_f32(sm.xs[r + l], static_cast<const float*>(p.Gp) + (size_t)l * p.p + base, nvalid, vec);
+  }
+  if (warm && threadIdx.x >= 32 && threadIdx.x < 64) {
+    // While the copies are in flight, warp 1 runs the (unrolled, once-per-
+    // pass) factorisation and inverse on the second factor's scratch, which
+    // pass 1 overwrites: that fetches their code into the instruction cache
+    // before the first real use, where the fetch would otherwise sit on the
+    // critical path.
+    cholesky<float>(sm.R2, r, sm.rd2, kDropTol);
+    invert_factor<float>(sm.R2, sm.rd2, r, sm.M2);
+  }
+  cp_async_wait_all();
+  if (p.gp_bf16) {
     __syncthreads();
     for (int l = 0; l < m; ++l)
       for (int c = threadIdx.x; c < nvalid; c += kThreads)
         sm.xs[r + l][c] = __bfloat162float(sm.gtmp[l][c]);
-  } else {
-    for (int l = 0; l < m; ++l)
-      copy_f32(sm.xs[r + l], static_cast<const float*>(p.Gp) + (size_t)l * p.p + base, nvalid, vec);
-    cp_async_wait_all();
   }
   const int pad = ((nvalid + 3) & ~3) - nvalid;
   for (int e = threadIdx.x; e < pad * (r + m); e += kThreads) sm.xs[e / pad][nvalid + e % pad] = 0.f;
@@ -270,38 +276,50 @@ __device__ __forceinline__ void cluster_sum(T* pub, T* sum, cg::cluster_group& c
 }
 
 // Warp 0: Cholesky A = R^T R in place on the n x n Gram in A (upper
-// triangle read, R written over it), lane j owning column j.  A pivot below
-// droptol times the largest diagonal entry marks its column as dependent on
-// the earlier ones: its row of R and its entry of rdiag (= 1 / R[k][k]) are
+// triangle read, R written over it), lane j holding column j in registers;
+// the pivot row is passed between lanes by shuffles.  A pivot below droptol
+// times the largest diagonal entry marks its column as dependent on the
+// earlier ones: its row of R and its entry of rdiag (= 1 / R[k][k]) are
 // zero, so the matching column of Q comes out zero and drops out of both the
 // head and the tail projection.  In fp32, 1 / R[k][k] is the hardware
 // reciprocal square root (within 2 ulp); the second CholeskyQR pass absorbs
-// that.  Short rolled loops: this runs once per CTA, where the fetch of
-// unrolled straight-line code would cost more than the arithmetic.
+// that.  The former loop over shared memory took 3.6 us per factorisation
+// (a chain of shared-memory round trips per column update, per timestamps);
+// not inlined, so that one warm-up run fetches its code before the first
+// real use (see stage_tile).
 template <typename T>
-__device__ __forceinline__ void cholesky(T (*A)[kMaxR + 1], int n, T* rdiag, T droptol) {
+__device__ __noinline__ void cholesky(T (*A)[kMaxR + 1], int n, T* rdiag, T droptol) {
   const int j = threadIdx.x & 31;
-  T dmax = 0;
-  for (int a = 0; a < n; ++a) dmax = fmax(dmax, A[a][a]);
+  T col[kMaxR];
+  T diag = T(0);
+#pragma unroll
+  for (int i = 0; i < kMaxR; ++i) {
+    col[i] = (j < n && i <= j) ? A[i][j] : T(0);
+    if (i == j) diag = col[i];
+  }
+  T dmax = diag;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dmax = fmax(dmax, __shfl_xor_sync(0xffffffffu, dmax, off));
   const T tol = droptol * dmax;
-  for (int k = 0; k < n; ++k) {
-    const T piv = A[k][k];
+#pragma unroll
+  for (int k = 0; k < kMaxR; ++k) {
+    if (k >= n) break;
+    const T piv = __shfl_sync(0xffffffffu, col[k], k);
     const bool keep = piv > tol && dmax > T(0);
     const T inv = keep ? rsqrt_t(piv) : T(0);
-    __syncwarp();
-    if (j == k) {
-      A[k][k] = piv * inv;
-      rdiag[k] = inv;
-    } else if (j > k && j < n) {
-      A[k][j] *= inv;
+    col[k] = j == k ? piv * inv : (j > k ? col[k] * inv : col[k]);
+    if (j == k) rdiag[k] = inv;
+    // A[i2][j] -= R[k][i2] R[k][j] for k < i2 <= j
+#pragma unroll
+    for (int i2 = k + 1; i2 < kMaxR; ++i2) {
+      const T rki2 = __shfl_sync(0xffffffffu, col[k], i2);
+      if (j >= i2) col[i2] = fma(-rki2, col[k], col[i2]);
     }
-    __syncwarp();
-    if (j > k && j < n) {
-      const T rkj = A[k][j];
-      for (int i2 = k + 1; i2 <= j; ++i2) A[i2][j] = fma(-A[k][i2], rkj, A[i2][j]);
-    }
-    __syncwarp();
   }
+#pragma unroll
+  for (int i = 0; i < kMaxR; ++i)
+    if (j < n && i <= j) A[i][j] = col[i];
+  __syncwarp();
 }
 
 // In place on the staged rows [0, nrows): x[c, :] <- x[c, :] M over the first

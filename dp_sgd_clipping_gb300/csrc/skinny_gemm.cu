@@ -355,7 +355,6 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   // ---- epilogue: thread = one feature row of the tile
   const int row = warp * 32 + lane;
   const int f = ft * kFeatTileM + row;
-  const size_t plane = (size_t)NP * p.Fp;
   float z[32];
   const bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->done, 0, wc));
   if (ok) {
