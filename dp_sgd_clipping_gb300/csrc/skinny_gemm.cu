@@ -397,15 +397,15 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
     if (threadIdx.x == 0) {
       const float cta_sum = ((ctl->red[0] + ctl->red[1]) + ctl->red[2]) + ctl->red[3];
       p.qpart[(size_t)i * nparts + (size_t)ft * p.splits + split] = cta_sum;
-      __threadfence();
-      const uint32_t prev = atomicAdd(cnt, 1u);
+      // release: this share is visible before the ticket is; acquire: the
+      // last CTA's loads below (after the CTA barrier) see every share
+      const uint32_t prev = atomic_add_acq_rel(cnt, 1u);
       ctl->is_last = (prev == (uint32_t)nparts - 1u);
     }
     __syncthreads();
     if (ctl->is_last && warp == 0) {
       // the last CTA of the sample adds the per-CTA sums: lane-parallel
       // loads, then a fixed shuffle tree (deterministic)
-      __threadfence();
       float q = 0.f;
       for (int u0 = 0; u0 < nparts; u0 += 32) {
         const int u = u0 + lane;
