@@ -499,13 +499,73 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   return v;
 }
 
-// Grid-level reduction of per-unit partials, run by the last CTA of the grid
-// to finish:  sq[i] = scale * sum_{u < nunits, w < nw} part[(u*su + i*si)*nw + w].
-// Every thread of every CTA calls it once at the end of the kernel.  The
-// summation order is fixed (thread partition, 8-wide batches, shuffle tree,
-// warps in order), so results do not depend on CTA timing.  `ticket` must be
-// zero at launch; the last CTA resets it.  With `accumulate`, sq[i] += the
-// result instead.
+// Per-sample sums of partials, by threads tid = 0 .. nthr-1 of one CTA (all
+// of them call it; sync() is a barrier over exactly those threads):
+//   sq[i] = scale * sum_{e < count(i)} *ptr(i, e)   (or sq[i] += ..., accumulate)
+// Up to kSumSamples samples at once and kSumBatch elements per thread, so a
+// thread has kSumSamples * kSumBatch loads in flight: the former sample-by-
+// sample loop, two CTA barriers per sample, took ~7 us at the end of the
+// persistent GEMMs (per timestamps).  The summation order is fixed (thread
+// partition, batch order, shuffle tree, warps in order), so results do not
+// depend on timing.  red_smem holds kSumSamples * (nthr / 32) floats; nthr
+// is a multiple of 32 and tid / 32 a warp index.
+constexpr int kSumSamples = 4;
+constexpr int kSumBatch = 8;
+template <class Count, class Ptr, class Sync>
+__device__ __forceinline__ void sum_per_sample(int B, Count count, Ptr ptr, float scale, float* sq,
+                                               bool accumulate, float* red_smem, int tid, int nthr,
+                                               Sync sync) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nwarps = nthr >> 5;
+  for (int i0 = 0; i0 < B; i0 += kSumSamples) {
+    long long cnt[kSumSamples];
+    long long nmax = 0;
+#pragma unroll
+    for (int j = 0; j < kSumSamples; ++j) {
+      cnt[j] = i0 + j < B ? count(i0 + j) : 0;
+      nmax = cnt[j] > nmax ? cnt[j] : nmax;
+    }
+    float acc[kSumSamples];
+#pragma unroll
+    for (int j = 0; j < kSumSamples; ++j) acc[j] = 0.f;
+    for (long long e0 = tid; e0 < nmax; e0 += (long long)kSumBatch * nthr) {
+      float v[kSumSamples][kSumBatch];
+#pragma unroll
+      for (int j = 0; j < kSumSamples; ++j)
+#pragma unroll
+        for (int q = 0; q < kSumBatch; ++q) {
+          const long long e = e0 + (long long)q * nthr;
+          v[j][q] = e < cnt[j] ? __ldcg(ptr(i0 + j, e)) : 0.f;
+        }
+#pragma unroll
+      for (int j = 0; j < kSumSamples; ++j)
+#pragma unroll
+        for (int q = 0; q < kSumBatch; ++q) acc[j] += v[j][q];
+    }
+#pragma unroll
+    for (int j = 0; j < kSumSamples; ++j) {
+      const float a = warp_sum(acc[j]);
+      if (lane == 0) red_smem[j * nwarps + warp] = a;
+    }
+    sync();
+    if (tid < kSumSamples && i0 + tid < B) {
+      const int i = i0 + tid;
+      float s = 0.f;
+      for (int w = 0; w < nwarps; ++w) s += red_smem[tid * nwarps + w];
+      sq[i] = accumulate ? sq[i] + scale * s : scale * s;
+    }
+    sync();
+  }
+}
+
+// The last CTA to finish a kernel (integer ticket) computes
+//   sq[i] = scale * sum_{u < nunits, w < nw} part[(u*su + i*si)*nw + w].
+// Every thread of every CTA calls it once at the end of the kernel, one
+// sample after the other with few registers (kernels whose producer warps
+// have given theirs away call it).  The summation order is fixed (thread
+// partition, 8-wide batches, shuffle tree, warps in order), so results do not
+// depend on CTA timing.  `ticket` must be zero at launch; the last CTA resets
+// it.  With `accumulate`, sq[i] += the result instead.
 __device__ __forceinline__ void reduce_partials_last_cta(const float* part, int B, int nunits,
                                                          long long su, long long si, int nw,
                                                          float scale, float* sq,

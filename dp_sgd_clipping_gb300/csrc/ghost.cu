@@ -52,7 +52,7 @@ struct Ctl {
   int consumed;
   int mma_units;
   int is_last;
-  float red[kThreads / 32];
+  float red[kSumSamples * (kThreads / 32)];
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * 2 * kTileBytes + sizeof(Ctl);
@@ -250,39 +250,27 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
   // item has 2 * kEpiWarps partials (CTA rank, epilogue warp)
   {
     constexpr int kPer = 2 * kEpiWarps;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) ctl->is_last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1u) ? 1 : 0;
+    if (threadIdx.x == 0) {
+      __threadfence();   // the CTA's partials, written before the barrier
+      ctl->is_last = atomic_add_acq_rel(p.ticket, 1u) == gridDim.x - 1u ? 1 : 0;
+    }
     __syncthreads();
     if (ctl->is_last) {
-      __threadfence();
       const int np = p.npairs, nf = p.nfull, ts = p.tail_split;
-      for (int i = 0; i < p.B; ++i) {
-        const int f0 = min(i * np, nf), f1 = min((i + 1) * np, nf);
-        const int s0 = nf + (max(i * np, nf) - nf) * ts, s1 = nf + (max((i + 1) * np, nf) - nf) * ts;
-        const long long n1 = (long long)(f1 - f0) * kPer, n2 = (long long)(s1 - s0) * kPer;
-        float acc = 0.f;
-        for (long long e0 = threadIdx.x; e0 < n1 + n2; e0 += 8ll * blockDim.x) {
-          float v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const long long e = e0 + (long long)q * blockDim.x;
-            v[q] = e < n1 ? __ldcg(p.part + (size_t)f0 * kPer + e)
-                          : (e < n1 + n2 ? __ldcg(p.part + (size_t)s0 * kPer + (e - n1)) : 0.f);
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc += v[q];
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) ctl->red[warp] = acc;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          float sum = 0.f;
-          for (int w = 0; w < kThreads / 32; ++w) sum += ctl->red[w];
-          p.sq[i] = sum;
-        }
-        __syncthreads();
-      }
+      auto f0 = [&](int i) { return min(i * np, nf); };
+      auto s0 = [&](int i) { return nf + (max(i * np, nf) - nf) * ts; };
+      auto n1 = [&](int i) { return (long long)(min((i + 1) * np, nf) - f0(i)) * kPer; };
+      auto n2 = [&](int i) {
+        return (long long)(nf + (max((i + 1) * np, nf) - nf) * ts - s0(i)) * kPer;
+      };
+      sum_per_sample(
+          p.B, [&](int i) { return n1(i) + n2(i); },
+          [&](int i, long long e) {
+            const long long a = n1(i);
+            return e < a ? p.part + (size_t)f0(i) * kPer + e : p.part + (size_t)s0(i) * kPer + (e - a);
+          },
+          1.f, p.sq, false, ctl->red, (int)threadIdx.x, kThreads, [] { __syncthreads(); });
       if (threadIdx.x == 0) *p.ticket = 0u;
     }
   }
