@@ -53,13 +53,18 @@ WORKLOAD_ROWS = {1: ("exact_direct", "hutch", "hutchpp", "clipped_noisy_grad"),
                  5: ("hutch", "hutchpp", "exact_direct", "clipped_noisy_grad")}
 
 
+L2_BYTES = 129e6
+
+
 def time_workload(api, L, W, wid, dev, reps, peaks):
-    """Latency of each row a standard workload names, one call at a time with
-    a CUDA event pair around it and L2 flushed before it (a 256 MB write
-    outside the events): the exact workload's 13 MB of inputs would otherwise
-    stay in L2.  Median of `reps` calls after three warm-up calls.  Returns
-    {workload name: {"rows": ..., "layer_totals": ...}}; the fp32 workload is
-    latency-bound and gets no roofline fraction."""
+    """Latency of each row a standard workload names.  Workloads whose inputs
+    are larger than L2 are timed as the step's rows are: `reps` calls of the
+    row back to back between one event pair.  The others (whose inputs would
+    stay in L2) one call at a time with a CUDA event pair around it and L2
+    flushed before it (a 256 MB write outside the events), median of `reps`.
+    Three warm-up calls first.  Returns {workload name: {"rows": ...,
+    "layer_totals": ...}}; the fp32 workload is latency-bound and gets no
+    roofline fraction."""
     import torch
     wl = W.get(wid)
     inp = W.make_inputs(wl)
@@ -102,19 +107,35 @@ def time_workload(api, L, W, wid, dev, reps, peaks):
             api.clipped_noisy_grad(A, G, qsrc, wl.C, wl.sigma, wl.seed, step, grad=grad,
                                    scales=scales, clipped=clipped, ws=ws[r])
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     times = {r: [] for r in rows}
-    for step in range(3 + reps):
+    large = A.numel() * A.element_size() + G.numel() * G.element_size() > L2_BYTES
+    if large:
+        timing = f"{reps} calls back to back per row (inputs larger than L2)"
         for r in rows:
-            flush.fill_(step & 0xFF)
+            for step in range(3):
+                call(r, step)
+            torch.cuda.synchronize(dev)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            call(r, step)
+            for step in range(reps):
+                call(r, 3 + step)
             e1.record(stream)
             torch.cuda.synchronize(dev)
-            if step >= 3:
-                times[r].append(e0.elapsed_time(e1))
+            times[r].append(e0.elapsed_time(e1) / reps)
+    else:
+        timing = f"median of {reps} calls, L2 flushed before each"
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for step in range(3 + reps):
+            for r in rows:
+                flush.fill_(step & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call(r, step)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                if step >= 3:
+                    times[r].append(e0.elapsed_time(e1))
     for r in rows:
         if r in ws and api.workspace_status(ws[r]) != 0:
             raise SystemExit(f"{wl.name} {r}: device reported a status")
@@ -132,7 +153,7 @@ def time_workload(api, L, W, wid, dev, reps, peaks):
             ms = out[r]["ms"] + out["clipped_noisy_grad"]["ms"]
             totals[r + "+grad"] = {"ms": round(ms, 4), "tokens_per_s": B * T / (ms * 1e-3)}
     return {wl.name: {"B": B, "T": T, "d": d, "p": p, "k": k, "C": wl.C, "sigma": wl.sigma,
-                      "timing": f"median of {reps} calls, L2 flushed before each",
+                      "timing": timing,
                       "rows": out, "layer_totals": totals}}
 
 
@@ -483,24 +504,41 @@ def main():
     wall1 = time.time()
     clk = clocks.stop(wall0, wall1) if rank == 0 else None
     elapsed_ms = start.elapsed_time(end)
-    # Per-row durations come from a second pass of the same steps with an
-    # event pair around every row.  An event between two calls keeps the
-    # second call's first kernel from launching early (programmatic launch),
-    # so these rows add up to a little more than the step timed above.
+    # Per-row durations, two ways.  row_ms: each row alone, K calls back to
+    # back between one event pair (the steady state of a loop over layers:
+    # each call's launch and prologue overlap the previous call's tail; the
+    # inputs are larger than L2).  in_step_ms: a second pass of the step
+    # with an event pair around every row; an event between two calls keeps
+    # the second call's first kernel from launching early, so these rows add
+    # up to a little more than the step timed above.
     for s in range(args.steps):
         ev[s][0].record(stream)
         for j, r in enumerate(rows):
             row_fn(r, args.warmup + s)()
             ev[s][j + 1].record(stream)
     barrier()
+    in_step_ms = {r: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1])
+                                     for s in range(args.steps))
+                  for j, r in enumerate(rows)}
+    row_ms = {}
+    for r in rows:
+        for s_ in range(3):
+            row_fn(r, s_)()
+        barrier()
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for s_ in range(args.steps):
+            row_fn(r, args.warmup + s_)()
+        r1.record(stream)
+        barrier()
+        row_ms[r] = r0.elapsed_time(r1) / args.steps
     for name in rows:
         if name not in ws:
             continue
         st = api.workspace_status(ws[name])
         if st != 0:
             raise SystemExit(f"{name}: device reported status {st}")
-    row_ms = {r: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps))
-              for j, r in enumerate(rows)}
     elapsed_ms = max_over_ranks(elapsed_ms, pg, dev)
 
     # ---------------------------------------------------------------- end to end, host buffers
@@ -622,6 +660,7 @@ def main():
     for r in rows:
         breakdown[r] = row_entry(work[r], row_ms[r], B * T, peaks)
         breakdown[r]["algorithmic"] = work[r][0]
+        breakdown[r]["in_step_ms"] = round(in_step_ms[r], 4)
     extra = {}
     for r, ms in extra_ms.items():
         extra[r] = row_entry(work[r], ms, B * T, peaks)
