@@ -292,6 +292,16 @@ def test_hutch_probe_widths(api, k):
     _run_all(api, wl, paths=("hutch",))
 
 
+@pytest.mark.parametrize("B,T,d,p", [(5, 2048, 2048, 1024), (3, 2304, 2304, 1280),
+                                     (2, 3072, 3072, 1536), (1, 5120, 5120, 1792)])
+def test_skinny_split_counts(api, B, T, d, p):
+    # the K-split of the skinny GEMMs is a cluster of 3, 5, 6 or 7 CTAs here
+    # (and 7 or 8 on Hutch++'s pass over G), so rows are finished by CTAs
+    # that own unequal row counts; the standard workloads give 1, 2, 4 and 8
+    wl = W.Workload(190 + B, f"splits_{B}_{T}_{d}_{p}", B, T, d, p, "bf16", 1e-2, 1.0, 1.0, 32, ())
+    _run_all(api, wl, paths=("hutch", "hutchpp"))
+
+
 @pytest.mark.parametrize("k", [3, 4, 5, 46, 47, 48])
 def test_hutchpp_budgets(api, k):
     # r = k // 3 head columns, m = k - 2r tail probes; k = 48 fills all 32 columns
