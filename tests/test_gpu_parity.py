@@ -206,6 +206,39 @@ def test_results_are_deterministic(api):
     assert torch.equal(g1, g2)
 
 
+@pytest.mark.parametrize("shape", [(3, 1000, 512, 1536), (4, 4096, 2048, 8192)])
+def test_back_to_back_calls_share_a_workspace(api, shape):
+    # Each kernel of an estimator call overlaps its prologue with the end of
+    # the previous kernel, and the next call's first kernel clears the
+    # workspace's tickets while nothing else is in flight.  Calls queued back
+    # to back on one workspace, with other seeds and inputs each time, must
+    # give what the same calls give alone on a workspace filled with NaN
+    # bytes: a read of an intermediate before it is stored, or of a ticket
+    # before it is cleared, sees another call's values or the NaN fill.
+    B, T, d, p = shape
+    wl = W.Workload(123, "b2b", B, T, d, p, "bf16", 1e-2, 1.0, 1.0, 32, ())
+    g = torch.Generator(device="cuda").manual_seed(11)
+    pairs = [(torch.randn(B, T, d, device="cuda", generator=g).to(torch.bfloat16),
+              (torch.randn(B, T, p, device="cuda", generator=g) * 1e-2).to(torch.bfloat16))
+             for _ in range(2)]
+    from dp_sgd_clipping_gb300 import _lib as L
+    for op, fn in ((L.OP_NORMS_HUTCH, api.norms_hutch), (L.OP_NORMS_HUTCHPP, api.norms_hutchpp)):
+        nb = api.workspace_bytes(op, B, T, d, p, L.BF16, wl.k)
+        calls = [(pairs[c % 2], seed) for c, seed in enumerate(range(1, 7))]
+        alone = []
+        for (A, G), seed in calls:
+            ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
+            alone.append(fn(A, G, wl.k, seed, 0, ws=ws))
+            torch.cuda.synchronize()
+        ws = torch.full((nb,), 0xFF, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        queued = [fn(A, G, wl.k, seed, 0, ws=ws) for (A, G), seed in calls]
+        torch.cuda.synchronize()
+        for a, q in zip(alone, queued):
+            assert torch.isfinite(a).all()
+            assert torch.equal(a, q), (op, host(a), host(q))
+
+
 # ----------------------------------------------------------------------------- standard workloads
 
 def test_exact_workload_ghost_vs_direct(api):
