@@ -95,6 +95,8 @@ SIGNATURES = {
     "dpclip_selftest_wait_timeout": (_i, [_vp, _sz, _i, _vp]),
     "dpclip_grad_tail_schedule": (_i, [_i, _i, _i, _i, _c.POINTER(_i), _c.POINTER(_i), _vp, _i,
                                        _c.POINTER(_i), _vp, _i, _c.POINTER(_i)]),
+    "dpclip_ghost_schedule": (_i, [_i, _i, _i, _i, _i, _c.POINTER(_i), _c.POINTER(_i),
+                                   _c.POINTER(_i), _c.POINTER(_i)]),
     "dpclip_status_string": (_c.c_char_p, [_i]),
     "dpclip_version": (_c.c_char_p, []),
 }
@@ -146,6 +148,16 @@ def grad_tail_schedule(pairs: int, ntiles: int, B: int, tblocks: int):
         if ns.value <= seg_cap and nc.value <= contrib_cap:
             return waves.value, ntail.value, segs[:ns.value], contrib[:nc.value]
         seg_cap, contrib_cap = ns.value, nc.value
+
+
+def ghost_schedule(pairs: int, B: int, T: int, d: int, p: int):
+    """The ghost form's work split (host only): (nfull, tail_split,
+    pb_per_split, tail_shared)."""
+    out = [_c.c_int() for _ in range(4)]
+    st = lib.dpclip_ghost_schedule(pairs, B, T, d, p, *[_c.byref(o) for o in out])
+    if st != 0:
+        raise DpclipError("dpclip_ghost_schedule", st, status_string(st))
+    return tuple(o.value for o in out)
 
 
 def status_string(status: int) -> str:

@@ -194,7 +194,11 @@ int ghost_npairs(int T) {
 Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
   Plan pl;
   Carve c;
-  pl.ctrl_bytes = kAlign;
+  const bool ghost = method != DPCLIP_EXACT_DIRECT;
+  const size_t xunits = std::min<size_t>(kGhostSharedUnits, (size_t)ghost_npairs(T) * B);
+  // error word, grid ticket; ghost: the ready counters of a shared X (one
+  // per unit, CTA rank and epilogue warp)
+  pl.ctrl_bytes = ghost ? align_up(4 * (2 + xunits * 2 * kEpiWarps), kAlign) : kAlign;
   pl.ctrl = c.take(pl.ctrl_bytes);
   // direct: one partial per CTA tile, sample and epilogue warp.  ghost: whole
   // units plus at most 8 sub-units for each unit of the last round (fewer
@@ -204,6 +208,7 @@ Plan plan_exact_bf16(int B, int T, int d, int p, int method) {
           ? (size_t)dp_ntiles(d, p) * B * kEpiWarps
           : ((size_t)ghost_npairs(T) * B + 8 * (size_t)(kMaxPersistentGrid / 2)) * 2 * kEpiWarps;
   pl.off[0] = c.take(parts * 4);
+  if (ghost) pl.off[1] = c.take(xunits * 2 * 128 * 256 * 4);   // shared X of the last round
   pl.total = c.total();
   return pl;
 }
@@ -522,6 +527,8 @@ int dpclip_norms_exact(const void* A, const void* G, int B, int T, int d, int p,
       gh.dblocks = cdiv(d, kBlockK);
       gh.pblocks = cdiv(p, kBlockK);
       gh.part = at<float>(ws, pl.off[0]);
+      gh.xbuf = at<float>(ws, pl.off[1]);
+      gh.xready = at<uint32_t>(ws, pl.ctrl + 8);
       gh.sq = sqnorms;
       gh.ticket = at<uint32_t>(ws, pl.ctrl + 4);
       gh.err = at<uint32_t>(ws, pl.ctrl);
@@ -1119,6 +1126,25 @@ int dpclip_grad_tail_schedule(int pairs, int ntiles, int B, int tblocks, int* wa
   plan_grad_schedule(ntiles, B, tblocks, pairs, *waves, *ntail, cover);
   grad_tail_dump(pairs, *ntail, (long long)B * tblocks, cover, segs, seg_cap, nsegs, contrib,
                  contrib_cap, ncontrib);
+  return DPCLIP_OK;
+}
+
+int dpclip_ghost_schedule(int pairs, int B, int T, int d, int p, int* nfull, int* tail_split,
+                          int* pb_per_split, int* tail_shared) {
+  if (pairs < 1 || pairs > kMaxPersistentGrid / 2 || B < 1 || T < 1 || d < 1 || p < 1 || !nfull ||
+      !tail_split || !pb_per_split || !tail_shared)
+    return DPCLIP_ERR_INVALID_ARG;
+  GhostParams gh;
+  std::memset(&gh, 0, sizeof(gh));
+  gh.B = B;
+  gh.npairs = ghost_npairs(T);
+  gh.dblocks = cdiv(d, kBlockK);
+  gh.pblocks = cdiv(p, kBlockK);
+  plan_ghost_schedule(gh, std::min(pairs, B * gh.npairs));
+  *nfull = gh.nfull;
+  *tail_split = gh.tail_split;
+  *pb_per_split = gh.pb_per_split;
+  *tail_shared = gh.tail_shared;
   return DPCLIP_OK;
 }
 

@@ -20,9 +20,16 @@
 // Units are dealt round-robin (unit u to pair u mod G).  All units cost the
 // same, so when their count is not a multiple of the grid the last round is
 // only partly busy; the units of that last round are therefore cut along p
-// into `tail_split` sub-units that each recompute X over all of d but only
-// a slice of Y's K range.  Because sum(X o Y) is linear in Y, the sub-units'
-// partial sums simply add up: no combine step is needed.
+// into `tail_split` sub-units, each with a slice of Y's K range.  Because
+// sum(X o Y) is linear in Y, the sub-units' partial sums simply add up.  X
+// (K = d) is either recomputed by every sub-unit or, when each pair has at
+// most one sub-unit of the last round (`tail_shared`), formed once by an
+// extra X sub-unit that stores it (fp32, 256 KB per unit) for the Y
+// sub-units: each epilogue warp of the X sub-unit releases a counter once
+// its rows are stored, and the matching warp of every Y sub-unit (same CTA
+// rank, same rows and columns) waits for that counter, bounded, before it
+// reads them.  All pairs are resident (the grid is the resident count), so
+// the X sub-unit always runs; its own pair never waits on the others.
 //
 // Pipeline: the leader's (rank 0) `full` barrier counts both CTAs' loads;
 // the MMA's completion is multicast to both CTAs' `empty` and `tfull`; each
@@ -73,27 +80,60 @@ __device__ __forceinline__ void pair_of(int pr, int& a, int& bb) {
   bb = col;
 }
 
-// Work item g -> (sample, unit index within the sample, p-block range).
+// Work item g -> (sample, unit index within the sample, K ranges: the first
+// kx K-blocks over d, then p-blocks [pb0, pb1)) and its role.
+enum { kWhole = 0, kXOnly = 1, kYOnly = 2 };
 struct GhostItem {
-  int i, pr, pb0, pb1;
+  int i, pr, pb0, pb1, kx, role, tu;
 };
 __device__ __forceinline__ bool ghost_item(const GhostParams& p, int g, GhostItem& it) {
   int u;
+  it.kx = p.dblocks;
+  it.role = kWhole;
+  it.tu = 0;
   if (g < p.nfull) {
     u = g;
     it.pb0 = 0;
     it.pb1 = p.pblocks;
   } else {
+    const int per = p.tail_split + p.tail_shared;
     const int t = g - p.nfull;
-    if (t >= (p.B * p.npairs - p.nfull) * p.tail_split) return false;
-    u = p.nfull + t / p.tail_split;
-    const int c = t % p.tail_split;
-    it.pb0 = c * p.pb_per_split;
-    it.pb1 = min(it.pb0 + p.pb_per_split, p.pblocks);
+    if (t >= (p.B * p.npairs - p.nfull) * per) return false;
+    it.tu = t / per;
+    u = p.nfull + it.tu;
+    int c = t % per;
+    if (p.tail_shared) {
+      if (c == 0) {
+        it.role = kXOnly;
+      } else {
+        it.role = kYOnly;
+        it.kx = 0;
+      }
+      c -= 1;
+    }
+    it.pb0 = c < 0 ? 0 : c * p.pb_per_split;
+    it.pb1 = c < 0 ? 0 : min(it.pb0 + p.pb_per_split, p.pblocks);
   }
   it.i = u / p.npairs;
   it.pr = u % p.npairs;
   return true;
+}
+
+// Spins (bounded; also ends once the call has recorded an error) until the
+// counter is nonzero; acquire ordering for the loads that follow it.
+__device__ __forceinline__ void wait_ready(const uint32_t* c, uint32_t* err) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v != 0u) return;
+    if (*reinterpret_cast<volatile uint32_t*>(err) != 0u) return;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(err, DPCLIP_ERR_TIMEOUT);
+      return;
+    }
+    __nanosleep(64);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constant__ GhostParams p) {
@@ -150,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
         int a, b;
         pair_of(itm.pr, a, b);
         const int ta = (2 * a + rank) * kGhostTile, tb = (2 * b + rank) * kGhostTile;
-        const int kblocks = p.dblocks + (itm.pb1 - itm.pb0);
+        const int kblocks = itm.kx + (itm.pb1 - itm.pb0);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) {
@@ -159,9 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
           }
           if (rank == 0) mbar_arrive_expect_tx(&ctl->full[s], kStageTx);
           const uint32_t bar = full0 + (uint32_t)s * (uint32_t)sizeof(uint64_t);
-          const bool on_a = kb < p.dblocks;
+          const bool on_a = kb < itm.kx;
           const CUtensorMap* map = on_a ? &p.map_a : &p.map_g;
-          const int k0 = (on_a ? kb : itm.pb0 + kb - p.dblocks) * kBlockK;
+          const int k0 = (on_a ? kb : itm.pb0 + kb - itm.kx) * kBlockK;
           tma_load_3d_pair(sP + s * kTileBytes, map, bar, k0, ta, i);
           tma_load_3d_pair(sQ + s * kTileBytes, map, bar, k0, tb, i);
           ctl->issued = it + 1;
@@ -185,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
           break;
         }
         tc_fence_after();
-        const int kblocks = p.dblocks + (itm.pb1 - itm.pb0);
+        const int kblocks = itm.kx + (itm.pb1 - itm.pb0);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&ctl->full[s], (it / kStages) & 1, wc)) {
@@ -194,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
           }
           ctl->consumed = it + 1;
           tc_fence_after();
-          const bool on_a = kb < p.dblocks;
-          const int kl = on_a ? kb : kb - p.dblocks;
+          const bool on_a = kb < itm.kx;
+          const int kl = on_a ? kb : kb - itm.kx;
           const uint32_t dt = tmem + (on_a ? 0u : 256u);
           const uint32_t a0 = smem_u32(sP + s * kTileBytes);
           const uint32_t b0 = smem_u32(sQ + s * kTileBytes);
@@ -229,17 +269,55 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       const int b = 2 * bb + half;                   // 128-token block of these columns
       const float w = a < b ? 2.f : (a == b ? 1.f : 0.f);
       const uint32_t base = tmem + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
+      // this thread's row of X (shared tail): [unit][rank][row][256 columns]
+      const size_t xrow = (((size_t)itm.tu * 2 + rank) * 128 + quad * 32 + lane) * 256 + half * 128;
+      uint32_t* ready = p.xready + ((size_t)itm.tu * 2 + rank) * kEpiWarps + ew;
       float s = 0.f;
+      if (itm.role == kXOnly) {
+        // store X for the Y sub-units of this unit, then release it
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float x[32], y[32];
-        tmem_ld32(base + c4 * 32, x);
-        tmem_ld32(base + 256 + c4 * 32, y);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          float x[64];
+          tmem_ld64(base + c2 * 64, x);
+          float4* dst = reinterpret_cast<float4*>(p.xbuf + xrow + c2 * 64);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) s = fmaf(x[j], y[j], s);
+          for (int j = 0; j < 16; ++j)
+            dst[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        }
+        tc_fence_before();
+        mbar_arrive_remote(release);
+        __syncwarp();
+        if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ready) : "memory");
+      } else {
+        if (itm.role == kYOnly) {
+          if (lane == 0) wait_ready(ready, p.err);
+          __syncwarp();
+        }
+        // the accumulators are released only after these loads: one wait
+        // per 64 columns of X and Y keeps the gap before the next unit short
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          float x[64], y[64];
+          if (itm.role == kYOnly) {
+            tmem_ld64(base + 256 + c2 * 64, y);
+            const float4* src = reinterpret_cast<const float4*>(p.xbuf + xrow + c2 * 64);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float4 v = __ldcg(src + j);
+              x[4 * j] = v.x;
+              x[4 * j + 1] = v.y;
+              x[4 * j + 2] = v.z;
+              x[4 * j + 3] = v.w;
+            }
+          } else {
+            tmem_ld64x2(base + c2 * 64, x, base + 256 + c2 * 64, y);
+          }
+#pragma unroll
+          for (int j = 0; j < 64; ++j) s = fmaf(x[j], y[j], s);
+        }
+        tc_fence_before();
+        mbar_arrive_remote(release);
       }
-      tc_fence_before();
-      mbar_arrive_remote(release);
       s = warp_sum(s);
       if (lane == 0) p.part[((size_t)g * 2 + rank) * kEpiWarps + ew] = w * s;
     }
@@ -257,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
     }
     __syncthreads();
     if (ctl->is_last) {
-      const int np = p.npairs, nf = p.nfull, ts = p.tail_split;
+      const int np = p.npairs, nf = p.nfull, ts = p.tail_split + p.tail_shared;
       auto f0 = [&](int i) { return min(i * np, nf); };
       auto s0 = [&](int i) { return nf + (max(i * np, nf) - nf) * ts; };
       auto n1 = [&](int i) { return (long long)(min((i + 1) * np, nf) - f0(i)) * kPer; };
@@ -316,7 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
 
 size_t ghost_smem() { return kSmemBytes; }
 
-// Tail split for `grid` pairs.
+// Tail split for `grid` pairs: the cut of the last round's units that
+// minimises that round's cost in K-blocks.  A unit is dblocks + pblocks.
+// Recomputing X, a sub-unit costs dblocks + its p-slice.  Sharing X (only
+// when every sub-unit of the round fits on its own pair, so that no pair
+// both waits for an X and owes one) costs max(dblocks, p-slice) plus the
+// store of X, the wait and its reload: about 3.3 us measured on the up_proj
+// shape (a 12-unit tail: 385 -> 381.6 us where 22 K-blocks, 6.8 us, were
+// saved), i.e. about 10 K-blocks of 0.31 us.
+constexpr int kSharedXCost = 10;
+
 void plan_ghost_schedule(GhostParams& p, int grid) {
   const int units = p.B * p.npairs;
   const int rounds = units / grid;
@@ -324,8 +411,8 @@ void plan_ghost_schedule(GhostParams& p, int grid) {
   const int tail = units - p.nfull;
   p.tail_split = 1;
   p.pb_per_split = p.pblocks;
+  p.tail_shared = 0;
   if (tail == 0) return;
-  // cost of the last round in K-blocks; a unit is dblocks + pblocks
   double best = (double)p.dblocks + p.pblocks;
   for (int want = 2; want <= 8; ++want) {
     const int pbc = (p.pblocks + want - 1) / want;
@@ -336,6 +423,18 @@ void plan_ghost_schedule(GhostParams& p, int grid) {
       best = cost;
       p.tail_split = s;
       p.pb_per_split = pbc;
+    }
+  }
+  for (int want = 1; want <= 8; ++want) {
+    const int pbc = (p.pblocks + want - 1) / want;
+    const int s = (p.pblocks + pbc - 1) / pbc;
+    if (tail * (s + 1) > grid) break;
+    const double cost = (double)std::max(p.dblocks, pbc) + kSharedXCost;
+    if (cost < best - 1e-9) {
+      best = cost;
+      p.tail_split = s;
+      p.pb_per_split = pbc;
+      p.tail_shared = 1;
     }
   }
 }

@@ -154,7 +154,13 @@ struct GhostParams {
   int npairs, dblocks, pblocks;   // npairs: units (a', b') per sample
   int nfull;             // units dealt whole (a multiple of the grid of pairs)
   int tail_split, pb_per_split;   // the remaining units cut along p
-  float* part;           // [nfull + (B*npairs - nfull) * tail_split][2][8]
+  // tail_shared = 1: each remaining unit is one X sub-unit (X over d, stored
+  // to xbuf) and tail_split Y sub-units that read it back; else every
+  // sub-unit recomputes X
+  int tail_shared;
+  float* xbuf;           // [remaining units][2][128][256] fp32 (tail_shared)
+  uint32_t* xready;      // [remaining units][2][8], zero at launch (tail_shared)
+  float* part;           // [nfull + (B*npairs - nfull) * (tail_split + tail_shared)][2][8]
   float* sq;             // per-sample result [B]
   uint32_t* ticket;      // zeroed grid ticket
   uint32_t* err;
@@ -297,7 +303,11 @@ void grad_tail_dump(int G, int ntail, long long L, uint32_t cover, int64_t* segs
                     int* nsegs, int64_t* contrib, int contrib_cap, int* ncontrib);
 constexpr int kMaxPersistentGrid = 160;   // CTAs of the persistent kernels (<= SMs)
 size_t ghost_smem();
-// Tail split of the ghost units for a grid: sets nfull, tail_split, pb_per_split.
+// Units of the ghost kernel's last round that may share a stored X: at most
+// one sub-unit per pair, so at most half the largest grid of pairs.
+constexpr int kGhostSharedUnits = kMaxPersistentGrid / 4;
+// Tail split of the ghost units for a grid: sets nfull, tail_split,
+// pb_per_split and tail_shared.
 void plan_ghost_schedule(GhostParams& p, int grid);
 
 }  // namespace dpclip

@@ -364,6 +364,19 @@ int dpclip_grad_tail_schedule(int pairs, int ntiles, int B, int tblocks, int* wa
                               int64_t* segs, int seg_cap, int* nsegs, int64_t* contrib,
                               int contrib_cap, int* ncontrib);
 
+/* Host-only diagnostic (no device work): how dpclip_norms_exact's ghost form
+ * deals its work units (sample, 256-token tile pair a' <= b') over `pairs`
+ * CTA pairs (grids of fewer pairs than units; the call uses min(resident
+ * pairs, units)).  *nfull units are dealt whole, round-robin; each of the
+ * B * units - *nfull others is cut along p into *tail_split slices of
+ * *pb_per_split 64-column blocks (the last one shorter), and, when
+ * *tail_shared is 1, one more sub-unit that forms the unit's A Gram block
+ * once for the slices (else every slice recomputes it).
+ * DPCLIP_ERR_INVALID_ARG for pairs outside 1..80, non-positive sizes or
+ * null outputs. */
+int dpclip_ghost_schedule(int pairs, int B, int T, int d, int p, int* nfull, int* tail_split,
+                          int* pb_per_split, int* tail_shared);
+
 /* Human-readable name of a status code. */
 const char* dpclip_status_string(int status);
 

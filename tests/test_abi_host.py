@@ -261,3 +261,83 @@ def test_grad_tail_schedule_rejects(L):
         st = L.lib.dpclip_grad_tail_schedule(*args, C.byref(w), C.byref(n), None, 0, C.byref(ns),
                                              None, 0, C.byref(nc))
         assert st == L.ERR_INVALID_ARG
+
+
+def _ghost_items(nfull, tail_units, split, pbc, shared, pblocks, dblocks):
+    """The sub-units of the ghost kernel's last round, in item order: (tail
+    unit, first K-block over d count, p-block range), as the kernel deals
+    them (one X sub-unit first when shared)."""
+    items = []
+    per = split + shared
+    for t in range(tail_units * per):
+        tu, c = divmod(t, per)
+        kx = dblocks
+        if shared:
+            if c == 0:
+                items.append((tu, dblocks, 0, 0))
+                continue
+            kx, c = 0, c - 1
+        pb0 = c * pbc
+        items.append((tu, kx, pb0, min(pb0 + pbc, pblocks)))
+    return items
+
+
+def test_ghost_schedule_covers_once(L):
+    """Every unit of the ghost form's last round has each of its p-blocks in
+    exactly one sub-unit and its A Gram block formed by exactly one sub-unit
+    per p-slice (recomputed) or once for all (shared); with a shared Gram
+    block each pair holds at most one sub-unit of that round, so no pair
+    both waits for a Gram block and owes one; and the chosen cut costs no
+    more K-blocks than dealing the units whole."""
+    for pairs in (1, 2, 7, 40, 76, 80):
+        for B, T in ((1, 300), (2, 2048), (4, 4096), (3, 4352), (1, 16384)):
+            for d, p in ((64, 64), (256, 512), (1024, 2048), (2048, 8192), (2048, 2048), (4096, 512)):
+                units = B * ((T + 255) // 256) * ((T + 255) // 256 + 1) // 2
+                grid = min(pairs, units)
+                nfull, split, pbc, shared = L.ghost_schedule(pairs, B, T, d, p)
+                db, pb = (d + 63) // 64, (p + 63) // 64
+                assert nfull == units // grid * grid
+                tail = units - nfull
+                assert split >= 1 and (split - 1) * pbc < pb <= split * pbc
+                assert shared in (0, 1)
+                if tail == 0:
+                    assert (split, pbc, shared) == (1, pb, 0)
+                    continue
+                items = _ghost_items(nfull, tail, split, pbc, shared, pb, db)
+                for tu in range(tail):
+                    mine = [it for it in items if it[0] == tu]
+                    cover = [0] * pb
+                    for _, kx, b0, b1 in mine:
+                        for k in range(b0, b1):
+                            cover[k] += 1
+                    assert cover == [1] * pb
+                    gram = [kx for _, kx, _, _ in mine]
+                    if shared:
+                        assert gram.count(db) == 1 and gram.count(0) == split
+                    else:
+                        assert gram == [db] * split
+                if shared:
+                    assert len(items) <= grid
+                    cost = max(db, pbc) + 10
+                else:
+                    cost = -(-len(items) // grid) * (db + pbc)
+                assert cost <= db + pb, (pairs, B, T, d, p)
+
+
+def test_ghost_schedule_up_proj(L):
+    # 544 units on 76 pairs: 7 whole rounds, 12 units left, each one Gram
+    # sub-unit over d (32 K-blocks) and four 32-block slices of p, all 60 of
+    # them at once on their own pairs; on q_proj (p = 2048) six 6-block
+    # slices that each recompute the Gram block cost less than sharing it
+    assert L.ghost_schedule(76, 4, 4096, 2048, 8192) == (532, 4, 32, 1)
+    assert L.ghost_schedule(76, 4, 4096, 2048, 2048) == (532, 6, 6, 0)
+
+
+def test_ghost_schedule_rejects(L):
+    import ctypes as C
+    o = [C.c_int() for _ in range(4)]
+    for args in ((0, 1, 64, 64, 64), (81, 1, 64, 64, 64), (4, 0, 64, 64, 64), (4, 1, 0, 64, 64),
+                 (4, 1, 64, 0, 64), (4, 1, 64, 64, 0)):
+        assert L.lib.dpclip_ghost_schedule(*args, *[C.byref(x) for x in o]) == L.ERR_INVALID_ARG
+    assert L.lib.dpclip_ghost_schedule(4, 1, 64, 64, 64, None, *[C.byref(x) for x in o[1:]]) == \
+        L.ERR_INVALID_ARG
