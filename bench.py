@@ -59,7 +59,8 @@ L2_BYTES = 129e6
 def time_workload(api, L, W, wid, dev, reps, peaks):
     """Latency of each row a standard workload names.  Workloads whose inputs
     are larger than L2 are timed as the step's rows are: `reps` calls of the
-    row back to back between one event pair.  The others (whose inputs would
+    row back to back between one event pair, the median of three such
+    blocks.  The others (whose inputs would
     stay in L2) one call at a time with a CUDA event pair around it and L2
     flushed before it (a 256 MB write outside the events), median of `reps`.
     Three warm-up calls first.  Returns {workload name: {"rows": ...,
@@ -111,18 +112,19 @@ def time_workload(api, L, W, wid, dev, reps, peaks):
     times = {r: [] for r in rows}
     large = A.numel() * A.element_size() + G.numel() * G.element_size() > L2_BYTES
     if large:
-        timing = f"{reps} calls back to back per row (inputs larger than L2)"
+        timing = f"{reps} calls back to back per row (inputs larger than L2), median of 3 such blocks"
         for r in rows:
             for step in range(3):
                 call(r, step)
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for step in range(reps):
-                call(r, 3 + step)
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            times[r].append(e0.elapsed_time(e1) / reps)
+            for blk in range(3):
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for step in range(reps):
+                    call(r, 3 + step)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                times[r].append(e0.elapsed_time(e1) / reps)
     else:
         timing = f"median of {reps} calls, L2 flushed before each"
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -520,19 +522,24 @@ def main():
     in_step_ms = {r: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1])
                                      for s in range(args.steps))
                   for j, r in enumerate(rows)}
+    # (three such blocks per row, the median kept, so that a stall of the
+    # host or the box during one block does not decide a row's figure)
     row_ms = {}
     for r in rows:
         for s_ in range(3):
             row_fn(r, s_)()
-        barrier()
-        r0 = torch.cuda.Event(enable_timing=True)
-        r1 = torch.cuda.Event(enable_timing=True)
-        r0.record(stream)
-        for s_ in range(args.steps):
-            row_fn(r, args.warmup + s_)()
-        r1.record(stream)
-        barrier()
-        row_ms[r] = r0.elapsed_time(r1) / args.steps
+        blocks = []
+        for b_ in range(3):
+            barrier()
+            r0 = torch.cuda.Event(enable_timing=True)
+            r1 = torch.cuda.Event(enable_timing=True)
+            r0.record(stream)
+            for s_ in range(args.steps):
+                row_fn(r, args.warmup + s_)()
+            r1.record(stream)
+            barrier()
+            blocks.append(r0.elapsed_time(r1) / args.steps)
+        row_ms[r] = statistics.median(blocks)
     for name in rows:
         if name not in ws:
             continue
