@@ -242,9 +242,11 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self, t0: float, t1: float):
+    def stop(self):
+        """Ends sampling; summary() then reads any window of the samples."""
+        self.rows = []
         if self.proc is None:
-            return None
+            return
         time.sleep(0.15)
         self.proc.terminate()
         self.proc.wait()
@@ -262,6 +264,13 @@ class ClockSampler:
                 except (ValueError, IndexError):
                     continue
         os.unlink(self.file.name)
+        self.rows = rows
+
+    def summary(self, t0: float, t1: float):
+        """Median SM clock and the throttle reasons seen between t0 and t1
+        (wall clock), from the samples inside the window, else the two
+        nearest to it."""
+        rows = getattr(self, "rows", [])
         if not rows:
             return None
         inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
@@ -504,12 +513,11 @@ def main():
     end.record(stream)
     barrier()
     wall1 = time.time()
-    clk = clocks.stop(wall0, wall1) if rank == 0 else None
     elapsed_ms = start.elapsed_time(end)
-    # Per-row durations, two ways.  row_ms: each row alone, K calls back to
+    # Per-row durations, two ways.  row_ms: each row alone, calls back to
     # back between one event pair (the steady state of a loop over layers:
     # each call's launch and prologue overlap the previous call's tail; the
-    # inputs are larger than L2).  in_step_ms: a second pass of the step
+    # inputs are larger than L2), see below.  in_step_ms: a second pass of the step
     # with an event pair around every row; an event between two calls keeps
     # the second call's first kernel from launching early, so these rows add
     # up to a little more than the step timed above.
@@ -522,8 +530,12 @@ def main():
     in_step_ms = {r: statistics.mean(ev[s][j].elapsed_time(ev[s][j + 1])
                                      for s in range(args.steps))
                   for j, r in enumerate(rows)}
-    # (three such blocks per row, the median kept, so that a stall of the
-    # host or the box during one block does not decide a row's figure)
+    # Three such blocks per row, the median kept, so that a stall of the host
+    # or the box during one block does not decide a row's figure.  Long runs
+    # of one tensor-bound row can reach the board's power cap (sw_power_cap,
+    # SM clock near 1.84 GHz seen in the ghost row), which the mixed step
+    # does not: clocks_rows records the clocks of these passes, and the
+    # roofline below uses the rows as timed inside the step.
     row_ms = {}
     for r in rows:
         for s_ in range(3):
@@ -540,6 +552,13 @@ def main():
             barrier()
             blocks.append(r0.elapsed_time(r1) / args.steps)
         row_ms[r] = statistics.median(blocks)
+    wall2 = time.time()
+    if rank == 0:
+        clocks.stop()
+    # the step's window, and the window of the rows timed alone (long runs of
+    # one tensor-bound row draw more power than the mixed step)
+    clk = clocks.summary(wall0, wall1) if rank == 0 else None
+    clk_rows = clocks.summary(wall1, wall2) if rank == 0 else None
     for name in rows:
         if name not in ws:
             continue
@@ -684,12 +703,16 @@ def main():
             if r in row_ms:
                 ms = row_ms[r] + row_ms["clipped_noisy_grad"]
                 layer_totals[r + "+grad"] = {"ms": round(ms, 4), "tokens_per_s": B * T / (ms * 1e-3)}
-    dom = max(rows, key=lambda r: row_ms[r])
+    # The dominant row's roofline as it runs inside the step (the second,
+    # event-bracketed pass of the step: same mix and clocks as the timed
+    # region, whose clock record shows full clock and no throttle reason).
+    dom = max(rows, key=lambda r: in_step_ms[r])
     traffic = _traffic_from_profiles(dom)
-    roof = dict(breakdown[dom])
+    roof = row_entry(work[dom], in_step_ms[dom], B * T, peaks)
     roofline = {"kernel": dom, "bound": roof["bound"], "achieved": roof["achieved"],
                 "peak": roof["peak"], "unit": roof["unit"], "frac": roof["frac"],
-                "traffic": traffic, "peak_source": peaks["source"] + (
+                "traffic": traffic, "timing": "inside the step (in_step_ms of the row)",
+                "peak_source": peaks["source"] + (
                     " (burst bf16: a sub-millisecond kernel at full clock)"
                     if roof["unit"] == "TFLOP/s" else " (HBM copy)")}
     if "frac_sustained" in roof:
@@ -701,7 +724,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(wl), "gpu_launches": args.steps * sum(LAUNCHES[r] for r in rows),
             "roofline": roofline, "breakdown": breakdown, "layer_totals": layer_totals,
-            "extra_rows": extra, "configs": per_config, "clocks": clk,
+            "extra_rows": extra, "configs": per_config, "clocks": clk, "clocks_rows": clk_rows,
             "e2e": e2e}
     if world == 1 and not args.no_cpu_baseline:
         # all of sample 0 (its tokens-independent work, the noise and the
