@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
       const uint32_t base = tmem + (uint32_t)half * 128u + ((uint32_t)(quad * 32) << 16);
       // this thread's row of X (shared tail): [unit][rank][row][256 columns]
       const size_t xrow = (((size_t)itm.tu * 2 + rank) * 128 + quad * 32 + lane) * 256 + half * 128;
-      uint32_t* ready = p.xready + ((size_t)itm.tu * 2 + rank) * kEpiWarps + ew;
+      const size_t xflag = ((size_t)itm.tu * 2 + rank) * kEpiWarps + ew;   // its warp's counter
       float s = 0.f;
       if (itm.role == kXOnly) {
         // store X for the Y sub-units of this unit, then release it
@@ -287,10 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1) ghost_kernel(const __grid_constan
         tc_fence_before();
         mbar_arrive_remote(release);
         __syncwarp();
-        if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ready) : "memory");
+        if (lane == 0)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.xready + xflag) : "memory");
       } else {
         if (itm.role == kYOnly) {
-          if (lane == 0) wait_ready(ready, p.err);
+          if (lane == 0) wait_ready(p.xready + xflag, p.err);
           __syncwarp();
         }
         // the accumulators are released only after these loads: one wait
