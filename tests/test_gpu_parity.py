@@ -258,17 +258,18 @@ def test_exact_workload_ghost_vs_direct(api):
 
 
 @pytest.mark.parametrize("B,T,d,p", [(1, 3328, 2048, 4096), (1, 3300, 2040, 4088),
-                                     (1, 4352, 2048, 4096), (2, 2560, 2048, 4096),
-                                     (1, 4096, 1024, 2048)])
+                                     (5, 1500, 2040, 2040), (1, 4352, 2048, 4096),
+                                     (2, 2560, 2048, 4096), (1, 4096, 1024, 2048)])
 def test_ghost_last_round_cuts(api, B, T, d, p):
     # More 256-token units than pairs, so the last round is cut: on 76 pairs
     # (one GB300) the first two shapes leave 15 units whose A Gram block is
     # formed once and shared by two p-slices (the second with a partial
     # token tile, a partial last K-block over d and a shorter second slice),
-    # the third 1 unit cut into 8 slices that each recompute it, the fourth
-    # 34 units cut in two, the fifth 60 whole units.  A unit carries about
-    # 1/100 of a sample's norm, so the check is at 2e-4, against the oracle
-    # and the direct form.
+    # the third 29 such units of two samples (one p-slice each), the fourth
+    # 1 unit cut into 8 slices that each recompute it, the fifth 34 units cut
+    # in two, the sixth 60 whole units.  A unit carries about 1/100 of a
+    # sample's norm (1/21 in the third), so the check is at 2e-4, against the
+    # oracle and the direct form.
     wl = W.Workload(124, f"ghost_cut_{B}_{T}_{d}_{p}", B, T, d, p, "bf16", 1e-2, 1.0, 1.0, 8, ())
     inp = W.make_inputs(wl)
     A, G = to_dev(inp)
