@@ -64,6 +64,14 @@ def test_library_arm_line():
     assert set(line["layer_totals"]) == {"hutch+grad", "hutchpp+grad", "exact_direct+grad",
                                          "exact_ghost+grad"}
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
+    assert "sm_mhz" in line["clocks_rows"] and "reasons" in line["clocks_rows"]
+    # the roofline is the slowest row of the step, as timed inside the step
+    bd = line["breakdown"]
+    dom = max(bd, key=lambda r: bd[r]["in_step_ms"])
+    assert roof["kernel"] == dom and roof["timing"].startswith("inside the step")
+    scale = 1e9 if roof["unit"] == "GB/s" else 1e12
+    ach = bd[dom]["algorithmic"] / (bd[dom]["in_step_ms"] * 1e-3) / scale
+    assert abs(roof["achieved"] - ach) < 1e-3 * ach + 0.01
     # the end-to-end leg moves the inputs in and the results out every step
     assert line["e2e"]["h2d_bytes_per_step"] == 2 * 4 * 4096 * (2048 + 8192)
     assert line["e2e"]["d2h_bytes_per_step"] >= 4 * 2048 * 8192
@@ -78,3 +86,26 @@ def test_library_arm_line():
             assert e["ms"] > 0, (name, r)
             if e["bound"] != "latency":
                 assert 0 < e["frac"] < 1.5, (name, r)
+
+
+def test_clock_summary_windows():
+    """The clock summary keeps the samples inside a window (else the two
+    nearest), reports their median SM clock and every throttle reason seen
+    among them."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler(0)
+    inactive = ["Not Active"] * 5
+    capped = ["Active", "Not Active", "Not Active", "Not Active", "Active"]
+    cs.rows = [(10.0, 2070.0, 2070.0, inactive), (10.1, 2070.0, 2070.0, inactive),
+               (10.2, 2070.0, 2070.0, inactive), (11.0, 1840.0, 2070.0, capped),
+               (11.1, 1830.0, 2070.0, capped), (11.2, 2070.0, 2070.0, inactive)]
+    step = cs.summary(9.95, 10.25)
+    assert step["sm_mhz"] == 2070.0 and step["reasons"] == [] and step["samples_in_window"] == 3
+    rows = cs.summary(10.95, 11.25)
+    assert rows["sm_mhz"] == 1840.0 and rows["reasons"] == ["sw_power_cap"]
+    assert rows["samples_in_window"] == 3
+    outside = cs.summary(20.0, 20.5)
+    assert outside["samples_in_window"] == 0 and outside["samples"] == 2
+    cs.rows = []
+    assert cs.summary(0.0, 1.0) is None
