@@ -351,7 +351,7 @@ T* at(void* ws, size_t off) {
 // ------------------------------------------------------------------ skinny launches
 int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo, int NP,
             bool per_sample, const Plan& pl, void* ws, void* out_hi, void* out_lo,
-            cudaStream_t s) {
+            cudaStream_t s, bool x_stream = false) {
   TokGemmParams tp;
   std::memset(&tp, 0, sizeof(tp));
   const int Bw = per_sample ? B : 1;
@@ -372,6 +372,7 @@ int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo
   tp.kblocks = cdiv(F, kBlockK);
   choose_splits(B * pl.mtiles, tp.kblocks, tp.splits, tp.kb_per_split);
   tp.Tp = pl.Tp;
+  tp.x_stream = x_stream ? 1 : 0;
   tp.out_hi = static_cast<__nv_bfloat16*>(out_hi);
   tp.out_lo = static_cast<__nv_bfloat16*>(out_lo);
   tp.err = at<uint32_t>(ws, pl.ctrl);
@@ -381,7 +382,8 @@ int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo
 
 int run_feat(const void* X, int B, int T, int F, const void* Yhi, const void* Ylo, int NP, int mode,
              const float* w, const Plan& pl, void* ws, size_t qpart_off,
-             float* out_f32, void* out_hi, void* out_lo, float* sq, cudaStream_t s) {
+             float* out_f32, void* out_hi, void* out_lo, float* sq, cudaStream_t s,
+             bool x_stream = false) {
   FeatGemmParams fp;
   std::memset(&fp, 0, sizeof(fp));
   if (!make_map(&fp.map_x, X, F, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
@@ -403,6 +405,7 @@ int run_feat(const void* X, int B, int T, int F, const void* Yhi, const void* Yl
   fp.sq = sq;
   fp.qpart = at<float>(ws, qpart_off);
   fp.counters = at<uint32_t>(ws, pl.ctrl + 4);
+  fp.x_stream = x_stream ? 1 : 0;
   fp.err = at<uint32_t>(ws, pl.ctrl);
   DPCLIP_CUDA(launch_feat_gemm(fp, mode, s));
   return DPCLIP_OK;
@@ -642,13 +645,15 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
     void *Y3h = at<void>(ws, pl.off[kY3hi]), *Y3l = at<void>(ws, pl.off[kY3lo]);
     const size_t qpart = pl.off[kHQpart];
     // sweep 1: Y1 = G S, Z1 = A^T Y1
-    DPCLIP_TRY(run_tok(G, B, T, p, S, nullptr, 16, false, pl, ws, Y1h, Y1l, s));
+    // G is read once per sweep and A in each of the three: G's loads evict
+    // first, so that A (smaller than L2) can stay there between its passes
+    DPCLIP_TRY(run_tok(G, B, T, p, S, nullptr, 16, false, pl, ws, Y1h, Y1l, s, true));
     DPCLIP_TRY(run_feat(A, B, T, d, Y1h, Y1l, 16, kFeatOutHiLo, nullptr, pl, ws, qpart,
                         nullptr, Z1h, Z1l, nullptr, s));
     // sweep 2: U = A Z1, V = G^T U  (= O S)
     DPCLIP_TRY(run_tok(A, B, T, d, Z1h, Z1l, 16, true, pl, ws, Uh, Ul, s));
     DPCLIP_TRY(run_feat(G, B, T, p, Uh, Ul, 16, kFeatOutF32, nullptr, pl, ws, qpart, V,
-                        nullptr, nullptr, nullptr, s));
+                        nullptr, nullptr, nullptr, s, true));
     // Q, W
     HppQrParams hq;
     std::memset(&hq, 0, sizeof(hq));
@@ -665,7 +670,7 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
     hq.err = at<uint32_t>(ws, pl.ctrl);
     DPCLIP_CUDA(launch_hpp_qr(hq, s));
     // sweep 3: Y3 = G [Q | W], head + tail / m from A^T Y3
-    DPCLIP_TRY(run_tok(G, B, T, p, QWh, QWl, 32, true, pl, ws, Y3h, Y3l, s));
+    DPCLIP_TRY(run_tok(G, B, T, p, QWh, QWl, 32, true, pl, ws, Y3h, Y3l, s, true));
     DPCLIP_TRY(run_feat(A, B, T, d, Y3h, Y3l, 32, kFeatSqNorm, w, pl, ws, qpart, nullptr,
                         nullptr, nullptr, sqnorms, s));
     return DPCLIP_OK;

@@ -76,6 +76,7 @@ struct TokGemmParams {
   int B, T, F, NP;
   int w_per_sample, has_lo;
   int mtiles, kblocks, splits, kb_per_split, Tp;
+  int x_stream;          // X is read once: its loads evict first from L2
   __nv_bfloat16* out_hi;
   __nv_bfloat16* out_lo;
   uint32_t* err;
@@ -98,6 +99,7 @@ struct FeatGemmParams {
   float* sq;             // [B] output of the sqnorm mode
   float* qpart;          // [B][ftiles][splits]: each CTA's share of the square sum
   uint32_t* counters;    // [B]: CTAs of the sample done (sqnorm mode)
+  int x_stream;          // X is read once: its loads evict first from L2
   uint32_t* err;
 };
 

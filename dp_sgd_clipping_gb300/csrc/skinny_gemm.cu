@@ -168,11 +168,17 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
   // each tile walks its K-blocks from its own starting point, so that the
   // CTAs in flight spread their row segments over the memory channels
   const int rot = nkb > 0 ? (int)(((unsigned)tile * 5u) % (unsigned)nkb) : 0;
+  const uint64_t xpol = p.x_stream ? l2_evict_first_policy() : 0;
+  auto load_x = [&](int st, int f) {
+    if (p.x_stream)
+      tma_load_3d_hint(sX + st * kXTileBytes, &p.map_x, &ctl->full[st], f, mt * kTokTileM, i, xpol);
+    else
+      tma_load_3d(sX + st * kXTileBytes, &p.map_x, &ctl->full[st], f, mt * kTokTileM, i);
+  };
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < nearly; ++it) {
       mbar_arrive_expect_tx(&ctl->full[it], bytes);
-      tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it],
-                  (kb0 + (it + rot) % nkb) * kBlockK, mt * kTokTileM, i);
+      load_x(it, (kb0 + (it + rot) % nkb) * kBlockK);
     }
   }
   pdl_wait();   // W may come from the previous kernel
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(128, 1) tok_gemm_kernel(const __grid_constant_
       if (it >= nearly) {
         if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(&ctl->full[s], bytes);
-        tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, mt * kTokTileM, i);
+        load_x(s, f0);
       }
       tma_load_3d(sWhi + s * kWBytes, &p.map_whi, &ctl->full[s], f0, 0, wz);
       if (p.has_lo) tma_load_3d(sWlo + s * kWBytes, &p.map_wlo, &ctl->full[s], f0, 0, wz);
@@ -302,12 +308,21 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
 
   const uint32_t bytes = kXTileBytes + 2 * kYBytes;
   const int f0 = ft * kFeatTileM;
+  const uint64_t xpol = p.x_stream ? l2_evict_first_policy() : 0;
+  auto load_x = [&](int st, int t0) {
+    if (p.x_stream) {
+      tma_load_3d_hint(sX + st * kXTileBytes, &p.map_x, &ctl->full[st], f0, t0, i, xpol);
+      tma_load_3d_hint(sX + st * kXTileBytes + kHalf, &p.map_x, &ctl->full[st], f0 + 64, t0, i,
+                       xpol);
+    } else {
+      tma_load_3d(sX + st * kXTileBytes, &p.map_x, &ctl->full[st], f0, t0, i);
+      tma_load_3d(sX + st * kXTileBytes + kHalf, &p.map_x, &ctl->full[st], f0 + 64, t0, i);
+    }
+  };
   if (warp == 0 && lane == 0) {
     for (int it = 0; it < nearly; ++it) {
-      const int t0 = (tb0 + it) * kBlockK;
       mbar_arrive_expect_tx(&ctl->full[it], bytes);
-      tma_load_3d(sX + it * kXTileBytes, &p.map_x, &ctl->full[it], f0, t0, i);
-      tma_load_3d(sX + it * kXTileBytes + kHalf, &p.map_x, &ctl->full[it], f0 + 64, t0, i);
+      load_x(it, (tb0 + it) * kBlockK);
     }
   }
   pdl_wait();   // Y may come from the previous kernel
@@ -321,8 +336,7 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
       if (it >= nearly) {
         if (!mbar_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1, wc)) break;
         mbar_arrive_expect_tx(&ctl->full[s], bytes);
-        tma_load_3d(sX + s * kXTileBytes, &p.map_x, &ctl->full[s], f0, t0, i);
-        tma_load_3d(sX + s * kXTileBytes + kHalf, &p.map_x, &ctl->full[s], f0 + 64, t0, i);
+        load_x(s, t0);
       }
       tma_load_3d(sYhi + s * kYBytes, &p.map_yhi, &ctl->full[s], t0, 0, i);
       tma_load_3d(sYlo + s * kYBytes, &p.map_ylo, &ctl->full[s], t0, 0, i);
