@@ -348,6 +348,27 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// Hutch++'s second pass over G (feature-side, each CTA walking its tokens in
+// order) leaves the last tokens' rows of G in L2 for the third pass when it
+// loads them with the default policy instead of evict-first: as many 64-token
+// blocks as fit in L2 beside A with a 24 MB margin (12 MB measured the same,
+// 40 MB half as good).  Returns the first kept token.
+int hpp_keep_t0(int B, int T, int d, int p) {
+  static int l2 = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      v = 0;
+    return v;
+  }();
+  const double a_bytes = 2.0 * B * T * (double)d;
+  const double room = (double)l2 - a_bytes - 24e6;
+  if (room <= 0) return 1 << 30;
+  const double per_block = 2.0 * B * kBlockK * (double)p;   // one 64-token block of every sample
+  const int blocks = (int)std::min<double>(room / per_block, (double)cdiv(T, kBlockK));
+  return blocks <= 0 ? (1 << 30) : std::max(0, T - blocks * kBlockK);
+}
+
 // ------------------------------------------------------------------ skinny launches
 int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo, int NP,
             bool per_sample, const Plan& pl, void* ws, void* out_hi, void* out_lo,
@@ -383,7 +404,7 @@ int run_tok(const void* X, int B, int T, int F, const void* Whi, const void* Wlo
 int run_feat(const void* X, int B, int T, int F, const void* Yhi, const void* Ylo, int NP, int mode,
              const float* w, const Plan& pl, void* ws, size_t qpart_off,
              float* out_f32, void* out_hi, void* out_lo, float* sq, cudaStream_t s,
-             bool x_stream = false) {
+             bool x_stream = false, int x_keep_t0 = 1 << 30) {
   FeatGemmParams fp;
   std::memset(&fp, 0, sizeof(fp));
   if (!make_map(&fp.map_x, X, F, T, B, kBlockK, kBlockK)) return DPCLIP_ERR_UNSUPPORTED;
@@ -406,6 +427,7 @@ int run_feat(const void* X, int B, int T, int F, const void* Yhi, const void* Yl
   fp.qpart = at<float>(ws, qpart_off);
   fp.counters = at<uint32_t>(ws, pl.ctrl + 4);
   fp.x_stream = x_stream ? 1 : 0;
+  fp.x_keep_t0 = x_keep_t0;
   fp.err = at<uint32_t>(ws, pl.ctrl);
   DPCLIP_CUDA(launch_feat_gemm(fp, mode, s));
   return DPCLIP_OK;
@@ -653,7 +675,7 @@ int dpclip_norms_hutchpp_ex(const void* A, const void* G, int B, int T, int d, i
     // sweep 2: U = A Z1, V = G^T U  (= O S)
     DPCLIP_TRY(run_tok(A, B, T, d, Z1h, Z1l, 16, true, pl, ws, Uh, Ul, s));
     DPCLIP_TRY(run_feat(G, B, T, p, Uh, Ul, 16, kFeatOutF32, nullptr, pl, ws, qpart, V,
-                        nullptr, nullptr, nullptr, s, true));
+                        nullptr, nullptr, nullptr, s, true, hpp_keep_t0(B, T, d, p)));
     // Q, W
     HppQrParams hq;
     std::memset(&hq, 0, sizeof(hq));

@@ -99,7 +99,8 @@ struct FeatGemmParams {
   float* sq;             // [B] output of the sqnorm mode
   float* qpart;          // [B][ftiles][splits]: each CTA's share of the square sum
   uint32_t* counters;    // [B]: CTAs of the sample done (sqnorm mode)
-  int x_stream;          // X is read once: its loads evict first from L2
+  int x_stream;          // X is read once: its loads evict first from L2 ...
+  int x_keep_t0;         // ... except tokens >= x_keep_t0, which the next sweep reads first
   uint32_t* err;
 };
 

@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(128, 1) feat_gemm_kernel(const __grid_constant
   const int f0 = ft * kFeatTileM;
   const uint64_t xpol = p.x_stream ? l2_evict_first_policy() : 0;
   auto load_x = [&](int st, int t0) {
-    if (p.x_stream) {
+    if (p.x_stream && t0 < p.x_keep_t0) {
       tma_load_3d_hint(sX + st * kXTileBytes, &p.map_x, &ctl->full[st], f0, t0, i, xpol);
       tma_load_3d_hint(sX + st * kXTileBytes + kHalf, &p.map_x, &ctl->full[st], f0 + 64, t0, i,
                        xpol);
