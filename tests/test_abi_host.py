@@ -115,6 +115,15 @@ def test_entry_points_reject_before_any_launch(L):
              FAKE, big, None) == L.ERR_INVALID_ARG
     assert g(FAKE, FAKE, 2, 8, 16, 16, L.BF16, FAKE, 1.0, 1.0, 1, 0, None, None, None, FAKE, big,
              None) == L.ERR_INVALID_ARG
+    # sizes past the index ranges: d * p beyond the Philox block index (2^34
+    # elements), B * T beyond 2^30 tokens
+    for B, T, d, p in ((1, 8, 1 << 18, 1 << 17), (1 << 16, 1 << 15, 16, 16)):
+        assert lib.dpclip_norms_exact(FAKE, FAKE, B, T, d, p, L.BF16, 0, FAKE, FAKE, big,
+                                      None) == L.ERR_UNSUPPORTED
+        assert lib.dpclip_norms_hutch(FAKE, FAKE, B, T, d, p, L.BF16, 8, 1, 0, FAKE, FAKE, big,
+                                      None) == L.ERR_UNSUPPORTED
+        assert g(FAKE, FAKE, B, T, d, p, L.BF16, FAKE, 1.0, 1.0, 1, 0, FAKE, None, None, FAKE,
+                 big, None) == L.ERR_UNSUPPORTED
     # non-positive sizes
     for B, T, d, p in ((0, 8, 16, 16), (2, 0, 16, 16), (2, 8, -8, 16), (2, 8, 16, 0)):
         assert lib.dpclip_norms_exact(FAKE, FAKE, B, T, d, p, L.F32, 0, FAKE, FAKE, big,
